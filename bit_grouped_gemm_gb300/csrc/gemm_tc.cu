@@ -1,0 +1,413 @@
+// gemm_tc.cu -- grouped W4A16 expert GEMM on the 5th-generation tensor cores
+// (tcgen05 + TMEM + TMA) for sm_103a.
+//
+// The grouped GEMM with block-wise fused dequantisation of "Perplexity libera
+// Lily, un motor de IA que supera a MLX-LM en Apple Silicon"
+// (diariobitcoin.com), section "Las optimizaciones en el prefill": packed
+// 4-bit weights are rebuilt block by block on chip, the rebuilt values never
+// reach device memory, and products accumulate in FP32. The packed format is
+// the one of section "Qwen3.6 combina tres cargas de trabajo" (groups of 64,
+// one bf16 scale and one bf16 bias per group).
+//
+// GB300 design (not the pages' Metal design):
+//   * the weights are the MMA's M side: a unit is a 128-token tile of one
+//     expert (a block-map tile) times two 128-row weight blocks (gate and up
+//     rows n0..n0+127 for the gate/up pass; rows n0..n0+255 of down for the
+//     down pass), K swept in chunks of 64 (one quantisation group);
+//   * packed weight tiles arrive by TMA (128-byte swizzle) into shared
+//     memory; 8 dequant warps turn each thread's 64 nibbles of one weight row
+//     into bf16 (one fused multiply-add, one rounding) and store them with
+//     tcgen05.st straight into tensor memory, where the MMA reads them as its
+//     A operand -- rebuilt weights never touch shared or global memory;
+//   * token activations (the B operand, N = tile rows rounded up to 16) come
+//     by TMA in the canonical 128-byte-swizzled K-major layout;
+//   * one thread issues tcgen05.mma (M=128, K=16, bf16 in, fp32 in TMEM) for
+//     both weight blocks; 4 epilogue warps read the accumulators back with
+//     tcgen05.ld and apply SwiGLU (gate/up) or the top-k weight (down);
+//   * persistent CTAs (one per SM, 512 TMEM columns each) walk the units;
+//     the number of units is read from device memory, never from the host.
+// Every wait is bounded: on timeout the CTA latches an error, drains its own
+// TMA copies and MMAs, frees TMEM and exits.
+#include "moe_common.cuh"
+
+namespace moe {
+namespace tc {
+
+constexpr int kThreads = 512;
+constexpr int kBStages = 4;               // activation chunks (64 K) in flight
+constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
+constexpr int kAStages = 4;               // TMEM weight stages (64 K)
+constexpr int kBTileBytes = 128 * 128;    // 128 token rows x 64 bf16
+constexpr int kQTileBytes = 128 * 128;    // 128 weight rows x 32 words
+constexpr int kQStageBytes = 2 * kQTileBytes;
+constexpr int kOffB = 0;
+constexpr int kOffQ = kOffB + kBStages * kBTileBytes;
+constexpr int kOffBar = kOffQ + kQStages * kQStageBytes;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kAccCol0 = 0, kAccCol1 = 128, kAStageCol = 256;
+
+struct Params {
+  TcMaps maps;
+  int mode;             // 0: gate/up + SwiGLU, 1: down * top-k weight
+  int T, k, E, K, N;
+  int nblk;             // units per tile
+  int has_shared;
+  const int32_t* bmap;
+  const int32_t* num_tiles;
+  W4Dev w0, w1, sw0, sw1;
+  uint16_t* out;
+  int out_ld;
+  const float* topk_w;
+  const int32_t* perm;
+  DevErr err;
+};
+
+struct Unit {
+  int e, m0, rows, j;
+  bool shared;
+};
+
+__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int n_routed) {
+  Unit r;
+  const int tile = u / p.nblk;
+  r.j = u - tile * p.nblk;
+  if (tile < n_routed) {
+    const int32_t* m = p.bmap + 3 * (size_t)tile;
+    r.e = m[0];
+    r.m0 = m[1];
+    r.rows = m[2];
+    r.shared = false;
+  } else {
+    const int i = tile - n_routed;
+    r.e = 0;
+    r.m0 = p.T * p.k + kBM * i;
+    r.rows = min(kBM, p.T - kBM * i);
+    r.shared = true;
+  }
+  return r;
+}
+
+// first weight row of block `blk` of unit j
+__device__ __forceinline__ int block_row0(const Params& p, int j, int blk) {
+  return p.mode == 0 ? 128 * j : 256 * j + 128 * blk;
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                          const DevErr& err, int site) {
+  bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) {
+    if ((threadIdx.x & 31) == 0 && !*abort_flag) report_timeout(err, site);
+    *abort_flag = 1;
+  }
+  return ok;
+}
+
+__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity,
+                                            volatile int* abort_flag, const DevErr& err,
+                                            int site) {
+  bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
+  if (!ok) {
+    if (!*abort_flag) report_timeout(err, site);
+    *abort_flag = 1;
+  }
+  return ok;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_constant__ Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
+  uint8_t* smem_b = smem + kOffB;
+  uint8_t* smem_q = smem + kOffQ;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* b_full = bars;
+  uint64_t* b_empty = b_full + kBStages;
+  uint64_t* q_full = b_empty + kBStages;
+  uint64_t* q_empty = q_full + kQStages;
+  uint64_t* a_full = q_empty + kQStages;
+  uint64_t* a_empty = a_full + kAStages;
+  uint64_t* acc_full = a_empty + kAStages;
+  uint64_t* acc_empty = acc_full + 1;
+  uint64_t* drain = acc_empty + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kBStages; ++i) {
+      mbar_init(&b_full[i], 1);
+      mbar_init(&b_empty[i], 1);
+    }
+    for (int i = 0; i < kQStages; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 8);
+    }
+    for (int i = 0; i < kAStages; ++i) {
+      mbar_init(&a_full[i], 8);
+      mbar_init(&a_empty[i], 1);
+    }
+    mbar_init(acc_full, 1);
+    mbar_init(acc_empty, 4);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&p.maps.b);
+    tma_prefetch_desc(&p.maps.q0);
+    tma_prefetch_desc(&p.maps.q1);
+    if (p.has_shared) {
+      tma_prefetch_desc(&p.maps.sq0);
+      tma_prefetch_desc(&p.maps.sq1);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  const int n_routed = *p.num_tiles;
+  const int n_shared = p.has_shared ? (p.T + kBM - 1) / kBM : 0;
+  const int units = (n_routed + n_shared) * p.nblk;
+  const int nchunk = p.K / 64;
+  const int kgroups = p.K / 64;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t bcnt = 0, qcnt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u, n_routed);
+        const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
+        const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
+        const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
+        const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
+        for (int c = 0; c < nchunk && ok; ++c) {
+          if ((c & 3) == 0) {
+            const int s = qcnt % kQStages;
+            if (!(ok = thread_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1)))
+              break;
+            mbar_arrive_expect_tx(&q_full[s], kQStageBytes);
+            tma_load_2d(smem_q + s * kQStageBytes, m0, 32 * (c >> 2), y0, &q_full[s]);
+            tma_load_2d(smem_q + s * kQStageBytes + kQTileBytes, m1, 32 * (c >> 2), y1, &q_full[s]);
+            ++qcnt;
+          }
+          const int s = bcnt % kBStages;
+          if (!(ok = thread_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2)))
+            break;
+          mbar_arrive_expect_tx(&b_full[s], kBTileBytes);
+          tma_load_2d(smem_b + s * kBTileBytes, &p.maps.b, 64 * c, U.m0, &b_full[s]);
+          ++bcnt;
+        }
+      }
+      if (!ok) {
+        // let this CTA's own copies land before shared memory is released
+        for (int s = 0; s < kBStages; ++s) {
+          uint32_t uses = (bcnt + kBStages - 1 - s) / kBStages;
+          if (uses) mbar_wait_drain(&b_full[s], (uses - 1) & 1, p.err.limit_ns);
+        }
+        for (int s = 0; s < kQStages; ++s) {
+          uint32_t uses = (qcnt + kQStages - 1 - s) / kQStages;
+          if (uses) mbar_wait_drain(&q_full[s], (uses - 1) & 1, p.err.limit_ns);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      uint32_t bcnt = 0, acnt = 0, it = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+        const Unit U = decode_unit(p, u, n_routed);
+        const int ntok = (U.rows + 15) & ~15;
+        const uint32_t idesc = idesc_bf16_f32(128, ntok);
+        if (!(ok = thread_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3))) break;
+        tc_fence_after();
+        for (int c = 0; c < nchunk; ++c) {
+          const int bs = bcnt % kBStages, as = acnt % kAStages;
+          if (!(ok = thread_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4))) break;
+          if (!(ok = thread_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5))) break;
+          tc_fence_after();
+          const uint32_t bbase = smem_u32(smem_b + bs * kBTileBytes);
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            const uint64_t bd = smem_desc_sw128(bbase + 32 * kk);
+            const uint32_t a0 = tmem + kAStageCol + 64 * as + 8 * kk;
+            const uint32_t acc = (c | kk) != 0;
+            mma_bf16_ts(tmem + kAccCol0, a0, bd, idesc, acc);
+            mma_bf16_ts(tmem + kAccCol1, a0 + 32, bd, idesc, acc);
+          }
+          mma_commit(&b_empty[bs]);
+          mma_commit(&a_empty[as]);
+          ++bcnt;
+          ++acnt;
+        }
+        if (!ok) break;
+        mma_commit(acc_full);
+      }
+      // all MMAs of this thread complete before TMEM is released
+      mma_commit(drain);
+      mbar_wait_drain(drain, 0, p.err.limit_ns);
+    }
+  } else if (warp >= 4 && warp < 12) {
+    // ------------------------------------------------------ dequant warps
+    const int blk = (warp - 4) >> 2;
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    uint32_t qcnt = 0, acnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit U = decode_unit(p, u, n_routed);
+      const W4Dev& w = U.shared ? (blk == 0 ? p.sw0 : p.sw1) : (blk == 0 ? p.w0 : p.w1);
+      const size_t row = (U.shared ? 0 : (size_t)U.e * p.N) + block_row0(p, U.j, blk) + r;
+      const uint16_t* srow = w.s + row * kgroups;
+      const uint16_t* brow = w.b + row * kgroups;
+      uint2 s4 = __ldg(reinterpret_cast<const uint2*>(srow));
+      uint2 b4 = __ldg(reinterpret_cast<const uint2*>(brow));
+      for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
+        uint2 s4n = s4, b4n = b4;
+        if (qc + 1 < nchunk / 4) {
+          s4n = __ldg(reinterpret_cast<const uint2*>(srow + 4 * (qc + 1)));
+          b4n = __ldg(reinterpret_cast<const uint2*>(brow + 4 * (qc + 1)));
+        }
+        const int qs = qcnt % kQStages;
+        if (!(ok = warp_wait(&q_full[qs], (qcnt / kQStages) & 1, abort_flag, p.err, 6))) break;
+        const uint8_t* qrow = smem_q + qs * kQStageBytes + blk * kQTileBytes + r * 128;
+        const uint32_t sw = r & 7;
+#pragma unroll
+        for (int sub = 0; sub < 4; ++sub) {
+          const int as = acnt % kAStages;
+          if (!(ok = warp_wait(&a_empty[as], ((acnt / kAStages) & 1) ^ 1, abort_flag, p.err, 7)))
+            break;
+          tc_fence_after();
+          const uint4 wa = *reinterpret_cast<const uint4*>(qrow + (((2 * sub) ^ sw) << 4));
+          const uint4 wb = *reinterpret_cast<const uint4*>(qrow + (((2 * sub + 1) ^ sw) << 4));
+          const uint32_t sbits = (sub & 1) ? (((sub >> 1) ? s4.y : s4.x) >> 16)
+                                           : (((sub >> 1) ? s4.y : s4.x) & 0xFFFFu);
+          const uint32_t bbits = (sub & 1) ? (((sub >> 1) ? b4.y : b4.x) >> 16)
+                                           : (((sub >> 1) ? b4.y : b4.x) & 0xFFFFu);
+          const uint32_t s2u = sbits | (sbits << 16), b2u = bbits | (bbits << 16);
+          const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
+          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
+          uint32_t out[32];
+          const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t o4[4];
+            dequant_word_bf16(words[i], s2, b2, o4);
+            out[4 * i + 0] = o4[0];
+            out[4 * i + 1] = o4[1];
+            out[4 * i + 2] = o4[2];
+            out[4 * i + 3] = o4[3];
+          }
+          tmem_st_32x32b_x32(tmem + lane_base + kAStageCol + 64 * as + 32 * blk, out);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&a_full[as]);
+          ++acnt;
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&q_empty[qs]);
+        ++qcnt;
+        s4 = s4n;
+        b4 = b4n;
+      }
+    }
+  } else if (warp >= 12) {
+    // ------------------------------------------------------ epilogue warps
+    const int quarter = warp & 3;
+    const int r = 32 * quarter + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    uint32_t it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+      const Unit U = decode_unit(p, u, n_routed);
+      if (!(ok = warp_wait(acc_full, it & 1, abort_flag, p.err, 8))) break;
+      tc_fence_after();
+      for (int c0 = 0; c0 < U.rows; c0 += 32) {
+        uint32_t v0[32], v1[32];
+        tmem_ld_32x32b_x32(tmem + lane_base + kAccCol0 + c0, v0);
+        tmem_ld_32x32b_x32(tmem + lane_base + kAccCol1 + c0, v1);
+        tmem_wait_ld();
+        const int nval = min(32, U.rows - c0);
+        if (p.mode == 0) {
+          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + r;
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            if (cc < nval) {
+              const float g = __uint_as_float(v0[cc]);
+              const float uu = __uint_as_float(v1[cc]);
+              o[(size_t)cc * p.out_ld] = f32_to_bf16(silu_f32(g) * uu);
+            }
+          }
+        } else {
+          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + r;
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            if (cc < nval) {
+              const int pos = U.m0 + c0 + cc;
+              const float wt = U.shared ? 1.0f : __ldg(p.topk_w + __ldg(p.perm + pos));
+              o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * wt);
+              o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * wt);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace tc
+
+cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, DevErr err,
+                           int num_sms, cudaStream_t st) {
+  tc::Params p;
+  p.maps = maps;
+  p.mode = mode;
+  p.T = g.T;
+  p.k = g.k;
+  p.E = g.E;
+  p.K = g.K;
+  p.N = g.N;
+  p.nblk = mode == 0 ? g.N / 128 : g.N / 256;
+  p.has_shared = g.has_shared;
+  p.bmap = g.bmap;
+  p.num_tiles = g.num_tiles;
+  p.w0 = g.w0;
+  p.w1 = g.w1;
+  p.sw0 = g.sw0;
+  p.sw1 = g.sw1;
+  p.out = g.out;
+  p.out_ld = g.out_ld;
+  p.topk_w = g.topk_w;
+  p.perm = g.perm;
+  p.err = err;
+  const int max_units = (g.max_routed_tiles + (g.has_shared ? (g.T + kBM - 1) / kBM : 0)) * p.nblk;
+  int grid = num_sms < max_units ? num_sms : max_units;
+  if (grid < 1) grid = 1;
+  cudaError_t e = cudaFuncSetAttribute(tc::w4_grouped_gemm_tc,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  tc::w4_grouped_gemm_tc<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

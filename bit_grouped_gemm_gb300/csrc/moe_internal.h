@@ -1,0 +1,79 @@
+// moe_internal.h -- declarations shared by the library's .cu files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe_w4.h"
+
+namespace moe {
+
+constexpr int kBM = 128;          // rows per block-map tile
+constexpr int kRouterTB = 32;     // tokens per router / scatter block
+constexpr int kGroup = 64;        // quantisation group
+
+// Device error state: plain pointers, usable on host and device.
+struct DevErr {
+  int* word;                      // error bits (DEVERR_*)
+  int* where;                     // first failing site code
+  unsigned long long limit_ns;    // bounded-wait limit
+};
+
+struct W4Dev {                    // one matrix set (device pointers)
+  const uint32_t* q;
+  const uint16_t* s;
+  const uint16_t* b;
+};
+
+// -------------------------------------------------------------- routing ---
+cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
+                               const float* bias, int E, int k, int32_t* topk_idx,
+                               float* topk_w, float* logits, int32_t* blk_cnt,
+                               cudaStream_t st);
+cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E,
+                              int32_t* cnt, int32_t* off, int32_t* tile_off, int32_t* bmap,
+                              int32_t* num_tiles, cudaStream_t st);
+cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off, int T, int k,
+                                 int E, int32_t* perm, int32_t* inv, cudaStream_t st);
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
+                               int with_shared, uint16_t* xs, cudaStream_t st);
+cudaError_t launch_combine(const uint16_t* d, const int32_t* inv, int T, int k, int H,
+                           int with_shared, uint16_t* y, cudaStream_t st);
+cudaError_t launch_residual(const uint16_t* x, const uint16_t* y, long long n, float alpha,
+                            uint16_t* out, cudaStream_t st);
+cudaError_t launch_debug_wait(DevErr e, cudaStream_t st);
+
+// ---------------------------------------------------------------- GEMMs ---
+// Problem of one grouped GEMM launch (gate/up + SwiGLU, or down + weight).
+struct GemmProblem {
+  int T, k, E;
+  int K;                    // reduction size (gate/up: H, down: I)
+  int N;                    // weight rows per expert (gate/up: I, down: H)
+  int has_shared;
+  const int32_t* bmap;      // routed block map [tiles][3]
+  const int32_t* num_tiles; // device count of routed tiles
+  int max_routed_tiles;     // host upper bound (grid sizing)
+  const uint16_t* act_in;   // B operand rows [rows][K] bf16 (xs or act)
+  uint16_t* out;            // output rows [rows][out_ld] bf16
+  int out_ld;
+  const float* topk_w;      // down: per-slot weights (by slot)
+  const int32_t* perm;      // down: position -> slot
+  W4Dev w0, w1;             // routed: gate,up (mode 0) or down,down (mode 1)
+  W4Dev sw0, sw1;           // shared expert, same roles
+};
+
+// tcgen05 tensor-core path. `maps` holds the encoded tensor maps the kernel
+// needs (B operand, routed q for w0/w1, shared q for sw0/sw1).
+struct TcMaps {
+  CUtensorMap b;            // act_in, bf16 [rows][K], box 64 x 128, swizzle 128B
+  CUtensorMap q0, q1;       // routed q of w0/w1, uint32 [E*N][K/8], box 32 x 128
+  CUtensorMap sq0, sq1;     // shared q
+};
+cudaError_t launch_gemm_tc(int mode, const GemmProblem& p, const TcMaps& maps, DevErr err,
+                           int num_sms, cudaStream_t st);
+
+// small-M mma.sync path (decode-sized token groups).
+cudaError_t launch_gemm_smallm(int mode, const GemmProblem& p, cudaStream_t st);
+
+}  // namespace moe

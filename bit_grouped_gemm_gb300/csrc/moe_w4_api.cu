@@ -1,0 +1,547 @@
+// moe_w4_api.cu -- the C ABI of include/moe_w4.h: plan (scratch) management,
+// host-side argument checks, tensor-map encoding and the launch sequence of
+// one MoE layer (router+top-k, scan+block map, scatter, gather, gate/up GEMM,
+// down GEMM, combine), all on the caller's stream with no host sync.
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+struct TimedLaunch {
+  int kind;
+  cudaEvent_t a, b;
+};
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Layout {                 // byte offsets into the scratch allocation
+  size_t topk_idx, topk_w, logits, blk_cnt, cnt, off, tile_off, num_tiles, perm, inv, bmap,
+      err, xs, act, d, total;
+  int nblk_max, max_tiles, rows_cap;
+};
+
+Layout make_layout(const moe_plan_desc& d) {
+  Layout L;
+  const size_t Tm = (size_t)d.max_tokens, k = (size_t)d.top_k, E = (size_t)d.num_experts;
+  L.nblk_max = (int)((Tm + kRouterTB - 1) / kRouterTB);
+  L.max_tiles = (int)((Tm * k + kBM - 1) / kBM + E);
+  L.rows_cap = (int)(Tm * k + (d.has_shared ? Tm : 0));
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = o;
+    o = align_up(o + bytes, 256);
+    return r;
+  };
+  L.topk_idx = take(Tm * k * 4);
+  L.topk_w = take(Tm * k * 4);
+  L.logits = take(Tm * E * 4);
+  L.blk_cnt = take((size_t)L.nblk_max * E * 4);
+  L.cnt = take(E * 4);
+  L.off = take((E + 1) * 4);
+  L.tile_off = take((E + 1) * 4);
+  L.num_tiles = take(16);
+  L.perm = take(Tm * k * 4);
+  L.inv = take(Tm * k * 4);
+  L.bmap = take((size_t)L.max_tiles * 3 * 4);
+  L.err = take(16);
+  L.xs = take((size_t)L.rows_cap * d.hidden * 2);
+  L.act = take((size_t)L.rows_cap * d.inter * 2);
+  L.d = take((size_t)L.rows_cap * d.hidden * 2);
+  L.total = o;
+  return L;
+}
+
+moe_status check_desc(const moe_plan_desc* d) {
+  if (!d) return MOE_ERR_INVALID_ARG;
+  if (d->hidden <= 0 || d->inter <= 0 || d->num_experts <= 0 || d->top_k <= 0 ||
+      d->max_tokens <= 0)
+    return MOE_ERR_INVALID_ARG;
+  if (d->group_size != kGroup) return MOE_ERR_UNSUPPORTED;
+  if (d->block_m != kBM) return MOE_ERR_UNSUPPORTED;
+  if (d->hidden % d->group_size || d->inter % d->group_size) return MOE_ERR_INVALID_ARG;
+  if (d->hidden % 256 || d->inter % 256) return MOE_ERR_UNSUPPORTED;
+  if (d->num_experts % 8 || d->num_experts > 512) return MOE_ERR_UNSUPPORTED;
+  if (d->top_k > d->num_experts) return MOE_ERR_INVALID_ARG;
+  if (d->top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (d->gemm_path < 0 || d->gemm_path > 2) return MOE_ERR_INVALID_ARG;
+  if (d->small_m_max_tokens < 0 || d->wait_limit_ms < 0) return MOE_ERR_INVALID_ARG;
+  // 32-bit row/element indices inside the kernels
+  if ((long long)d->max_tokens * (d->top_k + 1) * d->hidden >= (1LL << 31))
+    return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+// 2D row-major tensor map: `rows` x `cols` elements, box `box_cols` x `box_rows`,
+// 128-byte swizzle (box_cols * elem == 128).
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+               uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+struct moe_plan {
+  moe_plan_desc d;
+  int device = 0;
+  int num_sms = 0;
+  Layout L;
+  uint8_t* scratch = nullptr;
+  CUtensorMap tm_xs, tm_act;
+  bool timing = false;
+  std::vector<TimedLaunch> timed;
+  std::vector<cudaEvent_t> ev_pool;
+  int last_path = 0;
+
+  template <class T>
+  T* at(size_t off) const {
+    return reinterpret_cast<T*>(scratch + off);
+  }
+  DevErr err() const {
+    DevErr e;
+    e.word = at<int>(L.err);
+    e.where = at<int>(L.err) + 1;
+    e.limit_ns = (unsigned long long)(d.wait_limit_ms > 0 ? d.wait_limit_ms : 1000) * 1000000ull;
+    return e;
+  }
+  cudaEvent_t event() {
+    if (!ev_pool.empty()) {
+      cudaEvent_t e = ev_pool.back();
+      ev_pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+};
+
+namespace {
+
+// Runs one launch; when timing is on, brackets it with events on `st`.
+template <class F>
+cudaError_t timed(moe_plan* p, int kind, cudaStream_t st, F&& launch) {
+  if (!p->timing) return launch();
+  TimedLaunch t{kind, p->event(), p->event()};
+  cudaEventRecord(t.a, st);
+  cudaError_t e = launch();
+  cudaEventRecord(t.b, st);
+  p->timed.push_back(t);
+  return e;
+}
+
+moe_status st_of(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+moe_status check_w4(const moe_w4& m) {
+  if (!m.qweight || !m.scales || !m.biases) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(m.qweight) || !aligned16(m.scales) || !aligned16(m.biases))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_experts(const moe_experts* x) {
+  if (!x) return MOE_ERR_INVALID_ARG;
+  moe_status s;
+  if ((s = check_w4(x->gate)) != MOE_OK) return s;
+  if ((s = check_w4(x->up)) != MOE_OK) return s;
+  return check_w4(x->down);
+}
+
+W4Dev dev(const moe_w4& m) { return W4Dev{m.qweight, m.scales, m.biases}; }
+
+moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* router_w,
+                      const float* router_bias, moe_routing* out, bool want_logits,
+                      cudaStream_t st) {
+  const moe_plan_desc& d = p->d;
+  const int nblk = (T + kRouterTB - 1) / kRouterTB;
+  float* logits = want_logits ? p->at<float>(p->L.logits) : nullptr;
+  cudaError_t e;
+  e = timed(p, 0, st, [&] {
+    return launch_router_topk(x, T, d.hidden, router_w, router_bias, d.num_experts, d.top_k,
+                              p->at<int32_t>(p->L.topk_idx), p->at<float>(p->L.topk_w), logits,
+                              p->at<int32_t>(p->L.blk_cnt), st);
+  });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = timed(p, 1, st, [&] {
+    return launch_route_scan(p->at<int32_t>(p->L.blk_cnt), nblk, T, d.top_k, d.num_experts,
+                             p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
+                             p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
+                             p->at<int32_t>(p->L.num_tiles), st);
+  });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = timed(p, 2, st, [&] {
+    return launch_route_scatter(p->at<int32_t>(p->L.topk_idx), p->at<int32_t>(p->L.blk_cnt), T,
+                                d.top_k, d.num_experts, p->at<int32_t>(p->L.perm),
+                                p->at<int32_t>(p->L.inv), st);
+  });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (out) {
+    out->topk_idx = p->at<int32_t>(p->L.topk_idx);
+    out->topk_w = p->at<float>(p->L.topk_w);
+    out->counts = p->at<int32_t>(p->L.cnt);
+    out->offsets = p->at<int32_t>(p->L.off);
+    out->tile_offsets = p->at<int32_t>(p->L.tile_off);
+    out->perm = p->at<int32_t>(p->L.perm);
+    out->inv = p->at<int32_t>(p->L.inv);
+    out->block_map = p->at<int32_t>(p->L.bmap);
+    out->num_tiles = p->at<int32_t>(p->L.num_tiles);
+    out->logits = logits;
+  }
+  return MOE_OK;
+}
+
+moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
+                    const moe_experts* routed, const moe_experts* shared, uint16_t* y,
+                    cudaStream_t st) {
+  const moe_plan_desc& d = p->d;
+  const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
+  const int hs = d.has_shared;
+  const int small_max = d.small_m_max_tokens > 0 ? d.small_m_max_tokens : 16;
+  const int path = d.gemm_path != 0 ? d.gemm_path : (T <= small_max ? 2 : 1);
+  p->last_path = path;
+
+  cudaError_t e = timed(p, 3, st, [&] {
+    return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), st);
+  });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
+  long long bound = ((long long)T * k + kBM - 1) / kBM + E;
+  if (bound > (long long)T * k) bound = (long long)T * k;
+
+  GemmProblem g{};
+  g.T = T;
+  g.k = k;
+  g.E = E;
+  g.has_shared = hs;
+  g.bmap = r->block_map;
+  g.num_tiles = r->num_tiles;
+  g.max_routed_tiles = (int)bound;
+  g.topk_w = r->topk_w;
+  g.perm = r->perm;
+
+  // gate/up: B = xs [rows][H], out = act [rows][I]
+  GemmProblem g0 = g;
+  g0.K = H;
+  g0.N = I;
+  g0.act_in = p->at<uint16_t>(p->L.xs);
+  g0.out = p->at<uint16_t>(p->L.act);
+  g0.out_ld = I;
+  g0.w0 = dev(routed->gate);
+  g0.w1 = dev(routed->up);
+  if (hs) {
+    g0.sw0 = dev(shared->gate);
+    g0.sw1 = dev(shared->up);
+  }
+  // down: B = act [rows][I], out = d [rows][H]
+  GemmProblem g1 = g;
+  g1.K = I;
+  g1.N = H;
+  g1.act_in = p->at<uint16_t>(p->L.act);
+  g1.out = p->at<uint16_t>(p->L.d);
+  g1.out_ld = H;
+  g1.w0 = dev(routed->down);
+  g1.w1 = dev(routed->down);
+  if (hs) {
+    g1.sw0 = dev(shared->down);
+    g1.sw1 = dev(shared->down);
+  }
+
+  if (path == 1) {
+    TcMaps m0{}, m1{};
+    m0.b = p->tm_xs;
+    m1.b = p->tm_act;
+    const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
+    bool ok = encode_2d(&m0.q0, U32, 4, routed->gate.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
+              encode_2d(&m0.q1, U32, 4, routed->up.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
+              encode_2d(&m1.q0, U32, 4, routed->down.qweight, (uint64_t)E * H, I / 8, 32, 128);
+    m1.q1 = m1.q0;
+    if (ok && hs) {
+      ok = encode_2d(&m0.sq0, U32, 4, shared->gate.qweight, I, H / 8, 32, 128) &&
+           encode_2d(&m0.sq1, U32, 4, shared->up.qweight, I, H / 8, 32, 128) &&
+           encode_2d(&m1.sq0, U32, 4, shared->down.qweight, H, I / 8, 32, 128);
+      m1.sq1 = m1.sq0;
+    } else if (ok) {
+      m0.sq0 = m0.q0;
+      m0.sq1 = m0.q1;
+      m1.sq0 = m1.sq1 = m1.q0;
+    }
+    if (!ok) return MOE_ERR_CUDA;
+    e = timed(p, 4, st, [&] { return launch_gemm_tc(0, g0, m0, p->err(), p->num_sms, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 5, st, [&] { return launch_gemm_tc(1, g1, m1, p->err(), p->num_sms, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    e = timed(p, 4, st, [&] { return launch_gemm_smallm(0, g0, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 5, st, [&] { return launch_gemm_smallm(1, g1, st); });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  e = timed(p, 6, st, [&] {
+    return launch_combine(p->at<uint16_t>(p->L.d), r->inv, T, k, H, hs, y, st);
+  });
+  return st_of(e);
+}
+
+moe_status check_T(const moe_plan* p, int T) {
+  if (T < 1) return MOE_ERR_INVALID_ARG;
+  if (T > p->d.max_tokens) return MOE_ERR_CAPACITY;
+  return MOE_OK;
+}
+
+moe_status check_route_args(const moe_plan* p, const uint16_t* x, int T, const uint16_t* rw,
+                            const float* rb) {
+  moe_status s = check_T(p, T);
+  if (s != MOE_OK) return s;
+  if (!x || !rw || !aligned16(x) || !aligned16(rw)) return MOE_ERR_INVALID_ARG;
+  if (rb && (reinterpret_cast<uintptr_t>(rb) & 3u)) return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+moe_status check_ffn_args(const moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
+                          const moe_experts* routed, const moe_experts* shared,
+                          const uint16_t* y) {
+  moe_status s = check_T(p, T);
+  if (s != MOE_OK) return s;
+  if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
+  const size_t bytes = (size_t)T * p->d.hidden * 2;
+  const uint8_t* xb = reinterpret_cast<const uint8_t*>(x);
+  const uint8_t* yb = reinterpret_cast<const uint8_t*>(y);
+  if (xb < yb + bytes && yb < xb + bytes) return MOE_ERR_INVALID_ARG;   // y overlaps x
+  if ((s = check_experts(routed)) != MOE_OK) return s;
+  if (p->d.has_shared) {
+    if ((s = check_experts(shared)) != MOE_OK) return s;
+  } else if (shared) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  if (r && (!r->topk_w || !r->perm || !r->inv || !r->block_map || !r->num_tiles))
+    return MOE_ERR_INVALID_ARG;
+  return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status moe_plan_scratch_bytes(const moe_plan_desc* desc, size_t* bytes) {
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (!bytes) return MOE_ERR_INVALID_ARG;
+  *bytes = make_layout(*desc).total;
+  return MOE_OK;
+}
+
+moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* out) {
+  if (!out) return MOE_ERR_INVALID_ARG;
+  *out = nullptr;
+  moe_status s = check_desc(desc);
+  if (s != MOE_OK) return s;
+  if (device < 0) return MOE_ERR_INVALID_ARG;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device >= ndev) return MOE_ERR_CUDA;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  if (cudaSetDevice(device) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MOE_ERR_CUDA;
+  if (prop.major != 10 || prop.minor != 3) {   // kernels are built for sm_103a only
+    cudaSetDevice(prev);
+    return MOE_ERR_UNSUPPORTED;
+  }
+  moe_plan* p = new moe_plan();
+  p->d = *desc;
+  p->device = device;
+  p->num_sms = prop.multiProcessorCount;
+  p->L = make_layout(*desc);
+  if (cudaMalloc(&p->scratch, p->L.total) != cudaSuccess) {
+    delete p;
+    cudaSetDevice(prev);
+    return MOE_ERR_CUDA;
+  }
+  cudaMemset(p->scratch + p->L.err, 0, 16);
+  bool ok = encode_2d(&p->tm_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->at<uint16_t>(p->L.xs),
+                      p->L.rows_cap, desc->hidden, 64, 128) &&
+            encode_2d(&p->tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                      p->at<uint16_t>(p->L.act), p->L.rows_cap, desc->inter, 64, 128);
+  if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
+    cudaFree(p->scratch);
+    delete p;
+    cudaSetDevice(prev);
+    return MOE_ERR_CUDA;
+  }
+  cudaSetDevice(prev);
+  *out = p;
+  return MOE_OK;
+}
+
+moe_status moe_plan_destroy(moe_plan_t p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(p->device);
+  cudaDeviceSynchronize();
+  for (auto& t : p->timed) {
+    cudaEventDestroy(t.a);
+    cudaEventDestroy(t.b);
+  }
+  for (auto e : p->ev_pool) cudaEventDestroy(e);
+  cudaFree(p->scratch);
+  cudaSetDevice(prev);
+  delete p;
+  return MOE_OK;
+}
+
+moe_status moe_route(moe_plan_t p, const uint16_t* x, int T, const uint16_t* router_w,
+                     const float* router_bias, moe_routing* out, moe_stream_t stream) {
+  if (!p || !out) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_route_args(p, x, T, router_w, router_bias);
+  if (s != MOE_OK) return s;
+  return route_impl(p, x, T, router_w, router_bias, out, true,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_grouped_w4_ffn(moe_plan_t p, const uint16_t* x, int T, const moe_routing* r,
+                              const moe_experts* routed, const moe_experts* shared, uint16_t* y,
+                              moe_stream_t stream) {
+  if (!p || !r) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_ffn_args(p, x, T, r, routed, shared, y);
+  if (s != MOE_OK) return s;
+  return ffn_impl(p, x, T, r, routed, shared, y, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint16_t* router_w,
+                             const float* router_bias, const moe_experts* routed,
+                             const moe_experts* shared, uint16_t* y, moe_stream_t stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_route_args(p, x, T, router_w, router_bias);
+  if (s != MOE_OK) return s;
+  s = check_ffn_args(p, x, T, nullptr, routed, shared, y);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  moe_routing r;
+  s = route_impl(p, x, T, router_w, router_bias, &r, false, st);
+  if (s != MOE_OK) return s;
+  return ffn_impl(p, x, T, &r, routed, shared, y, st);
+}
+
+moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const uint16_t* y, int T,
+                            float alpha, uint16_t* x_out, moe_stream_t stream) {
+  if (!p || !x || !y || !x_out) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_T(p, T);
+  if (s != MOE_OK) return s;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(x_out)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  return st_of(timed(p, 7, st, [&] {
+    return launch_residual(x, y, (long long)T * p->d.hidden, alpha, x_out, st);
+  }));
+}
+
+moe_status moe_get_error(moe_plan_t p) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(p->device);
+  int h[2] = {0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(h, p->at<int>(p->L.err), 8, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(p->at<int>(p->L.err), 0, 8);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  cudaSetDevice(prev);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (h[0] & 1) return MOE_ERR_DEVICE_TIMEOUT;
+  return MOE_OK;
+}
+
+moe_status moe_debug_wait_timeout(moe_plan_t p, int limit_us, moe_stream_t stream) {
+  if (!p || limit_us <= 0 || limit_us > 10000000) return MOE_ERR_INVALID_ARG;
+  DevErr e = p->err();
+  e.limit_ns = (unsigned long long)limit_us * 1000ull;
+  return st_of(launch_debug_wait(e, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_enable_timing(moe_plan_t p, int on) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  p->timing = on != 0;
+  return MOE_OK;
+}
+
+moe_status moe_read_timing(moe_plan_t p, moe_timing* out) {
+  if (!p || !out) return MOE_ERR_INVALID_ARG;
+  memset(out, 0, sizeof(*out));
+  moe_status s = MOE_OK;
+  for (auto& t : p->timed) {
+    if (cudaEventSynchronize(t.b) != cudaSuccess) s = MOE_ERR_CUDA;
+    float ms = 0.f;
+    if (s == MOE_OK && cudaEventElapsedTime(&ms, t.a, t.b) == cudaSuccess) {
+      out->ms[t.kind] += ms;
+      out->launches[t.kind] += 1;
+    }
+    p->ev_pool.push_back(t.a);
+    p->ev_pool.push_back(t.b);
+  }
+  p->timed.clear();
+  return s;
+}
+
+int moe_last_gemm_path(moe_plan_t p) { return p ? p->last_path : 0; }
+
+void* moe_debug_buffer(moe_plan_t p, int which) {
+  if (!p) return nullptr;
+  switch (which) {
+    case 0: return p->scratch + p->L.xs;
+    case 1: return p->scratch + p->L.act;
+    case 2: return p->scratch + p->L.d;
+  }
+  return nullptr;
+}
+
+const char* moe_status_string(moe_status s) {
+  switch (s) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_CAPACITY: return "T above plan capacity";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device bounded wait timed out";
+  }
+  return "unknown status";
+}
+
+int moe_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,499 @@
+// route_kernels.cu -- GPU-resident routing of the MoE block and the small
+// elementwise kernels around the grouped GEMMs.
+//
+// Routing follows "Perplexity libera Lily, un motor de IA que supera a MLX-LM
+// en Apple Silicon" (diariobitcoin.com): section "Qwen3.6 combina tres cargas
+// de trabajo" (router scores 256 experts, picks 8) and section "Las
+// optimizaciones en el prefill" (histogram, prefix scan, scatter and block
+// map kept on the GPU with no CPU synchronisation). Every step here is
+// deterministic: counts are per token block, ranks inside an expert follow
+// token order, and no result depends on atomic ordering.
+#include <cuda_pipeline.h>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Router logits + top-k + per-block histogram.
+//
+// One CTA = 32 tokens, 8 warps. Logits are a bf16 [32 x H] x [H x E] product
+// on mma.sync m16n8k16 (FP32 accumulate); warp w owns experts
+// [8*TPW*w, 8*TPW*(w+1)). Then each warp selects the top k of 4 tokens by k
+// rounds of a warp arg-max (higher logit first, lower index on ties), and the
+// block writes its per-expert counts to blk_cnt[block][E].
+// ---------------------------------------------------------------------------
+constexpr int kRtK = 32;          // K chunk staged per step
+constexpr int kRtXStride = kRtK + 8;
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                          uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src, int src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src),
+               "r"(src_bytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int TPW>  // n8 tiles per warp (E <= 64 * TPW)
+__global__ void __launch_bounds__(256) router_topk_kernel(
+    const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
+    const float* __restrict__ bias, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, float* __restrict__ logits_out, int32_t* __restrict__ blk_cnt) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int wstride = E + 8;                                       // bf16 elements
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);              // [2][32][40]
+  uint16_t* wr_s = xs_s + 2 * kRouterTB * kRtXStride;              // [2][32][E+8]
+  float* lg_s = reinterpret_cast<float*>(smem);                    // reused: [32][E+1]
+  __shared__ int cnt_s[1024];
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kRouterTB;
+  const int ntiles = E / 8;
+
+  auto stage = [&](int buf, int kc) {
+    const int k0 = kc * kRtK;
+    // x: 32 rows x 32 cols = 128 chunks of 16 B
+    if (tid < kRouterTB * 4) {
+      int r = tid >> 2, c = (tid & 3) * 8;
+      int t = t0 + r;
+      const uint16_t* src = x + (size_t)(t < T ? t : 0) * H + k0 + c;
+      cp_async16(xs_s + (buf * kRouterTB + r) * kRtXStride + c, src, t < T ? 16 : 0);
+    }
+    // Wr: 32 rows x E cols
+    const int chunks_per_row = E / 8;
+    for (int i = tid; i < kRtK * chunks_per_row; i += 256) {
+      int r = i / chunks_per_row, c = (i % chunks_per_row) * 8;
+      cp_async16(wr_s + (buf * kRtK + r) * wstride + c, wr + (size_t)(k0 + r) * E + c, 16);
+    }
+    cp_async_commit();
+  };
+
+  for (int i = tid; i < E; i += 256) cnt_s[i] = 0;
+
+  float acc[2][TPW][4];
+#pragma unroll
+  for (int m = 0; m < 2; ++m)
+#pragma unroll
+    for (int n = 0; n < TPW; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[m][n][i] = 0.f;
+
+  const int nk = H / kRtK;
+  const int tile0 = warp * TPW;
+  stage(0, 0);
+  for (int kc = 0; kc < nk; ++kc) {
+    const int buf = kc & 1;
+    if (kc + 1 < nk) {
+      stage(buf ^ 1, kc + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    if (tile0 < ntiles) {
+#pragma unroll
+      for (int ks = 0; ks < kRtK / 16; ++ks) {
+        uint32_t a[2][4];
+#pragma unroll
+        for (int m = 0; m < 2; ++m) {
+          int row = m * 16 + (lane & 15);
+          int col = ks * 16 + (lane >> 4) * 8;
+          ldsm_x4(smem_u32(xs_s + (buf * kRouterTB + row) * kRtXStride + col), a[m][0], a[m][1],
+                  a[m][2], a[m][3]);
+        }
+#pragma unroll
+        for (int np = 0; np < TPW / 2; ++np) {
+          int nt = tile0 + 2 * np;
+          if (nt < ntiles) {
+            // lanes 0-15: k rows 0..15 of tile nt; lanes 16-31: same rows, tile nt+1
+            int krow = ks * 16 + (lane & 15);
+            int ncol = (nt + (lane >> 4)) * 8;
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(smem_u32(wr_s + (buf * kRtK + krow) * wstride + ncol), b0, b1, b2, b3);
+#pragma unroll
+            for (int m = 0; m < 2; ++m) {
+              mma_16816(acc[m][2 * np], a[m][0], a[m][1], a[m][2], a[m][3], b0, b1);
+              mma_16816(acc[m][2 * np + 1], a[m][0], a[m][1], a[m][2], a[m][3], b2, b3);
+            }
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  // logits (+ bias) to shared memory
+  const int lstride = E + 1;
+  {
+    const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int n = 0; n < TPW; ++n) {
+        int nt = tile0 + n;
+        if (nt < ntiles) {
+          int e0 = nt * 8 + 2 * c;
+          float b0 = bias ? bias[e0] : 0.f, b1 = bias ? bias[e0 + 1] : 0.f;
+          int r0 = m * 16 + g;
+          lg_s[r0 * lstride + e0] = acc[m][n][0] + b0;
+          lg_s[r0 * lstride + e0 + 1] = acc[m][n][1] + b1;
+          lg_s[(r0 + 8) * lstride + e0] = acc[m][n][2] + b0;
+          lg_s[(r0 + 8) * lstride + e0 + 1] = acc[m][n][3] + b1;
+        }
+      }
+  }
+  __syncthreads();
+
+  // top-k: warp w handles local tokens w, w+8, w+16, w+24
+  constexpr int VPL = TPW * 8 * 8 / 32 > 0 ? TPW * 2 : 1;   // values per lane (E <= 64*TPW)
+  for (int tl = warp; tl < kRouterTB; tl += 8) {
+    const int t = t0 + tl;
+    if (t >= T) break;
+    float v[VPL];
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      int e = lane + 32 * i;
+      v[i] = e < E ? lg_s[tl * lstride + e] : -INFINITY;
+    }
+    if (logits_out) {
+      for (int e = lane; e < E; e += 32) logits_out[(size_t)t * E + e] = lg_s[tl * lstride + e];
+    }
+    float sel_v0 = 0.f, my_w = 0.f, zsum = 0.f;
+    int my_idx = 0;
+    float my_val = 0.f;
+    for (int j = 0; j < k; ++j) {
+      // best of this lane: highest value, lowest index (i ascending -> e ascending)
+      float bv = -INFINITY;
+      int be = 0x7fffffff;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        int e = lane + 32 * i;
+        if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
+          bv = v[i];
+          be = e;
+        }
+      }
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) {
+        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (ov > bv || (ov == bv && oe < be)) {
+          bv = ov;
+          be = oe;
+        }
+      }
+      if ((be & 31) == lane) v[be >> 5] = -INFINITY;   // mark taken (owner lane)
+      if (j == 0) sel_v0 = bv;
+      float p = expf(bv - sel_v0);
+      zsum += p;
+      if (lane == j) {
+        my_idx = be;
+        my_val = p;
+      }
+    }
+    if (lane < k) {
+      my_w = my_val / zsum;
+      topk_idx[(size_t)t * k + lane] = my_idx;
+      topk_w[(size_t)t * k + lane] = my_w;
+      atomicAdd(&cnt_s[my_idx], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < E; e += 256) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
+}
+
+cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
+                               const float* bias, int E, int k, int32_t* topk_idx,
+                               float* topk_w, float* logits, int32_t* blk_cnt,
+                               cudaStream_t st) {
+  const int nblk = (T + kRouterTB - 1) / kRouterTB;
+  size_t stage_bytes = (size_t)2 * kRouterTB * kRtXStride * 2 + (size_t)2 * kRtK * (E + 8) * 2;
+  size_t logit_bytes = (size_t)kRouterTB * (E + 1) * 4;
+  size_t smem = stage_bytes > logit_bytes ? stage_bytes : logit_bytes;
+  if (E <= 256) {
+    auto kern = router_topk_kernel<4>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<nblk, 256, smem, st>>>(x, T, H, wr, bias, E, k, topk_idx, topk_w, logits, blk_cnt);
+  } else {
+    auto kern = router_topk_kernel<8>;
+    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<nblk, 256, smem, st>>>(x, T, H, wr, bias, E, k, topk_idx, topk_w, logits, blk_cnt);
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Prefix scans and block map (one CTA, one thread per expert).
+//   blk_cnt[b][e] -> exclusive offset of block b inside expert e's segment
+//   cnt[e], off[e] = sum_{e'<e} cnt[e'], tile_off[e] = sum_{e'<e} ceil(cnt/BM)
+//   bmap[tile] = (e, off[e] + BM*i, min(BM, cnt[e] - BM*i))
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ int block_excl_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int ws = lane < nw ? warp_sums[lane] : 0;
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_sums[lane] = wi - ws;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  int r = inc - v + warp_sums[warp];
+  __syncthreads();
+  return r;
+}
+
+__global__ void route_scan_kernel(int32_t* __restrict__ blk_cnt, int nblk, int T, int k, int E,
+                                  int32_t* __restrict__ cnt, int32_t* __restrict__ off,
+                                  int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
+                                  int32_t* __restrict__ num_tiles) {
+  __shared__ int warp_sums[32];
+  __shared__ int tot_rows, tot_tiles;
+  const int e = threadIdx.x;
+  const bool valid = e < E;
+  int total = 0;
+  if (valid) {
+    for (int b = 0; b < nblk; ++b) {
+      int c = blk_cnt[(size_t)b * E + e];
+      blk_cnt[(size_t)b * E + e] = total;
+      total += c;
+    }
+  }
+  int tiles = valid ? (total + kBM - 1) / kBM : 0;
+  int o = block_excl_scan(valid ? total : 0, warp_sums, &tot_rows);
+  int to = block_excl_scan(tiles, warp_sums, &tot_tiles);
+  if (valid) {
+    cnt[e] = total;
+    off[e] = o;
+    tile_off[e] = to;
+    for (int b = 0; b < nblk; ++b) blk_cnt[(size_t)b * E + e] += o;
+    for (int i = 0; i < tiles; ++i) {
+      int rows = total - kBM * i;
+      int32_t* m = bmap + 3 * (size_t)(to + i);
+      m[0] = e;
+      m[1] = o + kBM * i;
+      m[2] = rows < kBM ? rows : kBM;
+    }
+  }
+  if (threadIdx.x == 0) {
+    off[E] = tot_rows;
+    tile_off[E] = tot_tiles;
+    num_tiles[0] = tot_tiles;
+  }
+}
+
+cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E, int32_t* cnt,
+                              int32_t* off, int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
+                              cudaStream_t st) {
+  int threads = ((E + 31) / 32) * 32;
+  route_scan_kernel<<<1, threads, 0, st>>>(blk_cnt, nblk, T, k, E, cnt, off, tile_off, bmap,
+                                           num_tiles);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Stable scatter: slot s = t*k + j of block b goes to
+//   pos = blk_off[b][e] + #{t' < t in block b : token t' selected e}
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) route_scatter_kernel(
+    const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_off, int T, int k,
+    int E, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  __shared__ int idx_s[kRouterTB * 32];
+  const int t0 = blockIdx.x * kRouterTB;
+  const int nt = min(kRouterTB, T - t0);
+  const int nslots = nt * k;
+  for (int i = threadIdx.x; i < nslots; i += blockDim.x) idx_s[i] = topk_idx[(size_t)t0 * k + i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < nslots; i += blockDim.x) {
+    const int tl = i / k;
+    const int e = idx_s[i];
+    int rank = 0;
+    for (int s = 0; s < tl * k; ++s) rank += (idx_s[s] == e);
+    const int pos = blk_off[(size_t)blockIdx.x * E + e] + rank;
+    const int slot = t0 * k + i;
+    perm[pos] = slot;
+    inv[slot] = pos;
+  }
+}
+
+cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off, int T, int k,
+                                 int E, int32_t* perm, int32_t* inv, cudaStream_t st) {
+  const int nblk = (T + kRouterTB - 1) / kRouterTB;
+  route_scatter_kernel<<<nblk, 256, 0, st>>>(topk_idx, blk_off, T, k, E, perm, inv);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Gather: xs[pos] = x[perm[pos] / k] for routed positions, and
+// xs[T*k + t] = x[t] for the shared expert's rows. One warp per row.
+// ---------------------------------------------------------------------------
+__global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
+                                   int T, int k, int H, int with_shared,
+                                   uint16_t* __restrict__ xs) {
+  const int rows = T * k + (with_shared ? T : 0);
+  const int lane = threadIdx.x & 31;
+  const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int vec = H / 8;   // 16-byte vectors per row
+  for (int r = wid; r < rows; r += nw) {
+    const int src = r < T * k ? perm[r] / k : r - T * k;
+    const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)src * H);
+    uint4* d = reinterpret_cast<uint4*>(xs + (size_t)r * H);
+    for (int i = lane; i < vec; i += 32) d[i] = __ldg(s + i);
+  }
+}
+
+cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
+                               int with_shared, uint16_t* xs, cudaStream_t st) {
+  const int rows = T * k + (with_shared ? T : 0);
+  int blocks = (rows + 7) / 8;
+  if (blocks > 4096) blocks = 4096;
+  gather_rows_kernel<<<blocks, 256, 0, st>>>(x, perm, T, k, H, with_shared, xs);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Combine: y[t] = d[T*k + t] + sum_j d[inv[t*k + j]] (rows of d already carry
+// their top-k weight), FP32 in fixed order (shared, then j = 0..k-1), one
+// rounding to bf16.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ d,
+                                                      const int32_t* __restrict__ inv, int T,
+                                                      int k, int H, int with_shared,
+                                                      uint16_t* __restrict__ y) {
+  __shared__ int rows_s[33];
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < k) rows_s[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+    __syncthreads();
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      if (with_shared) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(d + (size_t)(T * k + t) * H + h0));
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += bf16_lo(w[i]);
+          acc[2 * i + 1] += bf16_hi(w[i]);
+        }
+      }
+      for (int j = 0; j < k; ++j) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(d + (size_t)rows_s[j] * H + h0));
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += bf16_lo(w[i]);
+          acc[2 * i + 1] += bf16_hi(w[i]);
+        }
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ow[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+      *reinterpret_cast<uint4*>(y + (size_t)t * H + h0) = o;
+    }
+  }
+}
+
+cudaError_t launch_combine(const uint16_t* d, const int32_t* inv, int T, int k, int H,
+                           int with_shared, uint16_t* y, cudaStream_t st) {
+  int blocks = T < 4096 ? T : 4096;
+  combine_kernel<<<blocks, 256, 0, st>>>(d, inv, T, k, H, with_shared, y);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Residual: out = bf16(x + alpha * y), 8 elements per thread.
+// ---------------------------------------------------------------------------
+__global__ void residual_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y,
+                                long long n8, float alpha, uint16_t* __restrict__ out) {
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
+       i += (long long)gridDim.x * blockDim.x) {
+    uint4 a = reinterpret_cast<const uint4*>(x)[i];
+    uint4 b = reinterpret_cast<const uint4*>(y)[i];
+    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+    const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
+    uint4 o;
+    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+      ow[j] = pack_bf16x2(fmaf(alpha, bf16_lo(bw[j]), bf16_lo(aw[j])),
+                          fmaf(alpha, bf16_hi(bw[j]), bf16_hi(aw[j])));
+    reinterpret_cast<uint4*>(out)[i] = o;
+  }
+}
+
+cudaError_t launch_residual(const uint16_t* x, const uint16_t* y, long long n, float alpha,
+                            uint16_t* out, cudaStream_t st) {
+  long long n8 = n / 8;
+  long long blocks = (n8 + 255) / 256;
+  if (blocks > 4096) blocks = 4096;
+  if (blocks < 1) blocks = 1;
+  residual_kernel<<<(int)blocks, 256, 0, st>>>(x, y, n8, alpha, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Failure-path check: wait on an mbarrier nobody arrives on; the bounded wait
+// must give up, latch the timeout bit and return.
+// ---------------------------------------------------------------------------
+__global__ void debug_wait_kernel(DevErr err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, &abort_flag, err.limit_ns)) report_timeout(err, 99);
+  }
+}
+
+cudaError_t launch_debug_wait(DevErr e, cudaStream_t st) {
+  debug_wait_kernel<<<1, 32, 0, st>>>(e);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,208 @@
+/*
+ * moe_w4.h -- C ABI of the GB300 (sm_103a) W4A16 mixture-of-experts block.
+ *
+ * The block is the expert layer of a Qwen3.6-35B-A3B-style model as described
+ * in "Perplexity libera Lily, un motor de IA que supera a MLX-LM en Apple
+ * Silicon" (diariobitcoin.com):
+ *   - section "Qwen3.6 combina tres cargas de trabajo": a router scores all E
+ *     (256) experts and selects k (8) per token; one shared expert processes
+ *     every token; weights are 4-bit affine with groups of 64, one bfloat16
+ *     scale and one bfloat16 bias per group;
+ *   - section "Las optimizaciones en el prefill": the grouped GEMM rebuilds
+ *     weights block by block on chip and accumulates in FP32 (the dequantised
+ *     array never exists in memory), and the routing histogram, prefix scan,
+ *     scatter and block map stay on the GPU with no CPU synchronisation
+ *     inside a layer.
+ *
+ * Conventions for every call:
+ *   - All tensor arguments are DEVICE pointers owned by the caller, on the
+ *     plan's device, 16-byte aligned. bf16 tensors are passed as uint16_t bit
+ *     patterns. The library never frees or keeps caller memory past a call.
+ *   - A plan owns only its device scratch, allocated once in moe_plan_create
+ *     and sized for max_tokens.
+ *   - Calls are stream-ordered and asynchronous: they enqueue kernels on
+ *     `stream` (NULL = legacy default stream) and never wait for the device.
+ *     Grid sizes never depend on routing results, so no value is read back.
+ *   - Argument errors are found on the host before any launch and returned as
+ *     a status; nothing is enqueued then. Errors found on the device (a
+ *     bounded wait that ran out) are latched in a device word and reported by
+ *     moe_get_error.
+ *   - A plan is not thread-safe: calls on one plan must come from one host
+ *     thread at a time, and calls that share a plan's scratch must be ordered
+ *     on the device (same stream, or explicit events).
+ */
+#ifndef MOE_W4_H
+#define MOE_W4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* cudaStream_t compatible handle, so this header needs no CUDA headers */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,    /* null/misaligned pointer, bad size, bad field */
+  MOE_ERR_UNSUPPORTED = 2,    /* valid request this build has no kernel for */
+  MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
+  MOE_ERR_CAPACITY = 4,       /* T above the plan's max_tokens */
+  MOE_ERR_DEVICE_TIMEOUT = 5  /* a device-side bounded wait ran out */
+} moe_status;
+
+/* Plan description. Sizes are in elements. */
+typedef struct {
+  int hidden;            /* H: model width (2048); multiple of group_size */
+  int inter;             /* I: expert FFN width (512); multiple of group_size */
+  int num_experts;       /* E: routed experts (256); 8..512, multiple of 8 */
+  int top_k;             /* k: experts per token (8); 1..min(E, 32) */
+  int group_size;        /* G: quantisation group along K; must be 64 */
+  int has_shared;        /* 1: one always-on shared expert with weight 1 */
+  int max_tokens;        /* capacity: scratch is sized for this T, once */
+  int block_m;           /* rows per block-map tile; must be 128 */
+  int gemm_path;         /* 0 auto, 1 tensor-core (tcgen05) path, 2 small-M path */
+  int small_m_max_tokens;/* auto: T <= this uses the small-M path (default 16 if 0) */
+  int wait_limit_ms;     /* device bounded-wait limit (default 1000 if 0) */
+} moe_plan_desc;
+
+typedef struct moe_plan* moe_plan_t;
+
+/* One 4-bit affine matrix set for E experts, N output rows, K inputs.
+ * Weight W[e][n][kk] = q * scale[e][n][kk/64] + bias[e][n][kk/64] where q is
+ * nibble (kk % 8) -- bits 4*(kk%8) .. 4*(kk%8)+3 -- of qweight[e][n][kk/8],
+ * read as an unsigned integer 0..15. */
+typedef struct {
+  const uint32_t* qweight;   /* [E][N][K/8] */
+  const uint16_t* scales;    /* [E][N][K/64] bf16 */
+  const uint16_t* biases;    /* [E][N][K/64] bf16 */
+} moe_w4;
+
+/* SwiGLU expert set: gate and up are N = inter, K = hidden; down is
+ * N = hidden, K = inter. An expert computes
+ *   a[n] = silu(sum_k x[k] Wg[n][k]) * sum_k x[k] Wu[n][k],
+ *   out[m] = sum_n a[n] Wd[m][n]. */
+typedef struct {
+  moe_w4 gate, up, down;
+} moe_experts;
+
+/* Routing result. moe_route fills this with pointers into plan scratch that
+ * stay valid until the next moe_route / moe_forward_layer on the plan. A
+ * caller may also point it at its own device buffers with these layouts
+ * (slot s = t*k + j, position = row in expert-contiguous order):
+ *   topk_idx     int32 [T][k]  selected experts, rank order (logit desc,
+ *                              lower index first on ties)
+ *   topk_w       f32   [T][k]  softmax over all E, renormalised over the k
+ *   counts       int32 [E]     histogram of selected experts
+ *   offsets      int32 [E+1]   exclusive prefix scan of counts; [E] = T*k
+ *   tile_offsets int32 [E+1]   exclusive scan of ceil(counts/block_m)
+ *   perm         int32 [T*k]   position -> slot, stable in token order
+ *   inv          int32 [T*k]   slot -> position
+ *   block_map    int32 [tiles][3] (expert, first position, rows) per tile,
+ *                              expert-major; shared-expert tiles excluded
+ *   num_tiles    int32 [1]     number of block_map tiles
+ *   logits       f32   [T][E]  router logits (moe_route only; may be NULL
+ *                              when the struct is given to
+ *                              moe_grouped_w4_ffn) */
+typedef struct {
+  int32_t* topk_idx;
+  float* topk_w;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* tile_offsets;
+  int32_t* perm;
+  int32_t* inv;
+  int32_t* block_map;
+  int32_t* num_tiles;
+  float* logits;
+} moe_routing;
+
+/* Create a plan on CUDA device `device`: validates `desc` (host only; no
+ * CUDA call is made when it is invalid) and allocates the scratch. */
+moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* out);
+
+/* Free the plan and its scratch. Waits for the device to finish using it. */
+moe_status moe_plan_destroy(moe_plan_t plan);
+
+/* Bytes of device scratch a plan with this description allocates (host only). */
+moe_status moe_plan_scratch_bytes(const moe_plan_desc* desc, size_t* bytes);
+
+/* Routing (histogram, prefix scan, scatter and block map in section "Las
+ * optimizaciones en el prefill"; router and top-8 in section "Qwen3.6
+ * combina tres cargas de trabajo"):
+ *   logits[t][e] = sum_h x[t][h] * router_w[h][e] + router_bias[e]  (FP32)
+ * then top-k, weights, counts, offsets, tile offsets, perm, inv, block map.
+ * x: bf16 [T][H]; router_w: bf16 [H][E]; router_bias: f32 [E] or NULL.
+ * `out` receives pointers into plan scratch. 1 <= T <= max_tokens. */
+moe_status moe_route(moe_plan_t plan, const uint16_t* x, int T, const uint16_t* router_w,
+                     const float* router_bias, moe_routing* out, moe_stream_t stream);
+
+/* Experts on a given routing (the grouped GEMM with block-wise dequant in
+ * section "Las optimizaciones en el prefill"):
+ *   y[t] = shared(x[t]) + sum_j topk_w[t][j] * expert_{topk_idx[t][j]}(x[t])
+ * x: bf16 [T][H]; routing: as moe_route produces (topk_w, perm, inv,
+ * block_map and num_tiles are read); routed: E experts; shared: one expert
+ * set with E = 1, or NULL (must be non-NULL iff desc.has_shared);
+ * y: bf16 [T][H], must not overlap x. Dequantised weights exist only in
+ * on-chip memory; accumulation is FP32. */
+moe_status moe_grouped_w4_ffn(moe_plan_t plan, const uint16_t* x, int T,
+                              const moe_routing* routing, const moe_experts* routed,
+                              const moe_experts* shared, uint16_t* y, moe_stream_t stream);
+
+/* moe_route followed by moe_grouped_w4_ffn: one MoE layer, no host sync. */
+moe_status moe_forward_layer(moe_plan_t plan, const uint16_t* x, int T,
+                             const uint16_t* router_w, const float* router_bias,
+                             const moe_experts* routed, const moe_experts* shared,
+                             uint16_t* y, moe_stream_t stream);
+
+/* Residual update between stacked layers: x_out[i] = bf16(x[i] + alpha*y[i])
+ * over T*H elements, FP32 arithmetic. x_out may equal x. */
+moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const uint16_t* y, int T,
+                            float alpha, uint16_t* x_out, moe_stream_t stream);
+
+/* Reads and clears the plan's device error word. Synchronises the device:
+ * call it between layers or steps, never inside one. Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA if the context has failed. */
+moe_status moe_get_error(moe_plan_t plan);
+
+/* Launch a kernel whose bounded wait can never be satisfied, with the given
+ * limit: it must give up, latch MOE_ERR_DEVICE_TIMEOUT and exit. Lets a test
+ * check the failure path without faulting or hanging the GPU. */
+moe_status moe_debug_wait_timeout(moe_plan_t plan, int limit_us, moe_stream_t stream);
+
+/* Kernel timing for profiling. When enabled, every kernel the plan launches
+ * is bracketed by CUDA events on its stream. moe_read_timing synchronises,
+ * adds up the elapsed times per kernel kind since the last read, and resets.
+ * Kinds: 0 router, 1 scan, 2 scatter, 3 gather, 4 gate/up GEMM, 5 down GEMM,
+ * 6 combine, 7 residual. */
+#define MOE_NUM_KERNEL_KINDS 8
+typedef struct {
+  double ms[MOE_NUM_KERNEL_KINDS];
+  long long launches[MOE_NUM_KERNEL_KINDS];
+} moe_timing;
+moe_status moe_enable_timing(moe_plan_t plan, int on);
+moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
+
+/* Introspection of plan scratch for tests and profiling: device address of
+ * the gathered activations (which = 0: bf16 [rows][H], routed positions
+ * first, then the shared expert's T rows), the SwiGLU activations (1: bf16
+ * [rows][I]) or the weighted expert outputs (2: bf16 [rows][H]) of the last
+ * layer. NULL for an unknown `which`. */
+void* moe_debug_buffer(moe_plan_t plan, int which);
+
+/* Which GEMM path the last moe_grouped_w4_ffn took: 1 tensor-core, 2 small-M. */
+int moe_last_gemm_path(moe_plan_t plan);
+
+/* Text of a status code. */
+const char* moe_status_string(moe_status s);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W4_H */

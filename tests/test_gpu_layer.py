@@ -1,0 +1,254 @@
+"""GPU parity of one MoE layer against the fp64 oracle, through the C ABI.
+
+Routing arrays must match bit for bit (inputs drawn so every token's 8th/9th
+logit gap is >= 1e-3); top-k weights within 1e-5; outputs within
+max|y_gpu - y_oracle| <= 2e-2 * rms(y_oracle).
+"""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_grouped_gemm_gb300 import binding as bg
+from bit_grouped_gemm_gb300 import stack, synth
+from tests import parity
+from tests.oracle_pins import check_route_invariants
+
+pytestmark = pytest.mark.gpu
+
+NTHREADS = os.cpu_count() or 4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bit_grouped_gemm_gb300 import build
+    build.build()
+    bg.load_library()
+
+
+class Case:
+    """One layer on the GPU plus its host copies for the oracle."""
+
+    def __init__(self, w: synth.Workload, layer: int = 0, gap: bool = True):
+        self.w = w
+        sh = w.shape
+        self.L = stack.make_layer(w, layer, "cuda")
+        self.x = synth.tokens_x(w, "cuda")
+        if gap:
+            parity.enforce_gap(w, self.x, self.L.router_w, self.L.router_bias, sh.top_k)
+        self.xh = parity.bits(self.x)
+        self.wr = parity.bits(self.L.router_w)
+        self.rb = None if self.L.router_bias is None else self.L.router_bias.cpu().numpy()
+        self.routed = parity.host_set(self.L.routed)
+        self.shared = parity.host_set(self.L.shared) if self.L.shared is not None else None
+
+    def oracle_route(self):
+        orc = oracle.get()
+        sh = self.w.shape
+        logits = orc.router_logits(self.xh, self.wr, self.rb)
+        idx, w, gap = orc.topk(logits, sh.top_k)
+        maps = orc.route_maps(idx, sh.num_experts, 128)
+        return logits, idx, w, gap, maps
+
+    def oracle_layer(self, rows=None):
+        sh = self.w.shape
+        return oracle.get().moe_rows(self.xh, self.wr, self.rb, self.routed, self.shared,
+                                     sh.top_k, sh.group_size, rows=rows, nthreads=NTHREADS)
+
+
+def make_plan(w: synth.Workload, gemm_path=0, max_tokens=None):
+    sh = w.shape
+    d = bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k, sh.group_size,
+                     int(sh.has_shared), max_tokens or w.tokens, 128, gemm_path)
+    return bg.moe_plan_create(d, 0)
+
+
+WL = synth.standard_workloads()
+SMALL = synth.MoEShape(hidden=256, inter=256, num_experts=16, top_k=4)
+
+
+@pytest.mark.parametrize("name", ["t128_uniform", "t512_zipf", "t2048_uniform", "t2048_zipf"])
+def test_route_bit_exact(name):
+    w = WL[name]
+    c = Case(w)
+    plan = make_plan(w)
+    try:
+        r = bg.moe_route(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias)
+        g = parity.routing_to_numpy(r, w.tokens, w.shape.top_k, w.shape.num_experts)
+        logits, idx, wts, gap, maps = c.oracle_route()
+        assert gap.min() >= parity.GAP_MIN
+        np.testing.assert_allclose(g["logits"], logits, rtol=0, atol=1e-4)
+        assert np.array_equal(g["topk_idx"], idx)
+        assert np.abs(g["topk_w"] - wts).max() <= parity.W_TOL
+        assert np.abs(g["topk_w"].sum(axis=1) - 1).max() <= 1e-6
+        for key in ("counts", "offsets", "tile_offsets", "perm", "inv", "block_map"):
+            assert np.array_equal(g[key], maps[key]), key
+        assert g["num_tiles"] == maps["num_tiles"]
+        check_route_invariants(g, g["topk_idx"], w.shape.num_experts, 128)
+        if w.routing == "zipf":
+            assert g["counts"].max() > 4 * g["counts"].mean()    # skewed groups
+            assert (g["counts"] == 0).any()
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def run_layer(c: Case, plan: int):
+    w = c.w
+    y = torch.empty_like(c.x)
+    bg.moe_forward_layer(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias, c.L.routed_c,
+                         c.L.shared_c, y)
+    torch.cuda.synchronize()
+    assert bg.moe_get_error(plan) == 0
+    return y
+
+
+LAYER_CASES = [
+    ("t128_uniform", 1), ("t128_uniform", 2), ("t512_zipf", 0), ("t512_zipf", 2),
+]
+
+
+@pytest.mark.parametrize("name,path", LAYER_CASES)
+def test_layer_parity_full(name, path):
+    w = WL[name]
+    c = Case(w)
+    plan = make_plan(w, path)
+    try:
+        y = run_layer(c, plan)
+        assert bg.moe_last_gemm_path(plan) == (path if path else 1)
+        orc = c.oracle_layer()
+        parity.check_y(parity.bf16_f64(parity.bits(y)), orc["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("name", ["t2048_uniform", "t2048_zipf"])
+def test_layer_parity_sampled(name):
+    w = WL[name]
+    c = Case(w)
+    plan = make_plan(w)
+    try:
+        y = run_layer(c, plan)
+        rng = np.random.default_rng(0)
+        rows = np.sort(rng.choice(w.tokens, size=96, replace=False)).astype(np.int32)
+        orc = c.oracle_layer(rows)
+        parity.check_y(parity.bf16_f64(parity.bits(y))[rows], orc["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+@pytest.mark.parametrize("path", [0, 1])
+def test_decode_sized_layer(T, path):
+    w = dataclasses.replace(WL["decode_t8_l40"], tokens=T, layers=1)
+    c = Case(w)
+    plan = make_plan(w, path)
+    try:
+        y = run_layer(c, plan)
+        assert bg.moe_last_gemm_path(plan) == (path if path else 2)
+        parity.check_y(parity.bf16_f64(parity.bits(y)), c.oracle_layer()["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T,shared,path,routing", [
+    (37, True, 1, "zipf"), (37, True, 2, "zipf"), (300, False, 1, "uniform"),
+    (300, False, 2, "uniform"), (129, True, 0, "zipf"),
+])
+def test_small_shapes_ragged(T, shared, path, routing):
+    sh = dataclasses.replace(SMALL, has_shared=shared)
+    w = synth.Workload(f"small{T}", T, 1, routing, seed=77 + T, shape=sh)
+    c = Case(w)
+    plan = make_plan(w, path)
+    try:
+        r = bg.moe_route(plan, c.x, T, c.L.router_w, c.L.router_bias)
+        g = parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)
+        _, idx, _, _, maps = c.oracle_route()
+        assert np.array_equal(g["topk_idx"], idx)
+        assert np.array_equal(g["perm"], maps["perm"])
+        assert np.array_equal(g["block_map"], maps["block_map"])
+        y = run_layer(c, plan)
+        parity.check_y(parity.bf16_f64(parity.bits(y)), c.oracle_layer()["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def test_ffn_on_caller_routing():
+    # moe_grouped_w4_ffn on a routing the caller supplies (the oracle's)
+    w = WL["t128_uniform"]
+    c = Case(w)
+    sh = w.shape
+    _, idx, wts, _, maps = c.oracle_route()
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).cuda()
+    bufs = dict(topk_idx=dev(idx.astype(np.int32)), topk_w=dev(wts.astype(np.float32)),
+                counts=dev(maps["counts"]), offsets=dev(maps["offsets"]),
+                tile_offsets=dev(maps["tile_offsets"]), perm=dev(maps["perm"]),
+                inv=dev(maps["inv"]), block_map=dev(maps["block_map"].reshape(-1)),
+                num_tiles=dev(np.array([maps["num_tiles"]], np.int32)))
+    r = bg.MoeRouting(**{k: v.data_ptr() for k, v in bufs.items()}, logits=None)
+    plan = make_plan(w)
+    try:
+        y = torch.empty_like(c.x)
+        bg.moe_grouped_w4_ffn(plan, c.x, w.tokens, r, c.L.routed_c, c.L.shared_c, y)
+        torch.cuda.synchronize()
+        parity.check_y(parity.bf16_f64(parity.bits(y)), c.oracle_layer()["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+def test_deterministic(path):
+    w = WL["t512_zipf"]
+    c = Case(w, gap=False)
+    plan = make_plan(w, path)
+    try:
+        y1 = run_layer(c, plan).clone()
+        a1 = parity.bits(y1)
+        y2 = run_layer(c, plan)
+        assert np.array_equal(a1, parity.bits(y2))
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def test_device_timeout_is_reported_and_context_survives():
+    w = WL["t128_uniform"]
+    plan = make_plan(w)
+    try:
+        assert bg.moe_get_error(plan) == 0
+        bg.moe_debug_wait_timeout(plan, 20000)          # 20 ms limit, never satisfied
+        assert bg.moe_get_error(plan) == 5              # MOE_ERR_DEVICE_TIMEOUT
+        assert bg.moe_get_error(plan) == 0              # cleared
+        c = Case(w, gap=False)
+        run_layer(c, plan)                              # context still usable
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def test_host_argument_errors():
+    w = WL["t128_uniform"]
+    plan = make_plan(w)
+    try:
+        c = Case(w, gap=False)
+        y = torch.empty_like(c.x)
+        with pytest.raises(bg.MoeError) as ei:
+            bg.moe_forward_layer(plan, c.x, w.tokens + 1, c.L.router_w, None, c.L.routed_c,
+                                 c.L.shared_c, y)
+        assert ei.value.status == 4                      # capacity
+        with pytest.raises(bg.MoeError) as ei:
+            bg.moe_forward_layer(plan, c.x, 0, c.L.router_w, None, c.L.routed_c, c.L.shared_c, y)
+        assert ei.value.status == 1
+        with pytest.raises(bg.MoeError) as ei:              # y aliases x
+            bg.moe_forward_layer(plan, c.x, 8, c.L.router_w, None, c.L.routed_c, c.L.shared_c,
+                                 c.x)
+        assert ei.value.status == 1
+        with pytest.raises(bg.MoeError) as ei:              # misaligned x
+            bg.moe_forward_layer(plan, c.x.view(-1)[1:].data_ptr(), 8, c.L.router_w, None,
+                                 c.L.routed_c, c.L.shared_c, y)
+        assert ei.value.status == 1
+        with pytest.raises(bg.MoeError) as ei:              # shared set given but plan has none
+            bg.moe_forward_layer(plan, c.x, 8, c.L.router_w, None, c.L.routed_c, None, y)
+        assert ei.value.status == 1
+    finally:
+        bg.moe_plan_destroy(plan)

@@ -1,0 +1,117 @@
+"""GPU parity of the stacked layers (residual x <- bf16(x + moe(x)/sqrt(L))).
+
+The full-size prefill stack (T=4096, 40 layers, Zipf routing, ~18 GB of packed
+weights) runs on the GPU in the launch configuration the benchmark times; the
+oracle follows a sample of tokens through all 40 layers on its own (fp64,
+from the generator's inputs, never from GPU values). Per layer, for every
+sampled token whose routing has not yet diverged, routing indices must match
+exactly where the oracle's logit gap is >= 1e-3 and the output must be within
+2e-2 * rms. A token whose gap falls below 1e-3 may legitimately route
+differently (its logits differ by more than the gap after the GPU's bf16
+residual rounding), and is followed no further. The full routing arrays of
+every layer are checked for the invariants any correct map has.
+
+The decode stack (T = 8, 40 layers) is followed token by token the same way.
+"""
+import dataclasses
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from bit_grouped_gemm_gb300 import binding as bg
+from bit_grouped_gemm_gb300 import stack, synth
+from tests import parity
+from tests.oracle_pins import check_route_invariants
+
+pytestmark = pytest.mark.gpu
+NTHREADS = os.cpu_count() or 4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bit_grouped_gemm_gb300 import build
+    build.build()
+    bg.load_library()
+
+
+def oracle_layer_for_rows(L: stack.DeviceLayer, x_rows_bits: np.ndarray, sh: synth.MoEShape):
+    """Oracle on the given token rows of one layer, copying to the host only
+    the experts the oracle's own routing selects (plus router and shared)."""
+    orc = oracle.get()
+    wr = parity.bits(L.router_w)
+    rb = None if L.router_bias is None else L.router_bias.cpu().numpy()
+    logits = orc.router_logits(x_rows_bits, wr, rb)
+    idx, _, _ = orc.topk(logits, sh.top_k)
+    need = sorted(set(idx.reshape(-1).tolist()))
+    routed = {}
+    for m, (q, s, b) in L.routed.items():
+        qh = np.zeros(tuple(q.shape), np.uint32)
+        sh_ = np.zeros(tuple(s.shape), np.uint16)
+        bh = np.zeros(tuple(b.shape), np.uint16)
+        for e in need:
+            qh[e] = parity.words(q[e])
+            sh_[e] = parity.bits(s[e])
+            bh[e] = parity.bits(b[e])
+        routed[m] = (qh, sh_, bh)
+    shared = parity.host_set(L.shared) if L.shared is not None else None
+    return orc.moe_rows(x_rows_bits, wr, rb, routed, shared, sh.top_k, sh.group_size,
+                        nthreads=NTHREADS)
+
+
+def run_chain_check(w: synth.Workload, sample_rows, gemm_path=0):
+    sh = w.shape
+    T = w.tokens
+    layers = stack.make_layers(w, "cuda")
+    d = bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k, sh.group_size,
+                     int(sh.has_shared), T, 128, gemm_path)
+    plan = bg.moe_plan_create(d, 0)
+    alpha = stack.residual_alpha(w.layers)
+    try:
+        x = synth.tokens_x(w, "cuda")
+        x0 = parity.bits(x)[sample_rows]
+        y = torch.empty_like(x)
+        orc = oracle.get()
+        xo = x0.copy()                     # oracle's own chain for the sampled rows
+        alive = np.ones(len(sample_rows), bool)
+        compared = 0
+        worst = 0.0
+        for li, L in enumerate(layers):
+            r = bg.moe_route(plan, x, T, L.router_w, L.router_bias)
+            g = parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)
+            check_route_invariants(g, g["topk_idx"], sh.num_experts, 128)
+            bg.moe_forward_layer(plan, x, T, L.router_w, L.router_bias, L.routed_c, L.shared_c, y)
+            yg = parity.bf16_f64(parity.bits(y))[sample_rows]
+            o = oracle_layer_for_rows(L, xo, sh)
+            gidx = g["topk_idx"][sample_rows]
+            for i in range(len(sample_rows)):
+                if not alive[i]:
+                    continue
+                if o["gap"][i] < parity.GAP_MIN:
+                    alive[i] = False          # routing may differ from here on
+                    continue
+                assert np.array_equal(gidx[i], o["topk_idx"][i]), (li, i)
+                worst = max(worst, parity.check_y(yg[i], o["y"][i]))
+                compared += 1
+            bg.moe_residual_add(plan, x, y, T, alpha, x)
+            xo = orc.residual(xo, o["y"], alpha)
+        assert bg.moe_get_error(plan) == 0
+        return compared, alive, worst
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def test_prefill_stack_t4096_l40_sampled():
+    w = synth.standard_workloads()["prefill_t4096_l40_zipf"]
+    rows = np.array([0, 1, 777, 2048, 3333, 4095], np.int32)
+    compared, alive, worst = run_chain_check(w, rows)
+    assert compared >= 0.5 * len(rows) * w.layers, (compared, alive)
+
+
+def test_decode_stack_t8_l40():
+    w = synth.standard_workloads()["decode_t8_l40"]
+    rows = np.arange(8, dtype=np.int32)
+    compared, alive, worst = run_chain_check(w, rows)
+    assert compared >= 0.5 * len(rows) * w.layers, (compared, alive)
