@@ -1,0 +1,386 @@
+"""Benchmark of the W4A16 MoE block on GB300 (one JSON line on stdout).
+
+Default workload: the 40-layer stack of Qwen3.6-35B-A3B-shaped MoE layers
+(H=2048, I=512, 256 routed experts, top-8, one shared expert, 4-bit weights
+in groups of 64 with bf16 scale and bias) on a T=4096 prefill chunk with
+Zipf-skewed routing; ~18.2 GB of packed weights resident in HBM. One step is
+one pass of the whole stack: per layer, router + top-k, histogram/scan/block
+map, scatter, gather, grouped gate/up GEMM with SwiGLU, grouped down GEMM,
+combine, and the residual update x <- bf16(x + moe(x)/sqrt(40)).
+
+value: tokens/s over the timed steps (inputs resident in HBM; the packed
+weights, 18 GB, are far larger than L2, so every step streams them from HBM).
+e2e: the same through the C ABI with x copied in from pinned host memory and
+the result copied back, inside the timed region.
+roofline: the dominant kernel (grouped gate/up GEMM) against the measured
+dense bf16 peak. cpu_baseline: the fp64 oracle on a bounded sample.
+
+--impl reference times the oracle (the CPU reference of this build) on the
+same workload, a bounded sample per step.
+Multi-GPU: independent replicas (the block does not shard), one per rank.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-block prefill tokens/s (W4A16, 1 GB300) + % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+PROFILE_GATEUP = os.path.join(ROOT, "profiles", "w4_grouped_gemm_tc_gateup_t4096.txt")
+GEMM_SRC = os.path.join(ROOT, "bit_grouped_gemm_gb300", "csrc", "gemm_tc.cu")
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="prefill_t4096_l40_zipf")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args(argv)
+
+
+# ----------------------------------------------------------------- helpers
+
+
+def dist_info():
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def profiled_traffic(profile_path, kernel_src):
+    """DRAM bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the capture (keys 'source_sha256_16' and
+    'dram_bytes_per_launch' in the summary)."""
+    try:
+        kv = {}
+        with open(profile_path) as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256_16") != source_hash(kernel_src):
+            return None
+        return float(kv["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+def max_over_ranks(v, pg):
+    if pg is None:
+        return v
+    import torch
+    t = torch.tensor([float(v)], device="cuda")
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.4)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) >= 9:
+                        rows.append(parts)
+        except Exception:
+            return None
+        if not rows:
+            return None
+
+        def num(s):
+            try:
+                return float(s)
+            except ValueError:
+                return None
+        sm = sorted(v for v in (num(r[1]) for r in rows) if v is not None)
+        mx = [v for v in (num(r[2]) for r in rows) if v is not None]
+        reasons = sorted({self.REASONS[i] for r in rows for i in range(4)
+                          if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": sm[len(sm) // 2] if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------- the oracle
+
+
+def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers):
+    """Oracle tokens/s of the whole stack, from `sample_tokens` rows through
+    `sample_layers` layers, scaled by sample_layers / layers."""
+    import oracle
+    from bit_grouped_gemm_gb300 import synth
+    from tests import parity
+    sh = w.shape
+    xb = parity.bits(synth.tokens_x(w, "cpu")[:sample_tokens])
+    orc = oracle.get()
+    elapsed = 0.0
+    for li in range(sample_layers):
+        L = layers_dev[li]
+        wr = parity.bits(L.router_w)
+        rb = None if L.router_bias is None else L.router_bias.cpu().numpy()
+        routed = parity.host_set(L.routed)
+        shared = parity.host_set(L.shared) if L.shared is not None else None
+        t0 = time.perf_counter()
+        out = orc.moe_rows(xb, wr, rb, routed, shared, sh.top_k, sh.group_size,
+                           nthreads=threads)
+        elapsed += time.perf_counter() - t0
+        xb = orc.residual(xb, out["y"], 1.0 / math.sqrt(w.layers))
+    return sample_tokens * sample_layers / elapsed / w.layers, elapsed
+
+
+def workload(args):
+    from bit_grouped_gemm_gb300 import synth
+    w = synth.standard_workloads()[args.workload]
+    if args.layers:
+        w = dataclasses.replace(w, layers=args.layers)
+    return w
+
+
+# ------------------------------------------------------------------- main
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    ws, rank, local = dist_info()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    import torch
+    from bit_grouped_gemm_gb300 import binding as bg
+    from bit_grouped_gemm_gb300 import build, stack
+
+    torch.cuda.set_device(local)
+    pg = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        pg = dist
+    build.build()
+    bg.load_library()
+
+    w = workload(args)
+    sh = w.shape
+    T = w.tokens
+    from bit_grouped_gemm_gb300 import synth
+    layers = stack.make_layers(w, "cuda")
+    weight_bytes = sum(L.nbytes() for L in layers)
+    alpha = stack.residual_alpha(w.layers)
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), local)
+    stream = torch.cuda.current_stream()
+    x0 = synth.tokens_x(w, "cuda")
+    x = x0.clone()
+    y = torch.empty_like(x)
+
+    def step():
+        x.copy_(x0)
+        stack.run_stack(plan, x, layers, T, y, alpha)
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+    torch.cuda.synchronize()
+    assert bg.moe_get_error(plan) == 0
+
+    # --- timed region: inputs resident in HBM; per-kernel events on the stream
+    bg.moe_enable_timing(plan, True)
+    bg.moe_read_timing(plan)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg)
+    kt = bg.moe_read_timing(plan)
+    bg.moe_enable_timing(plan, False)
+    assert bg.moe_get_error(plan) == 0
+    ms_per_step = ms / args.steps
+    value = ws * T * args.steps / (ms / 1e3)
+
+    # --- end to end: pinned host x in, result out, through the public C ABI
+    e2e = None
+    if not args.no_e2e:
+        xh = x0.cpu().pin_memory()
+        out_h = torch.empty_like(xh).pin_memory()
+
+        def e2e_step():
+            x.copy_(xh, non_blocking=True)
+            stack.run_stack(plan, x, layers, T, y, alpha)
+            out_h.copy_(x, non_blocking=True)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), pg)
+        e2e = {"value": ws * T * args.steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": xh.numel() * xh.element_size(),
+               "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
+
+    # --- roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU)
+    peaks, peak_src = load_peaks()
+    n_pairs = T * (sh.top_k + int(sh.has_shared))
+    flops_gateup = 4.0 * sh.hidden * sh.inter * n_pairs        # per launch (one layer)
+    gu_ms, gu_n = kt["gate_up_gemm"]
+    achieved = flops_gateup / (gu_ms / gu_n / 1e3) / 1e12 if gu_n else None
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": (achieved / peak) if achieved else None,
+                "traffic": profiled_traffic(PROFILE_GATEUP, GEMM_SRC),
+                "kernel": "w4_grouped_gemm_tc, gate/up + SwiGLU (one launch per layer)",
+                "peak_source": f"{peak_src} bf16_tflops_sustained (of {peak_src})",
+                "algorithmic_flops_per_launch": flops_gateup}
+    step_flops = w.layers * (n_pairs * 6.0 * sh.hidden * sh.inter +
+                             T * 2.0 * sh.hidden * sh.num_experts)
+    kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
+               for k, v in kt.items()}
+    gpu_launches = int(sum(v[1] for v in kt.values()))
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        threads = os.cpu_count() or 1
+        st, sl = (min(T, 16 * threads), min(w.layers, 3))
+        rate, el = oracle_sample_rate(w, layers, threads, st, sl)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{st} tokens x layers 0-{sl - 1} of the {T}-token {w.layers}-layer "
+                         f"stack, fp64 oracle on {threads} threads, {el:.1f} s, "
+                         f"scaled by {sl}/{w.layers}"}
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens": T, "layers": w.layers, "hidden": sh.hidden,
+                   "inter": sh.inter, "experts": sh.num_experts, "top_k": sh.top_k,
+                   "shared_experts": int(sh.has_shared), "group_size": sh.group_size,
+                   "routing": w.routing + (f"(s={w.zipf_s})" if w.routing == "zipf" else ""),
+                   "weights_gb": round(weight_bytes / 1e9, 2),
+                   "l2": "inputs larger than L2: every step streams the packed weights "
+                         f"({weight_bytes / 1e9:.1f} GB) from HBM",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "algorithmic_tflop_per_step": step_flops / 1e12,
+        "achieved_tflops_stack": step_flops / (ms_per_step / 1e3) / 1e12,
+        "roofline": roofline,
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    bg.moe_plan_destroy(plan)
+    if pg:
+        pg.destroy_process_group()
+
+
+def run_reference(args, ws, rank):
+    """The oracle (this build's CPU reference) on the same workload: each step
+    is a bounded sample of tokens through one layer, scaled to the stack."""
+    if rank != 0:
+        return
+    import torch
+    from bit_grouped_gemm_gb300 import stack
+    w = workload(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    L0 = [stack.make_layer(w, 0, dev)]
+    threads = os.cpu_count() or 1
+    sample = min(w.tokens, 4 * threads)
+    for _ in range(max(args.warmup, 0)):
+        oracle_sample_rate(w, L0, threads, min(sample, threads), 1)
+    tok, secs = 0, 0.0
+    for _ in range(args.steps):
+        _, el = oracle_sample_rate(w, L0, threads, sample, 1)
+        tok += sample
+        secs += el
+    value = tok / secs / w.layers
+    cpu = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"{sample} tokens of layer 0 per step, fp64 oracle on {threads} "
+                     f"threads, scaled by 1/{w.layers}"}
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * secs / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.tokens, "layers": w.layers},
+        "cpu_baseline": cpu,
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()
