@@ -230,7 +230,7 @@ def main(argv=None):
     stream = torch.cuda.current_stream()
     x0 = synth.tokens_x(w, "cuda")
     x = x0.clone()
-    y = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
 
     def step():
         x.copy_(x0)

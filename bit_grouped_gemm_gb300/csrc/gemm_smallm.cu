@@ -40,6 +40,7 @@ struct Params {
   const int32_t* num_tiles;
   const uint16_t* act_in;
   uint16_t* out;
+  float* out_sh;
   int out_ld;
   const float* topk_w;
   const int32_t* perm;
@@ -269,8 +270,12 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
         if (p.mode == 0) {
           const float a = silu_f32(tot[0][nt][q]) * tot[1][nt][q];
           p.out[(size_t)pos * p.out_ld + nrow[0][h]] = f32_to_bf16(a);
+        } else if (shared) {
+          float* o = p.out_sh + (size_t)(pos - p.T * p.k) * p.out_ld;
+          o[nrow[0][h]] = tot[0][nt][q];
+          o[nrow[1][h]] = tot[1][nt][q];
         } else {
-          const float wt = shared ? 1.0f : __ldg(p.topk_w + __ldg(p.perm + pos));
+          const float wt = __ldg(p.topk_w + __ldg(p.perm + pos));
           p.out[(size_t)pos * p.out_ld + nrow[0][h]] = f32_to_bf16(tot[0][nt][q] * wt);
           p.out[(size_t)pos * p.out_ld + nrow[1][h]] = f32_to_bf16(tot[1][nt][q] * wt);
         }
@@ -295,6 +300,7 @@ cudaError_t launch_gemm_smallm(int mode, const GemmProblem& g, cudaStream_t st) 
   p.num_tiles = g.num_tiles;
   p.act_in = g.act_in;
   p.out = g.out;
+  p.out_sh = g.out_sh;
   p.out_ld = g.out_ld;
   p.topk_w = g.topk_w;
   p.perm = g.perm;

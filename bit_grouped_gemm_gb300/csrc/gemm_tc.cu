@@ -57,6 +57,7 @@ struct Params {
   const int32_t* num_tiles;
   W4Dev w0, w1, sw0, sw1;
   uint16_t* out;
+  float* out_sh;
   int out_ld;
   const float* topk_w;
   const int32_t* perm;
@@ -349,13 +350,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
               o[(size_t)cc * p.out_ld] = f32_to_bf16(silu_f32(g) * uu);
             }
           }
+        } else if (U.shared) {
+          // shared expert (weight 1): kept in fp32, it is as large as the output
+          float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j + r;
+#pragma unroll
+          for (int cc = 0; cc < 32; ++cc) {
+            if (cc < nval) {
+              o[(size_t)cc * p.out_ld] = __uint_as_float(v0[cc]);
+              o[(size_t)cc * p.out_ld + 128] = __uint_as_float(v1[cc]);
+            }
+          }
         } else {
           uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + r;
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc) {
             if (cc < nval) {
               const int pos = U.m0 + c0 + cc;
-              const float wt = U.shared ? 1.0f : __ldg(p.topk_w + __ldg(p.perm + pos));
+              const float wt = __ldg(p.topk_w + __ldg(p.perm + pos));
               o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * wt);
               o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * wt);
             }
@@ -396,6 +407,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, D
   p.sw0 = g.sw0;
   p.sw1 = g.sw1;
   p.out = g.out;
+  p.out_sh = g.out_sh;
   p.out_ld = g.out_ld;
   p.topk_w = g.topk_w;
   p.perm = g.perm;

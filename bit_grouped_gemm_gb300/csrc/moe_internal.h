@@ -38,9 +38,9 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
                                  int E, int32_t* perm, int32_t* inv, cudaStream_t st);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
                                int with_shared, uint16_t* xs, cudaStream_t st);
-cudaError_t launch_combine(const uint16_t* d, const int32_t* inv, int T, int k, int H,
-                           int with_shared, uint16_t* y, cudaStream_t st);
-cudaError_t launch_residual(const uint16_t* x, const uint16_t* y, long long n, float alpha,
+cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
+                           int k, int H, float* y, cudaStream_t st);
+cudaError_t launch_residual(const uint16_t* x, const float* y, long long n, float alpha,
                             uint16_t* out, cudaStream_t st);
 cudaError_t launch_debug_wait(DevErr e, cudaStream_t st);
 
@@ -55,7 +55,8 @@ struct GemmProblem {
   const int32_t* num_tiles; // device count of routed tiles
   int max_routed_tiles;     // host upper bound (grid sizing)
   const uint16_t* act_in;   // B operand rows [rows][K] bf16 (xs or act)
-  uint16_t* out;            // output rows [rows][out_ld] bf16
+  uint16_t* out;            // output rows [rows][out_ld] bf16 (down: routed rows only)
+  float* out_sh;            // down: the shared expert's rows, fp32 [T][out_ld]
   int out_ld;
   const float* topk_w;      // down: per-slot weights (by slot)
   const int32_t* perm;      // down: position -> slot

@@ -22,7 +22,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
   size_t topk_idx, topk_w, logits, blk_cnt, cnt, off, tile_off, num_tiles, perm, inv, bmap,
-      err, xs, act, d, total;
+      err, xs, act, d, dsh, total;
   int nblk_max, max_tiles, rows_cap;
 };
 
@@ -52,7 +52,8 @@ Layout make_layout(const moe_plan_desc& d) {
   L.err = take(16);
   L.xs = take((size_t)L.rows_cap * d.hidden * 2);
   L.act = take((size_t)L.rows_cap * d.inter * 2);
-  L.d = take((size_t)L.rows_cap * d.hidden * 2);
+  L.d = take(Tm * k * d.hidden * 2);
+  L.dsh = take(d.has_shared ? Tm * d.hidden * 4 : 0);
   L.total = o;
   return L;
 }
@@ -227,7 +228,7 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
 }
 
 moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
-                    const moe_experts* routed, const moe_experts* shared, uint16_t* y,
+                    const moe_experts* routed, const moe_experts* shared, float* y,
                     cudaStream_t st) {
   const moe_plan_desc& d = p->d;
   const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
@@ -274,6 +275,7 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   g1.N = H;
   g1.act_in = p->at<uint16_t>(p->L.act);
   g1.out = p->at<uint16_t>(p->L.d);
+  g1.out_sh = hs ? p->at<float>(p->L.dsh) : nullptr;
   g1.out_ld = H;
   g1.w0 = dev(routed->down);
   g1.w1 = dev(routed->down);
@@ -313,7 +315,8 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = timed(p, 6, st, [&] {
-    return launch_combine(p->at<uint16_t>(p->L.d), r->inv, T, k, H, hs, y, st);
+    return launch_combine(p->at<uint16_t>(p->L.d), hs ? p->at<float>(p->L.dsh) : nullptr,
+                          r->inv, T, k, H, y, st);
   });
   return st_of(e);
 }
@@ -335,14 +338,14 @@ moe_status check_route_args(const moe_plan* p, const uint16_t* x, int T, const u
 
 moe_status check_ffn_args(const moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
                           const moe_experts* routed, const moe_experts* shared,
-                          const uint16_t* y) {
+                          const float* y) {
   moe_status s = check_T(p, T);
   if (s != MOE_OK) return s;
   if (!x || !y || !aligned16(x) || !aligned16(y)) return MOE_ERR_INVALID_ARG;
-  const size_t bytes = (size_t)T * p->d.hidden * 2;
+  const size_t xbytes = (size_t)T * p->d.hidden * 2, ybytes = (size_t)T * p->d.hidden * 4;
   const uint8_t* xb = reinterpret_cast<const uint8_t*>(x);
   const uint8_t* yb = reinterpret_cast<const uint8_t*>(y);
-  if (xb < yb + bytes && yb < xb + bytes) return MOE_ERR_INVALID_ARG;   // y overlaps x
+  if (xb < yb + ybytes && yb < xb + xbytes) return MOE_ERR_INVALID_ARG;   // y overlaps x
   if ((s = check_experts(routed)) != MOE_OK) return s;
   if (p->d.has_shared) {
     if ((s = check_experts(shared)) != MOE_OK) return s;
@@ -436,7 +439,7 @@ moe_status moe_route(moe_plan_t p, const uint16_t* x, int T, const uint16_t* rou
 }
 
 moe_status moe_grouped_w4_ffn(moe_plan_t p, const uint16_t* x, int T, const moe_routing* r,
-                              const moe_experts* routed, const moe_experts* shared, uint16_t* y,
+                              const moe_experts* routed, const moe_experts* shared, float* y,
                               moe_stream_t stream) {
   if (!p || !r) return MOE_ERR_INVALID_ARG;
   moe_status s = check_ffn_args(p, x, T, r, routed, shared, y);
@@ -446,7 +449,7 @@ moe_status moe_grouped_w4_ffn(moe_plan_t p, const uint16_t* x, int T, const moe_
 
 moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint16_t* router_w,
                              const float* router_bias, const moe_experts* routed,
-                             const moe_experts* shared, uint16_t* y, moe_stream_t stream) {
+                             const moe_experts* shared, float* y, moe_stream_t stream) {
   if (!p) return MOE_ERR_INVALID_ARG;
   moe_status s = check_route_args(p, x, T, router_w, router_bias);
   if (s != MOE_OK) return s;
@@ -459,7 +462,7 @@ moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint1
   return ffn_impl(p, x, T, &r, routed, shared, y, st);
 }
 
-moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const uint16_t* y, int T,
+moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const float* y, int T,
                             float alpha, uint16_t* x_out, moe_stream_t stream) {
   if (!p || !x || !y || !x_out) return MOE_ERR_INVALID_ARG;
   moe_status s = check_T(p, T);
@@ -526,6 +529,7 @@ void* moe_debug_buffer(moe_plan_t p, int which) {
     case 0: return p->scratch + p->L.xs;
     case 1: return p->scratch + p->L.act;
     case 2: return p->scratch + p->L.d;
+    case 3: return p->d.has_shared ? p->scratch + p->L.dsh : nullptr;
   }
   return nullptr;
 }

@@ -391,14 +391,15 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, in
 }
 
 // ---------------------------------------------------------------------------
-// Combine: y[t] = d[T*k + t] + sum_j d[inv[t*k + j]] (rows of d already carry
-// their top-k weight), FP32 in fixed order (shared, then j = 0..k-1), one
-// rounding to bf16.
+// Combine: y[t] = d_sh[t] + sum_j d[inv[t*k + j]] in FP32, fixed order
+// (shared, then j = 0..k-1). Routed rows of d are bf16 and already carry
+// their top-k weight; the shared expert's rows are fp32 (weight 1). y is the
+// block's FP32 output.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ d,
+                                                      const float* __restrict__ d_sh,
                                                       const int32_t* __restrict__ inv, int T,
-                                                      int k, int H, int with_shared,
-                                                      uint16_t* __restrict__ y) {
+                                                      int k, int H, float* __restrict__ y) {
   __shared__ int rows_s[33];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
@@ -406,16 +407,14 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     __syncthreads();
     for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
       float acc[8];
+      if (d_sh) {
+        const float4* s = reinterpret_cast<const float4*>(d_sh + (size_t)t * H + h0);
+        const float4 a = __ldg(s), b = __ldg(s + 1);
+        acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+        acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+      } else {
 #pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      if (with_shared) {
-        uint4 v = __ldg(reinterpret_cast<const uint4*>(d + (size_t)(T * k + t) * H + h0));
-        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          acc[2 * i] += bf16_lo(w[i]);
-          acc[2 * i + 1] += bf16_hi(w[i]);
-        }
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
       }
       for (int j = 0; j < k; ++j) {
         uint4 v = __ldg(reinterpret_cast<const uint4*>(d + (size_t)rows_s[j] * H + h0));
@@ -426,44 +425,43 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
           acc[2 * i + 1] += bf16_hi(w[i]);
         }
       }
-      uint4 o;
-      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) ow[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
-      *reinterpret_cast<uint4*>(y + (size_t)t * H + h0) = o;
+      float4* o = reinterpret_cast<float4*>(y + (size_t)t * H + h0);
+      o[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      o[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     }
   }
 }
 
-cudaError_t launch_combine(const uint16_t* d, const int32_t* inv, int T, int k, int H,
-                           int with_shared, uint16_t* y, cudaStream_t st) {
+cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
+                           int k, int H, float* y, cudaStream_t st) {
   int blocks = T < 4096 ? T : 4096;
-  combine_kernel<<<blocks, 256, 0, st>>>(d, inv, T, k, H, with_shared, y);
+  combine_kernel<<<blocks, 256, 0, st>>>(d, d_sh, inv, T, k, H, y);
   return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
-// Residual: out = bf16(x + alpha * y), 8 elements per thread.
+// Residual: out = bf16(x + alpha * y), y fp32, 8 elements per thread.
 // ---------------------------------------------------------------------------
-__global__ void residual_kernel(const uint16_t* __restrict__ x, const uint16_t* __restrict__ y,
+__global__ void residual_kernel(const uint16_t* __restrict__ x, const float* __restrict__ y,
                                 long long n8, float alpha, uint16_t* __restrict__ out) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
        i += (long long)gridDim.x * blockDim.x) {
-    uint4 a = reinterpret_cast<const uint4*>(x)[i];
-    uint4 b = reinterpret_cast<const uint4*>(y)[i];
+    const uint4 a = reinterpret_cast<const uint4*>(x)[i];
+    const float4 b0 = reinterpret_cast<const float4*>(y)[2 * i];
+    const float4 b1 = reinterpret_cast<const float4*>(y)[2 * i + 1];
+    const float yb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
     const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
-    const uint32_t* bw = reinterpret_cast<const uint32_t*>(&b);
     uint4 o;
     uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
     for (int j = 0; j < 4; ++j)
-      ow[j] = pack_bf16x2(fmaf(alpha, bf16_lo(bw[j]), bf16_lo(aw[j])),
-                          fmaf(alpha, bf16_hi(bw[j]), bf16_hi(aw[j])));
+      ow[j] = pack_bf16x2(fmaf(alpha, yb[2 * j], bf16_lo(aw[j])),
+                          fmaf(alpha, yb[2 * j + 1], bf16_hi(aw[j])));
     reinterpret_cast<uint4*>(out)[i] = o;
   }
 }
 
-cudaError_t launch_residual(const uint16_t* x, const uint16_t* y, long long n, float alpha,
+cudaError_t launch_residual(const uint16_t* x, const float* y, long long n, float alpha,
                             uint16_t* out, cudaStream_t st) {
   long long n8 = n / 8;
   long long blocks = (n8 + 255) / 256;

@@ -145,21 +145,25 @@ moe_status moe_route(moe_plan_t plan, const uint16_t* x, int T, const uint16_t* 
  * x: bf16 [T][H]; routing: as moe_route produces (topk_w, perm, inv,
  * block_map and num_tiles are read); routed: E experts; shared: one expert
  * set with E = 1, or NULL (must be non-NULL iff desc.has_shared);
- * y: bf16 [T][H], must not overlap x. Dequantised weights exist only in
- * on-chip memory; accumulation is FP32. */
+ * y: f32 [T][H], the block's FP32 sum (the pages accumulate in FP32; a bf16
+ * rounding of y alone would cost about 1.5% of the output's rms at 4-sigma
+ * values), must not overlap x. Dequantised weights exist only in on-chip
+ * memory. Routed experts' outputs are weighted and kept in bf16 before the
+ * combine; the shared expert's are kept in FP32. */
 moe_status moe_grouped_w4_ffn(moe_plan_t plan, const uint16_t* x, int T,
                               const moe_routing* routing, const moe_experts* routed,
-                              const moe_experts* shared, uint16_t* y, moe_stream_t stream);
+                              const moe_experts* shared, float* y, moe_stream_t stream);
 
 /* moe_route followed by moe_grouped_w4_ffn: one MoE layer, no host sync. */
 moe_status moe_forward_layer(moe_plan_t plan, const uint16_t* x, int T,
                              const uint16_t* router_w, const float* router_bias,
                              const moe_experts* routed, const moe_experts* shared,
-                             uint16_t* y, moe_stream_t stream);
+                             float* y, moe_stream_t stream);
 
 /* Residual update between stacked layers: x_out[i] = bf16(x[i] + alpha*y[i])
- * over T*H elements, FP32 arithmetic. x_out may equal x. */
-moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const uint16_t* y, int T,
+ * over T*H elements; x and x_out bf16, y f32, FP32 arithmetic. x_out may
+ * equal x. */
+moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, int T,
                             float alpha, uint16_t* x_out, moe_stream_t stream);
 
 /* Reads and clears the plan's device error word. Synchronises the device:
@@ -188,8 +192,9 @@ moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
 /* Introspection of plan scratch for tests and profiling: device address of
  * the gathered activations (which = 0: bf16 [rows][H], routed positions
  * first, then the shared expert's T rows), the SwiGLU activations (1: bf16
- * [rows][I]) or the weighted expert outputs (2: bf16 [rows][H]) of the last
- * layer. NULL for an unknown `which`. */
+ * [rows][I]), the weighted routed expert outputs (2: bf16 [T*k][H]) or the
+ * shared expert's outputs (3: f32 [T][H]) of the last layer. NULL for an
+ * unknown `which` or a plan without a shared expert (3). */
 void* moe_debug_buffer(moe_plan_t plan, int which);
 
 /* Which GEMM path the last moe_grouped_w4_ffn took: 1 tensor-core, 2 small-M. */

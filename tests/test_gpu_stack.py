@@ -72,7 +72,7 @@ def run_chain_check(w: synth.Workload, sample_rows, gemm_path=0):
     try:
         x = synth.tokens_x(w, "cuda")
         x0 = parity.bits(x)[sample_rows]
-        y = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
         orc = oracle.get()
         xo = x0.copy()                     # oracle's own chain for the sampled rows
         alive = np.ones(len(sample_rows), bool)
@@ -83,7 +83,7 @@ def run_chain_check(w: synth.Workload, sample_rows, gemm_path=0):
             g = parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)
             check_route_invariants(g, g["topk_idx"], sh.num_experts, 128)
             bg.moe_forward_layer(plan, x, T, L.router_w, L.router_bias, L.routed_c, L.shared_c, y)
-            yg = parity.bf16_f64(parity.bits(y))[sample_rows]
+            yg = y.double().cpu().numpy()[sample_rows]
             o = oracle_layer_for_rows(L, xo, sh)
             gidx = g["topk_idx"][sample_rows]
             for i in range(len(sample_rows)):
