@@ -6,7 +6,8 @@ in groups of 64 with bf16 scale and bias) on a T=4096 prefill chunk with
 Zipf-skewed routing; ~18.2 GB of packed weights resident in HBM. One step is
 one pass of the whole stack: per layer, router + top-k, histogram/scan/block
 map, scatter, gather, grouped gate/up GEMM with SwiGLU, grouped down GEMM,
-combine, and the residual update x <- bf16(x + moe(x)/sqrt(40)).
+combine, and the stack update x <- bf16(x + moe(rmsnorm(x))/sqrt(40)) (the
+RMS-normalised stream is each layer's input).
 
 value: tokens/s over the timed steps (inputs resident in HBM; the packed
 weights, 18 GB, are far larger than L2, so every step streams them from HBM).
@@ -182,10 +183,11 @@ def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers):
         routed = parity.host_set(L.routed)
         shared = parity.host_set(L.shared) if L.shared is not None else None
         t0 = time.perf_counter()
-        out = orc.moe_rows(xb, wr, rb, routed, shared, sh.top_k, sh.group_size,
+        xn = orc.rmsnorm(xb)
+        out = orc.moe_rows(xn, wr, rb, routed, shared, sh.top_k, sh.group_size,
                            nthreads=threads)
-        elapsed += time.perf_counter() - t0
         xb = orc.residual(xb, out["y"], 1.0 / math.sqrt(w.layers))
+        elapsed += time.perf_counter() - t0
     return sample_tokens * sample_layers / elapsed / w.layers, elapsed
 
 
@@ -231,10 +233,11 @@ def main(argv=None):
     x0 = synth.tokens_x(w, "cuda")
     x = x0.clone()
     y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+    xn = torch.empty_like(x)
 
     def step():
         x.copy_(x0)
-        stack.run_stack(plan, x, layers, T, y, alpha)
+        stack.run_stack(plan, x, xn, layers, T, y, alpha)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -271,7 +274,7 @@ def main(argv=None):
 
         def e2e_step():
             x.copy_(xh, non_blocking=True)
-            stack.run_stack(plan, x, layers, T, y, alpha)
+            stack.run_stack(plan, x, xn, layers, T, y, alpha)
             out_h.copy_(x, non_blocking=True)
         for _ in range(2):
             e2e_step()

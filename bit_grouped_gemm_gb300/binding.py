@@ -80,7 +80,7 @@ def load_library(path: Optional[str] = None):
                                    ctypes.POINTER(MoeExperts), P, P]),
         "moe_forward_layer": (S, [P, P, I, P, P, ctypes.POINTER(MoeExperts),
                                   ctypes.POINTER(MoeExperts), P, P]),
-        "moe_residual_add": (S, [P, P, P, I, ctypes.c_float, P, P]),
+        "moe_residual_add": (S, [P, P, P, I, ctypes.c_float, P, P, P]),
         "moe_get_error": (S, [P]),
         "moe_debug_wait_timeout": (S, [P, I, P]),
         "moe_enable_timing": (S, [P, I]),
@@ -175,9 +175,10 @@ def moe_forward_layer(plan: int, x, T: int, router_w, router_bias, routed: MoeEx
         "moe_forward_layer")
 
 
-def moe_residual_add(plan: int, x, y, T: int, alpha: float, x_out, stream=None) -> None:
+def moe_residual_add(plan: int, x, y, T: int, alpha: float, x_out=None, xn_out=None,
+                     stream=None) -> None:
     _check(load_library().moe_residual_add(plan, _ptr(x), _ptr(y), T, float(alpha), _ptr(x_out),
-                                           _stream(stream)), "moe_residual_add")
+                                           _ptr(xn_out), _stream(stream)), "moe_residual_add")
 
 
 def moe_get_error(plan: int) -> int:

@@ -13,10 +13,10 @@
 //     pass, two down row slabs for the down pass); the tile's tokens are the
 //     n8 side, in passes of 8*NT tokens;
 //   * each thread streams 8 bytes of packed weights per row per group with a
-//     4-group register prefetch, and converts nibbles to bf16 "128 + q" with
-//     one LOP3 per pair (exact); the MMA sums (128+q)*x over one group of 64
+//     4-group register prefetch, and converts nibbles to fp16 "1024 + q" with
+//     one LOP3 per pair (exact); the MMA sums (1024+q)*x over one group of 64
 //     in FP32, and the group's affine map is applied to the 4 partial sums:
-//         sum_k w_k x_k = s * sum_k (128+q_k) x_k + (b - 128 s) * sum_k x_k
+//         sum_k w_k x_k = s * sum_k (1024+q_k) x_k + (b - 1024 s) * sum_k x_k
 //     which is exact algebra of w = q*s + b (the group sums of x are
 //     precomputed in FP32 while the tokens are staged in shared memory);
 //   * tokens are staged in shared memory with each 8-element block stored in
@@ -50,7 +50,7 @@ struct Params {
 __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                           uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
       "{%8, %9}, {%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -142,8 +142,8 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
           dst[4 * v + 1] = prmt(x8.x, x8.z, 0x7632);   // (x1, x5)
           dst[4 * v + 2] = prmt(x8.y, x8.w, 0x5410);   // (x2, x6)
           dst[4 * v + 3] = prmt(x8.y, x8.w, 0x7632);   // (x3, x7)
-          sum += bf16_lo(x8.x) + bf16_hi(x8.x) + bf16_lo(x8.y) + bf16_hi(x8.y) +
-                 bf16_lo(x8.z) + bf16_hi(x8.z) + bf16_lo(x8.w) + bf16_hi(x8.w);
+          sum += f16_lo(x8.x) + f16_hi(x8.x) + f16_lo(x8.y) + f16_hi(x8.y) +
+                 f16_lo(x8.z) + f16_hi(x8.z) + f16_lo(x8.w) + f16_hi(x8.w);
         }
       } else {
 #pragma unroll
@@ -196,8 +196,8 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            nibbles_to_bf16x2_128(qr[i][mt][h].x, pa[mt][h][0]);
-            nibbles_to_bf16x2_128(qr[i][mt][h].y, pa[mt][h][1]);
+            nibbles_to_f16x2_1024(qr[i][mt][h].x, pa[mt][h][0]);
+            nibbles_to_f16x2_1024(qr[i][mt][h].y, pa[mt][h][1]);
           }
         if (more) {
 #pragma unroll
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
                         pa[mt][0][wsel][psel + 1], pa[mt][1][wsel][psel + 1], b0, b1);
           }
         }
-        // affine map of the group: s * acc + (b - 128 s) * sum(x)
+        // affine map of the group: s * acc + (b - 1024 s) * sum(x)
         const int half = (i & 1) ? 16 : 0;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
             const uint32_t sv = ((i >> 1) ? sr[mt][h].y : sr[mt][h].x) >> half;
             const uint32_t bv = ((i >> 1) ? br[mt][h].y : br[mt][h].x) >> half;
             sc[h] = bf16_to_f32(static_cast<uint16_t>(sv & 0xFFFFu));
-            cb[h] = fmaf(-128.0f, sc[h], bf16_to_f32(static_cast<uint16_t>(bv & 0xFFFFu)));
+            cb[h] = fmaf(-1024.0f, sc[h], bf16_to_f32(static_cast<uint16_t>(bv & 0xFFFFu)));
           }
 #pragma unroll
           for (int nt = 0; nt < NT; ++nt) {
@@ -269,7 +269,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
         const int h = q >> 1;
         if (p.mode == 0) {
           const float a = silu_f32(tot[0][nt][q]) * tot[1][nt][q];
-          p.out[(size_t)pos * p.out_ld + nrow[0][h]] = f32_to_bf16(a);
+          p.out[(size_t)pos * p.out_ld + nrow[0][h]] = f32_to_f16_sat(a);
         } else if (shared) {
           float* o = p.out_sh + (size_t)(pos - p.T * p.k) * p.out_ld;
           o[nrow[0][h]] = tot[0][nt][q];

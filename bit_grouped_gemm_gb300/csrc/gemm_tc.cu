@@ -16,12 +16,16 @@
 //     down pass), K swept in chunks of 64 (one quantisation group);
 //   * packed weight tiles arrive by TMA (128-byte swizzle) into shared
 //     memory; 8 dequant warps turn each thread's 64 nibbles of one weight row
-//     into bf16 (one fused multiply-add, one rounding) and store them with
+//     into fp16 (one fused multiply-add, one rounding) and store them with
 //     tcgen05.st straight into tensor memory, where the MMA reads them as its
 //     A operand -- rebuilt weights never touch shared or global memory;
 //   * token activations (the B operand, N = tile rows rounded up to 16) come
 //     by TMA in the canonical 128-byte-swizzled K-major layout;
-//   * one thread issues tcgen05.mma (M=128, K=16, bf16 in, fp32 in TMEM) for
+//   * MMA operands are fp16: the bf16 activations are converted exactly (the
+//     block's input is RMS-normalised, far inside fp16's range) when they are
+//     gathered, and fp16's 11-bit significand keeps the rounding of the
+//     dequantised weights and SwiGLU activations 8x below bf16's;
+//   * one thread issues tcgen05.mma (M=128, K=16, fp16 in, fp32 in TMEM) for
 //     both weight blocks; 4 epilogue warps read the accumulators back with
 //     tcgen05.ld and apply SwiGLU (gate/up) or the top-k weight (down);
 //   * persistent CTAs (one per SM, 512 TMEM columns each) walk the units;
@@ -37,7 +41,7 @@ constexpr int kThreads = 512;
 constexpr int kBStages = 4;               // activation chunks (64 K) in flight
 constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
 constexpr int kAStages = 4;               // TMEM weight stages (64 K)
-constexpr int kBTileBytes = 128 * 128;    // 128 token rows x 64 bf16
+constexpr int kBTileBytes = 128 * 128;    // 128 token rows x 64 fp16
 constexpr int kQTileBytes = 128 * 128;    // 128 weight rows x 32 words
 constexpr int kQStageBytes = 2 * kQTileBytes;
 constexpr int kOffB = 0;
@@ -227,7 +231,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
         const Unit U = decode_unit(p, u, n_routed);
         const int ntok = (U.rows + 15) & ~15;
-        const uint32_t idesc = idesc_bf16_f32(128, ntok);
+        const uint32_t idesc = idesc_f16_f32(128, ntok);
         if (!(ok = thread_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3))) break;
         tc_fence_after();
         for (int c = 0; c < nchunk; ++c) {
@@ -241,8 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
             const uint64_t bd = smem_desc_sw128(bbase + 32 * kk);
             const uint32_t a0 = tmem + kAStageCol + 64 * as + 8 * kk;
             const uint32_t acc = (c | kk) != 0;
-            mma_bf16_ts(tmem + kAccCol0, a0, bd, idesc, acc);
-            mma_bf16_ts(tmem + kAccCol1, a0 + 32, bd, idesc, acc);
+            mma_f16_ts(tmem + kAccCol0, a0, bd, idesc, acc);
+            mma_f16_ts(tmem + kAccCol1, a0 + 32, bd, idesc, acc);
           }
           mma_commit(&b_empty[bs]);
           mma_commit(&a_empty[as]);
@@ -294,15 +298,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
                                            : (((sub >> 1) ? s4.y : s4.x) & 0xFFFFu);
           const uint32_t bbits = (sub & 1) ? (((sub >> 1) ? b4.y : b4.x) >> 16)
                                            : (((sub >> 1) ? b4.y : b4.x) & 0xFFFFu);
-          const uint32_t s2u = sbits | (sbits << 16), b2u = bbits | (bbits << 16);
-          const __nv_bfloat162 s2 = *reinterpret_cast<const __nv_bfloat162*>(&s2u);
-          const __nv_bfloat162 b2 = *reinterpret_cast<const __nv_bfloat162*>(&b2u);
+          // bf16 scale and bias as fp16 (exact inside fp16's normal range)
+          const __half2 s2 = __half2half2(__float2half_rn(bf16_to_f32((uint16_t)sbits)));
+          const __half2 b2 = __half2half2(__float2half_rn(bf16_to_f32((uint16_t)bbits)));
           uint32_t out[32];
           const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             uint32_t o4[4];
-            dequant_word_bf16(words[i], s2, b2, o4);
+            dequant_word_f16(words[i], s2, b2, o4);
             out[4 * i + 0] = o4[0];
             out[4 * i + 1] = o4[1];
             out[4 * i + 2] = o4[2];
@@ -347,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
             if (cc < nval) {
               const float g = __uint_as_float(v0[cc]);
               const float uu = __uint_as_float(v1[cc]);
-              o[(size_t)cc * p.out_ld] = f32_to_bf16(silu_f32(g) * uu);
+              o[(size_t)cc * p.out_ld] = f32_to_f16_sat(silu_f32(g) * uu);
             }
           }
         } else if (U.shared) {

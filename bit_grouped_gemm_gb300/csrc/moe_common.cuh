@@ -4,6 +4,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -130,8 +131,8 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (bf16 in, fp32 accumulate).
-__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+// D[tmem] (+)= A[tmem] * B[smem desc]; kind::f16 (16-bit inputs, fp32 accumulate).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -196,28 +197,48 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t smem_addr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A and B bf16, both K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4)                                 // D format: f32
-         | (1u << 7)                               // A format: bf16
-         | (1u << 10)                              // B format: bf16
+         | (0u << 7)                               // A format: f16
+         | (0u << 10)                              // B format: f16
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
 }
 
-// ------------------------------------------------------------- bf16 utils ---
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
+// ------------------------------------------------------ bf16 / fp16 utils ---
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t v) {
   return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
 __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
   __nv_bfloat16 b = __float2bfloat16_rn(f);
   return *reinterpret_cast<uint16_t*>(&b);
+}
+
+// fp16 with saturation to the finite range (no inf from large inputs).
+constexpr float kF16Max = 65504.0f;
+__device__ __forceinline__ float sat_f16_range(float v) {
+  return fminf(fmaxf(v, -kF16Max), kF16Max);
+}
+__device__ __forceinline__ uint16_t f32_to_f16_sat(float f) {
+  __half h = __float2half_rn(sat_f16_range(f));
+  return *reinterpret_cast<uint16_t*>(&h);
+}
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  __half2 v = __floats2half2_rn(sat_f16_range(lo), sat_f16_range(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half(static_cast<unsigned short>(v >> 16)));
 }
 
 // Bits of a LOP3: (a & b) | c.
@@ -227,14 +248,14 @@ __device__ __forceinline__ uint32_t lop3_and_or(uint32_t a, uint32_t b, uint32_t
   return d;
 }
 
-// Four bf16x2 words holding 128 + q for the eight nibbles of `w`, as pairs
-// (q0,q4), (q1,q5), (q2,q6), (q3,q7): 0x4300 is bf16 128.0 and a nibble in
-// the low mantissa bits adds its value exactly.
-__device__ __forceinline__ void nibbles_to_bf16x2_128(uint32_t w, uint32_t (&p)[4]) {
-  p[0] = lop3_and_or(w, 0x000F000Fu, 0x43004300u);
-  p[1] = lop3_and_or(w >> 4, 0x000F000Fu, 0x43004300u);
-  p[2] = lop3_and_or(w >> 8, 0x000F000Fu, 0x43004300u);
-  p[3] = lop3_and_or(w >> 12, 0x000F000Fu, 0x43004300u);
+// Four f16x2 words holding 1024 + q for the eight nibbles of `w`, as pairs
+// (q0,q4), (q1,q5), (q2,q6), (q3,q7): 0x6400 is fp16 1024.0, whose unit in
+// the last place is 1, so a nibble in the low mantissa bits adds its value.
+__device__ __forceinline__ void nibbles_to_f16x2_1024(uint32_t w, uint32_t (&p)[4]) {
+  p[0] = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+  p[1] = lop3_and_or(w >> 4, 0x000F000Fu, 0x64006400u);
+  p[2] = lop3_and_or(w >> 8, 0x000F000Fu, 0x64006400u);
+  p[3] = lop3_and_or(w >> 12, 0x000F000Fu, 0x64006400u);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
@@ -243,19 +264,19 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   return d;
 }
 
-// Dequantise one packed word (8 consecutive k) to 4 bf16x2 words in k order:
-// w_k = bf16(q_k * s + b), one rounding (bf16x2 fused multiply-add).
-__device__ __forceinline__ void dequant_word_bf16(uint32_t w, __nv_bfloat162 s2,
-                                                  __nv_bfloat162 b2, uint32_t (&out)[4]) {
+// Dequantise one packed word (8 consecutive k) to 4 f16x2 words in k order:
+// w_k = fp16(q_k * s + b), one rounding (f16x2 fused multiply-add of exact q).
+__device__ __forceinline__ void dequant_word_f16(uint32_t w, __half2 s2, __half2 b2,
+                                                 uint32_t (&out)[4]) {
   uint32_t p[4];
-  nibbles_to_bf16x2_128(w, p);
-  const __nv_bfloat162 c128 = __floats2bfloat162_rn(128.0f, 128.0f);
+  nibbles_to_f16x2_1024(w, p);
+  const __half2 c1024 = __floats2half2_rn(1024.0f, 1024.0f);
   uint32_t r[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&p[i]);
-    v = __hsub2(v, c128);            // exact: q in 0..15
-    v = __hfma2(v, s2, b2);          // round once to bf16
+    __half2 v = *reinterpret_cast<__half2*>(&p[i]);
+    v = __hsub2(v, c1024);           // exact: q in 0..15
+    v = __hfma2(v, s2, b2);          // round once to fp16
     r[i] = *reinterpret_cast<uint32_t*>(&v);
   }
   // (q0,q4) (q1,q5) (q2,q6) (q3,q7) -> (q0,q1) (q2,q3) (q4,q5) (q6,q7)
@@ -263,6 +284,11 @@ __device__ __forceinline__ void dequant_word_bf16(uint32_t w, __nv_bfloat162 s2,
   out[1] = prmt(r[2], r[3], 0x5410);
   out[2] = prmt(r[0], r[1], 0x7632);
   out[3] = prmt(r[2], r[3], 0x7632);
+}
+
+// bf16 bit pattern -> fp16 (saturating) bits, the pair packed as f16x2
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
+  return pack_f16x2_sat(bf16_lo(v), bf16_hi(v));
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }

@@ -11,6 +11,8 @@
 
 using namespace moe;
 
+static constexpr float kRmsEps = 1e-6f;   // RMS-norm epsilon of the stack update
+
 namespace {
 
 struct TimedLaunch {
@@ -397,9 +399,9 @@ moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* ou
     return MOE_ERR_CUDA;
   }
   cudaMemset(p->scratch + p->L.err, 0, 16);
-  bool ok = encode_2d(&p->tm_xs, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, p->at<uint16_t>(p->L.xs),
+  bool ok = encode_2d(&p->tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->at<uint16_t>(p->L.xs),
                       p->L.rows_cap, desc->hidden, 64, 128) &&
-            encode_2d(&p->tm_act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+            encode_2d(&p->tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
                       p->at<uint16_t>(p->L.act), p->L.rows_cap, desc->inter, 64, 128);
   if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(p->scratch);
@@ -463,14 +465,18 @@ moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint1
 }
 
 moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const float* y, int T,
-                            float alpha, uint16_t* x_out, moe_stream_t stream) {
-  if (!p || !x || !y || !x_out) return MOE_ERR_INVALID_ARG;
+                            float alpha, uint16_t* x_out, uint16_t* xn_out, moe_stream_t stream) {
+  if (!p || !x) return MOE_ERR_INVALID_ARG;
   moe_status s = check_T(p, T);
   if (s != MOE_OK) return s;
-  if (!aligned16(x) || !aligned16(y) || !aligned16(x_out)) return MOE_ERR_INVALID_ARG;
+  if (!x_out) x_out = const_cast<uint16_t*>(x);
+  if (!aligned16(x) || !aligned16(x_out) || (y && !aligned16(y)) || (xn_out && !aligned16(xn_out)))
+    return MOE_ERR_INVALID_ARG;
+  if (!y && !xn_out && x_out == x) return MOE_OK;
+  if (xn_out && (xn_out == x || xn_out == x_out)) return MOE_ERR_INVALID_ARG;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   return st_of(timed(p, 7, st, [&] {
-    return launch_residual(x, y, (long long)T * p->d.hidden, alpha, x_out, st);
+    return launch_residual_norm(x, y, T, p->d.hidden, alpha, x_out, xn_out, kRmsEps, st);
   }));
 }
 

@@ -170,57 +170,59 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
   }
   __syncthreads();
 
-  // top-k: warp w handles local tokens w, w+8, w+16, w+24
-  constexpr int VPL = TPW * 8 * 8 / 32 > 0 ? TPW * 2 : 1;   // values per lane (E <= 64*TPW)
+  // top-k: warp w handles local tokens w, w+8, w+16, w+24. A NaN logit
+  // ranks as -inf, and every round picks some not-yet-selected expert, so the
+  // indices are always valid whatever the inputs hold.
+  constexpr int VPL = TPW * 2;   // values per lane (E <= 64*TPW)
   for (int tl = warp; tl < kRouterTB; tl += 8) {
     const int t = t0 + tl;
     if (t >= T) break;
     float v[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
-      int e = lane + 32 * i;
-      v[i] = e < E ? lg_s[tl * lstride + e] : -INFINITY;
+      const int e = lane + 32 * i;
+      const float l = e < E ? lg_s[tl * lstride + e] : -INFINITY;
+      v[i] = isnan(l) ? -INFINITY : l;
     }
     if (logits_out) {
       for (int e = lane; e < E; e += 32) logits_out[(size_t)t * E + e] = lg_s[tl * lstride + e];
     }
-    float sel_v0 = 0.f, my_w = 0.f, zsum = 0.f;
+    uint32_t taken = 0;
+    float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
     int my_idx = 0;
-    float my_val = 0.f;
     for (int j = 0; j < k; ++j) {
-      // best of this lane: highest value, lowest index (i ascending -> e ascending)
+      // best unselected expert of this lane: highest logit, then lowest index
       float bv = -INFINITY;
-      int be = 0x7fffffff;
+      int be = -1;
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
-        int e = lane + 32 * i;
-        if (e < E && (v[i] > bv || (v[i] == bv && e < be))) {
+        const int e = lane + 32 * i;
+        if (e < E && !((taken >> i) & 1u) && (be < 0 || v[i] > bv || (v[i] == bv && e < be))) {
           bv = v[i];
           be = e;
         }
       }
 #pragma unroll
       for (int off = 16; off > 0; off >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (ov > bv || (ov == bv && oe < be)) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+        if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
           bv = ov;
           be = oe;
         }
       }
-      if ((be & 31) == lane) v[be >> 5] = -INFINITY;   // mark taken (owner lane)
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
       if (j == 0) sel_v0 = bv;
-      float p = expf(bv - sel_v0);
-      zsum += p;
+      const float pj = expf(bv - sel_v0);
+      zsum += pj;
       if (lane == j) {
         my_idx = be;
-        my_val = p;
+        my_val = pj;
       }
     }
     if (lane < k) {
-      my_w = my_val / zsum;
       topk_idx[(size_t)t * k + lane] = my_idx;
-      topk_w[(size_t)t * k + lane] = my_w;
+      topk_w[(size_t)t * k + lane] = my_val / zsum;
       atomicAdd(&cnt_s[my_idx], 1);
     }
   }
@@ -363,7 +365,9 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
 
 // ---------------------------------------------------------------------------
 // Gather: xs[pos] = x[perm[pos] / k] for routed positions, and
-// xs[T*k + t] = x[t] for the shared expert's rows. One warp per row.
+// xs[T*k + t] = x[t] for the shared expert's rows, converted from bf16 to the
+// GEMMs' fp16 operand type (exact inside fp16's range, saturating outside).
+// One warp per row.
 // ---------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                    int T, int k, int H, int with_shared,
@@ -377,7 +381,11 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
     const int src = r < T * k ? perm[r] / k : r - T * k;
     const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)src * H);
     uint4* d = reinterpret_cast<uint4*>(xs + (size_t)r * H);
-    for (int i = lane; i < vec; i += 32) d[i] = __ldg(s + i);
+    for (int i = lane; i < vec; i += 32) {
+      const uint4 v = __ldg(s + i);
+      d[i] = make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y),
+                        bf16x2_to_f16x2_sat(v.z), bf16x2_to_f16x2_sat(v.w));
+    }
   }
 }
 
@@ -440,34 +448,73 @@ cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* 
 }
 
 // ---------------------------------------------------------------------------
-// Residual: out = bf16(x + alpha * y), y fp32, 8 elements per thread.
+// Stack update between layers, one CTA per token row:
+//   x_out = bf16(x + alpha * y)            (y fp32; skipped when y is NULL)
+//   xn    = bf16(x_out / sqrt(mean(x_out^2) + eps))   (when xn is not NULL)
+// The mean of squares is taken over the bf16-rounded x_out, in FP32.
 // ---------------------------------------------------------------------------
-__global__ void residual_kernel(const uint16_t* __restrict__ x, const float* __restrict__ y,
-                                long long n8, float alpha, uint16_t* __restrict__ out) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n8;
-       i += (long long)gridDim.x * blockDim.x) {
-    const uint4 a = reinterpret_cast<const uint4*>(x)[i];
-    const float4 b0 = reinterpret_cast<const float4*>(y)[2 * i];
-    const float4 b1 = reinterpret_cast<const float4*>(y)[2 * i + 1];
-    const float yb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
-    const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
-    uint4 o;
-    uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+__global__ void __launch_bounds__(256) residual_norm_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ y, int T, int H, float alpha,
+    uint16_t* __restrict__ x_out, uint16_t* __restrict__ xn, float eps) {
+  __shared__ float warp_ss[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    const uint16_t* xr = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(xr + h0);
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+      float v[8];
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-      ow[j] = pack_bf16x2(fmaf(alpha, yb[2 * j], bf16_lo(aw[j])),
-                          fmaf(alpha, yb[2 * j + 1], bf16_hi(aw[j])));
-    reinterpret_cast<uint4*>(out)[i] = o;
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = bf16_lo(aw[j]);
+        v[2 * j + 1] = bf16_hi(aw[j]);
+      }
+      if (y) {
+        const float4* yr = reinterpret_cast<const float4*>(y + (size_t)t * H + h0);
+        const float4 b0 = yr[0], b1 = yr[1];
+        const float yb[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = fmaf(alpha, yb[j], v[j]);
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ow[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        const float r0 = bf16_lo(ow[j]), r1 = bf16_hi(ow[j]);
+        ss = fmaf(r0, r0, fmaf(r1, r1, ss));
+      }
+      if (y || x_out != x) *reinterpret_cast<uint4*>(x_out + (size_t)t * H + h0) = o;
+    }
+    if (!xn) continue;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    __syncthreads();
+    if (lane == 0) warp_ss[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_ss[w];
+    const float inv = 1.0f / sqrtf(tot / (float)H + eps);
+    // second pass over the row this thread wrote (its own values)
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>((y || x_out != x ? x_out : x) +
+                                                      (size_t)t * H + h0);
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ow[j] = pack_bf16x2(bf16_lo(aw[j]) * inv, bf16_hi(aw[j]) * inv);
+      *reinterpret_cast<uint4*>(xn + (size_t)t * H + h0) = o;
+    }
   }
 }
 
-cudaError_t launch_residual(const uint16_t* x, const float* y, long long n, float alpha,
-                            uint16_t* out, cudaStream_t st) {
-  long long n8 = n / 8;
-  long long blocks = (n8 + 255) / 256;
-  if (blocks > 4096) blocks = 4096;
-  if (blocks < 1) blocks = 1;
-  residual_kernel<<<(int)blocks, 256, 0, st>>>(x, y, n8, alpha, out);
+cudaError_t launch_residual_norm(const uint16_t* x, const float* y, int T, int H, float alpha,
+                                 uint16_t* x_out, uint16_t* xn, float eps, cudaStream_t st) {
+  int blocks = T < 8192 ? T : 8192;
+  residual_norm_kernel<<<blocks, 256, 0, st>>>(x, y, T, H, alpha, x_out, xn, eps);
   return cudaGetLastError();
 }
 

@@ -3,8 +3,8 @@
 ``make_layer`` materialises one layer's tensors (router, routed experts,
 shared expert) on a device from the seeded generator in ``synth`` and keeps
 the ``MoeExperts`` structs the C ABI takes. ``run_stack`` chains layers with
-the residual update ``x <- bf16(x + alpha * moe(x))``, every step through the
-C ABI.
+the residual update ``x <- bf16(x + alpha * moe(rmsnorm(x)))``, every step
+through the C ABI.
 """
 from __future__ import annotations
 
@@ -55,20 +55,18 @@ def residual_alpha(num_layers: int) -> float:
     return 1.0 / math.sqrt(num_layers)
 
 
-def run_stack(plan: int, x: torch.Tensor, layers: List[DeviceLayer], T: int,
-              y_buf: torch.Tensor, alpha: float, stream=None,
-              y_per_layer: Optional[List[torch.Tensor]] = None,
-              x_per_layer: Optional[List[torch.Tensor]] = None) -> torch.Tensor:
-    """Run the layers in order on ``x`` (updated in place) and return it.
+def run_stack(plan: int, x: torch.Tensor, xn: torch.Tensor, layers: List[DeviceLayer], T: int,
+              y_buf: torch.Tensor, alpha: float, stream=None) -> torch.Tensor:
+    """Run the layers in order on the residual stream ``x`` (bf16, updated in
+    place) and return it. Every layer sees the RMS-normalised stream ``xn``
+    (bf16 scratch of x's shape); ``y_buf`` is the fp32 [T, H] layer output.
 
-    When ``y_per_layer`` / ``x_per_layer`` are given, each layer's output and
-    input are copied there (for parity checks)."""
-    for i, L in enumerate(layers):
-        if x_per_layer is not None:
-            x_per_layer[i].copy_(x[:T])
-        binding.moe_forward_layer(plan, x, T, L.router_w, L.router_bias, L.routed_c, L.shared_c,
-                                  y_buf, stream)
-        if y_per_layer is not None:
-            y_per_layer[i].copy_(y_buf[:T])
-        binding.moe_residual_add(plan, x, y_buf, T, alpha, x, stream)
+        xn = rmsnorm(x)
+        for each layer: y = moe(xn); x = bf16(x + alpha * y); xn = rmsnorm(x)
+    """
+    binding.moe_residual_add(plan, x, None, T, 0.0, x, xn, stream)
+    for L in layers:
+        binding.moe_forward_layer(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
+                                  L.shared_c, y_buf, stream)
+        binding.moe_residual_add(plan, x, y_buf, T, alpha, x, xn, stream)
     return x

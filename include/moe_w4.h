@@ -160,11 +160,18 @@ moe_status moe_forward_layer(moe_plan_t plan, const uint16_t* x, int T,
                              const moe_experts* routed, const moe_experts* shared,
                              float* y, moe_stream_t stream);
 
-/* Residual update between stacked layers: x_out[i] = bf16(x[i] + alpha*y[i])
- * over T*H elements; x and x_out bf16, y f32, FP32 arithmetic. x_out may
- * equal x. */
+/* Update between stacked layers (not part of the expert block itself):
+ *   x_out[t] = bf16(x[t] + alpha * y[t])                 (skipped if y == NULL)
+ *   xn_out[t] = bf16(x_out[t] / sqrt(mean_h x_out[t][h]^2 + 1e-6))
+ *                                                        (skipped if NULL)
+ * x, x_out, xn_out bf16 [T][H]; y f32 [T][H]; FP32 arithmetic, the mean of
+ * squares over the bf16-rounded x_out. x_out may equal x (NULL means x);
+ * xn_out must be a separate buffer. xn_out is the RMS-normalised input of
+ * the next layer: without it the SwiGLU experts, quadratic in their input,
+ * make a residual stack grow without bound. */
 moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, int T,
-                            float alpha, uint16_t* x_out, moe_stream_t stream);
+                            float alpha, uint16_t* x_out, uint16_t* xn_out,
+                            moe_stream_t stream);
 
 /* Reads and clears the plan's device error word. Synchronises the device:
  * call it between layers or steps, never inside one. Returns MOE_OK,
@@ -190,8 +197,8 @@ moe_status moe_enable_timing(moe_plan_t plan, int on);
 moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
 
 /* Introspection of plan scratch for tests and profiling: device address of
- * the gathered activations (which = 0: bf16 [rows][H], routed positions
- * first, then the shared expert's T rows), the SwiGLU activations (1: bf16
+ * the gathered activations (which = 0: fp16 [rows][H], routed positions
+ * first, then the shared expert's T rows), the SwiGLU activations (1: fp16
  * [rows][I]), the weighted routed expert outputs (2: bf16 [T*k][H]) or the
  * shared expert's outputs (3: f32 [T][H]) of the last layer. NULL for an
  * unknown `which` or a plan without a shared expert (3). */

@@ -61,6 +61,7 @@ def _bind(lib):
     lib.oracle_moe_rows.argtypes = ([_P, _I, _I, _I, _I, _I, _I, _P, _P] + [_P] * 18
                                     + [_P, _I, _I, _P, _P, _P, _P, _P])
     lib.oracle_residual.argtypes = [_P, _P, _I, ctypes.c_double, _P]
+    lib.oracle_rmsnorm.argtypes = [_P, _I, _I, ctypes.c_double, _P]
     lib.oracle_w4_bits_per_weight.restype = ctypes.c_double
     lib.oracle_w4_bits_per_weight.argtypes = [_I]
     lib.oracle_planted.restype = _I
@@ -195,6 +196,14 @@ class Oracle:
                                  self._p(rows_a), n, int(nthreads), self._p(logits),
                                  self._p(idx), self._p(w), self._p(gap), self._p(y))
         return dict(logits=logits, topk_idx=idx, topk_w=w, gap=gap, y=y)
+
+    def rmsnorm(self, x, eps: float = 1e-6) -> np.ndarray:
+        """Row-wise x / sqrt(mean(x^2) + eps) of bf16 rows, rounded to bf16."""
+        x = np.ascontiguousarray(x, np.uint16)
+        rows, H = (1, x.shape[0]) if x.ndim == 1 else x.shape
+        out = np.empty_like(x)
+        self.lib.oracle_rmsnorm(self._p(x), rows, H, float(eps), self._p(out))
+        return out
 
     def residual(self, x, y, alpha: float) -> np.ndarray:
         x = np.ascontiguousarray(x, np.uint16)

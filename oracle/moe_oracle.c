@@ -361,6 +361,25 @@ void oracle_residual(const uint16_t* x, const double* y, int n, double alpha,
     x_next[i] = oracle_f64_to_bf16(oracle_bf16_to_f64(x[i]) + alpha * y[i]);
 }
 
+/* RMS normalisation of each row (the stacked layers' input):
+ *   out[r][h] = bf16(x[r][h] / sqrt(mean_h x[r][h]^2 + eps)), in fp64. */
+void oracle_rmsnorm(const uint16_t* x, int rows, int H, double eps, uint16_t* out) {
+  for (int r = 0; r < rows; ++r) {
+    double ss = 0.0;
+    for (int h = 0; h < H; ++h) {
+      double v = oracle_bf16_to_f64(x[(size_t)r * H + h]);
+      ss += v * v;
+    }
+#if ORACLE_PLANT == 12
+    double den = ss / H + eps;                /* planted: square root dropped */
+#else
+    double den = sqrt(ss / H + eps);
+#endif
+    for (int h = 0; h < H; ++h)
+      out[(size_t)r * H + h] = oracle_f64_to_bf16(oracle_bf16_to_f64(x[(size_t)r * H + h]) / den);
+  }
+}
+
 /* Storage accounting of the 4-bit affine format: bits per weight for group
  * size G with one 16-bit scale and one 16-bit bias per group. */
 double oracle_w4_bits_per_weight(int G) { return 4.0 + 2.0 * 16.0 / (double)G; }

@@ -308,7 +308,24 @@ def pin_residual(orc):
     assert np.array_equal(got, f64_to_bf16_bits_via_f32(y))
 
 
+def pin_rmsnorm(orc):
+    # constant rows normalise to +-1 (closed form); output mean square is 1
+    # up to bf16 rounding; scaling a row by a power of two changes nothing
+    c = np.array([orc.f64_to_bf16(v) for v in (3.0, -0.25, 96.0)], np.uint16)
+    rows = np.repeat(c[:, None], 64, axis=1)
+    out = bits_to_f64(orc.rmsnorm(rows))
+    assert np.array_equal(out, np.sign(bits_to_f64(c))[:, None] * np.ones((3, 64)))
+    rng = np.random.default_rng(13)
+    x = rand_bf16(rng, (6, 512), -5, 5)
+    xn = bits_to_f64(orc.rmsnorm(x))
+    assert np.allclose(np.mean(xn ** 2, axis=1), 1.0, rtol=0, atol=5e-3)
+    assert np.array_equal(np.sign(xn), np.sign(bits_to_f64(x)))
+    x4 = f64_to_bf16_bits_via_f32(bits_to_f64(x) * 4.0)
+    d = np.abs(bits_to_f64(orc.rmsnorm(x4)) - xn)
+    assert np.all(d <= 2.0 ** -7 * np.abs(xn) + 1e-30)
+
+
 ALL_PINS = [pin_bf16, pin_dequant_integer, pin_dequant_bias_only, pin_dequant_one_hot,
             pin_router_library, pin_topk_bruteforce, pin_topk_ties, pin_topk_weights,
             pin_route_maps, pin_ffn_odd_identity, pin_ffn_zero_gate, pin_layer_k1,
-            pin_layer_shared_weight_one, pin_residual]
+            pin_layer_shared_weight_one, pin_residual, pin_rmsnorm]

@@ -1,19 +1,22 @@
-"""GPU parity of the stacked layers (residual x <- bf16(x + moe(x)/sqrt(L))).
+"""GPU parity of the stacked layers:
+    xn = rmsnorm(x); y = moe(xn); x <- bf16(x + y/sqrt(L))
 
 The full-size prefill stack (T=4096, 40 layers, Zipf routing, ~18 GB of packed
-weights) runs on the GPU in the launch configuration the benchmark times; the
-oracle follows a sample of tokens through all 40 layers on its own (fp64,
-from the generator's inputs, never from GPU values). Per layer, for every
-sampled token whose routing has not yet diverged, routing indices must match
-exactly where the oracle's logit gap is >= 1e-3 and the output must be within
-2e-2 * rms. A token whose gap falls below 1e-3 may legitimately route
-differently (its logits differ by more than the gap after the GPU's bf16
-residual rounding), and is followed no further. The full routing arrays of
-every layer are checked for the invariants any correct map has.
+weights) runs on the GPU in the launch configuration the benchmark times. The
+oracle follows a sample of tokens through all 40 layers on its own, in fp64,
+from the generator's inputs; no oracle input ever comes from the GPU. At each
+layer the GPU also runs the layer on a copy of its own batch in which the
+sampled rows are replaced by the oracle's normalised inputs (same T, same
+grid, the rest of the batch keeps the GPU's routing context). On those rows:
+  * routing indices must equal the oracle's wherever the oracle's 8th/9th
+    logit gap is >= 1e-3;
+  * outputs must satisfy max|y_gpu - y_oracle| <= 2e-2 * rms(y_oracle) over
+    the compared rows of the layer.
+The GPU's own chain is checked at every layer for the invariants any correct
+routing map has.
 
-The decode stack (T = 8, 40 layers) is followed token by token the same way.
+The decode stack (T = 8, 40 layers) is checked the same way on all 8 rows.
 """
-import dataclasses
 import os
 
 import numpy as np
@@ -37,68 +40,78 @@ def built():
     bg.load_library()
 
 
-def oracle_layer_for_rows(L: stack.DeviceLayer, x_rows_bits: np.ndarray, sh: synth.MoEShape):
-    """Oracle on the given token rows of one layer, copying to the host only
-    the experts the oracle's own routing selects (plus router and shared)."""
+def oracle_layer_for_rows(L: stack.DeviceLayer, xn_bits: np.ndarray, sh: synth.MoEShape):
+    """Oracle on the given normalised rows of one layer, copying to the host
+    only the experts the oracle's own routing selects (plus router and shared)."""
     orc = oracle.get()
     wr = parity.bits(L.router_w)
     rb = None if L.router_bias is None else L.router_bias.cpu().numpy()
-    logits = orc.router_logits(x_rows_bits, wr, rb)
+    logits = orc.router_logits(xn_bits, wr, rb)
     idx, _, _ = orc.topk(logits, sh.top_k)
     need = sorted(set(idx.reshape(-1).tolist()))
     routed = {}
     for m, (q, s, b) in L.routed.items():
         qh = np.zeros(tuple(q.shape), np.uint32)
-        sh_ = np.zeros(tuple(s.shape), np.uint16)
+        shh = np.zeros(tuple(s.shape), np.uint16)
         bh = np.zeros(tuple(b.shape), np.uint16)
         for e in need:
             qh[e] = parity.words(q[e])
-            sh_[e] = parity.bits(s[e])
+            shh[e] = parity.bits(s[e])
             bh[e] = parity.bits(b[e])
-        routed[m] = (qh, sh_, bh)
+        routed[m] = (qh, shh, bh)
     shared = parity.host_set(L.shared) if L.shared is not None else None
-    return orc.moe_rows(x_rows_bits, wr, rb, routed, shared, sh.top_k, sh.group_size,
+    return orc.moe_rows(xn_bits, wr, rb, routed, shared, sh.top_k, sh.group_size,
                         nthreads=NTHREADS)
 
 
-def run_chain_check(w: synth.Workload, sample_rows, gemm_path=0):
+def to_dev_bits(b: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(b.view(np.int16).copy()).cuda().view(torch.bfloat16)
+
+
+def run_chain_check(w: synth.Workload, rows: np.ndarray):
     sh = w.shape
     T = w.tokens
     layers = stack.make_layers(w, "cuda")
-    d = bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k, sh.group_size,
-                     int(sh.has_shared), T, 128, gemm_path)
-    plan = bg.moe_plan_create(d, 0)
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
     alpha = stack.residual_alpha(w.layers)
+    orc = oracle.get()
+    stats = []
     try:
         x = synth.tokens_x(w, "cuda")
-        x0 = parity.bits(x)[sample_rows]
+        xn = torch.empty_like(x)
         y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
-        orc = oracle.get()
-        xo = x0.copy()                     # oracle's own chain for the sampled rows
-        alive = np.ones(len(sample_rows), bool)
-        compared = 0
-        worst = 0.0
+        y_chk = torch.empty_like(y)
+        xo = parity.bits(x)[rows]                    # oracle's own chain
+        bg.moe_residual_add(plan, x, None, T, 0.0, x, xn)
+        rows_t = torch.from_numpy(rows.astype(np.int64)).cuda()
         for li, L in enumerate(layers):
-            r = bg.moe_route(plan, x, T, L.router_w, L.router_bias)
+            # the GPU chain
+            r = bg.moe_route(plan, xn, T, L.router_w, L.router_bias)
             g = parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)
             check_route_invariants(g, g["topk_idx"], sh.num_experts, 128)
-            bg.moe_forward_layer(plan, x, T, L.router_w, L.router_bias, L.routed_c, L.shared_c, y)
-            yg = y.double().cpu().numpy()[sample_rows]
-            o = oracle_layer_for_rows(L, xo, sh)
-            gidx = g["topk_idx"][sample_rows]
-            for i in range(len(sample_rows)):
-                if not alive[i]:
-                    continue
-                if o["gap"][i] < parity.GAP_MIN:
-                    alive[i] = False          # routing may differ from here on
-                    continue
-                assert np.array_equal(gidx[i], o["topk_idx"][i]), (li, i)
-                worst = max(worst, parity.check_y(yg[i], o["y"][i]))
-                compared += 1
-            bg.moe_residual_add(plan, x, y, T, alpha, x)
+            bg.moe_forward_layer(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
+                                 L.shared_c, y)
+            # the same layer on the oracle's inputs for the sampled rows
+            xon = orc.rmsnorm(xo)
+            xin = xn.clone()
+            xin[rows_t] = to_dev_bits(xon)
+            rc = bg.moe_route(plan, xin, T, L.router_w, L.router_bias)
+            gidx = parity.routing_to_numpy(rc, T, sh.top_k, sh.num_experts)["topk_idx"][rows]
+            bg.moe_forward_layer(plan, xin, T, L.router_w, L.router_bias, L.routed_c,
+                                 L.shared_c, y_chk)
+            o = oracle_layer_for_rows(L, xon, sh)
+            ok = o["gap"] >= parity.GAP_MIN
+            assert np.array_equal(gidx[ok], o["topk_idx"][ok]), li
+            yg = y_chk.double().cpu().numpy()[rows]
+            ratio = parity.check_y(yg[ok], o["y"][ok])
+            stats.append((li, int(ok.sum()), ratio))
+            # advance both chains
+            bg.moe_residual_add(plan, x, y, T, alpha, x, xn)
             xo = orc.residual(xo, o["y"], alpha)
         assert bg.moe_get_error(plan) == 0
-        return compared, alive, worst
+        assert np.isfinite(x.float().cpu().numpy()).all()
+        return stats
     finally:
         bg.moe_plan_destroy(plan)
 
@@ -106,12 +119,11 @@ def run_chain_check(w: synth.Workload, sample_rows, gemm_path=0):
 def test_prefill_stack_t4096_l40_sampled():
     w = synth.standard_workloads()["prefill_t4096_l40_zipf"]
     rows = np.array([0, 1, 777, 2048, 3333, 4095], np.int32)
-    compared, alive, worst = run_chain_check(w, rows)
-    assert compared >= 0.5 * len(rows) * w.layers, (compared, alive)
+    stats = run_chain_check(w, rows)
+    assert sum(n for _, n, _ in stats) >= 0.9 * len(rows) * w.layers, stats
 
 
 def test_decode_stack_t8_l40():
     w = synth.standard_workloads()["decode_t8_l40"]
-    rows = np.arange(8, dtype=np.int32)
-    compared, alive, worst = run_chain_check(w, rows)
-    assert compared >= 0.5 * len(rows) * w.layers, (compared, alive)
+    stats = run_chain_check(w, np.arange(8, dtype=np.int32))
+    assert sum(n for _, n, _ in stats) >= 0.9 * 8 * w.layers, stats

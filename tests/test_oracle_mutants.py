@@ -17,6 +17,7 @@ PLANTS = {
     9: "router bias sign flipped",
     10: "down matrix transposed",
     11: "shared expert dropped",
+    12: "rms norm without square root",
 }
 
 
