@@ -87,6 +87,7 @@ def load_library(path: Optional[str] = None):
         "moe_read_timing": (S, [P, ctypes.POINTER(MoeTiming)]),
         "moe_last_gemm_path": (I, [P]),
         "moe_debug_buffer": (P, [P, I]),
+        "moe_route_noalloc": (S, [P, I, I, P, P, I, I, ctypes.POINTER(MoeRouting), P]),
         "moe_status_string": (ctypes.c_char_p, [S]),
         "moe_version": (I, []),
     }
@@ -173,6 +174,15 @@ def moe_forward_layer(plan: int, x, T: int, router_w, router_bias, routed: MoeEx
         plan, _ptr(x), T, _ptr(router_w), _ptr(router_bias), ctypes.byref(routed),
         ctypes.byref(shared) if shared is not None else None, _ptr(y), _stream(stream)),
         "moe_forward_layer")
+
+
+def moe_route_noalloc(x, T: int, hidden: int, router_w, router_bias, num_experts: int,
+                      top_k: int, out: MoeRouting, stream=None) -> None:
+    """Routing into caller-owned buffers with no device allocation (see header)."""
+    _check(load_library().moe_route_noalloc(_ptr(x), T, hidden, _ptr(router_w),
+                                            _ptr(router_bias), num_experts, top_k,
+                                            ctypes.byref(out), _stream(stream)),
+           "moe_route_noalloc")
 
 
 def moe_residual_add(plan: int, x, y, T: int, alpha: float, x_out=None, xn_out=None,

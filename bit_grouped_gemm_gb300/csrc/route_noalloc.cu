@@ -1,0 +1,86 @@
+// route_noalloc.cu -- routing for callers that cannot allocate device memory.
+//
+// moe_route needs a plan, and a plan allocates its scratch with cudaMalloc.
+// Some callers cannot do that: code running inside another framework's
+// memory pool or graph-capture region (where a cudaMalloc would break the
+// capture or force a device-wide synchronisation), allocator-less embedded
+// runtimes, and callbacks that must not block. moe_route_noalloc serves
+// them: the caller passes inputs and every output buffer, and the only
+// scratch the routing kernels need (the per-token-block expert counts) lives
+// in a fixed array in this file, sized for at most kMaxTokens tokens and
+// kMaxExperts experts.
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace {
+
+constexpr int kMaxTokens = 4096;
+constexpr int kMaxExperts = 512;
+constexpr int kMaxBlocks = (kMaxTokens + moe::kRouterTB - 1) / moe::kRouterTB;
+constexpr int kMaxDevices = 64;
+
+// Per-token-block expert counts, then the blocks' offsets into each
+// expert's segment: 128 x 512 int32 = 256 KB on every GPU that loads the
+// library, kept until the process exits. Every call overwrites all entries
+// it reads, so nothing needs clearing between calls; calls that overlap on
+// the GPU (different streams, no ordering) race on it.
+static __device__ __align__(256) int32_t g_blk_cnt[kMaxBlocks * kMaxExperts];
+
+std::mutex g_mu;
+int32_t* g_blk_cnt_addr[kMaxDevices] = {};
+
+// Device address of g_blk_cnt on the current device. In host code the name
+// g_blk_cnt is only a host-side stand-in, so the address is looked up once
+// per device, with that device current, and reused.
+moe_status scratch_address(int32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_blk_cnt_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_blk_cnt) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    g_blk_cnt_addr[dev] = static_cast<int32_t*>(p);
+  }
+  *out = g_blk_cnt_addr[dev];
+  return MOE_OK;
+}
+
+bool al(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+
+extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
+                                        const uint16_t* router_w, const float* router_bias,
+                                        int num_experts, int top_k, const moe_routing* out,
+                                        moe_stream_t stream) {
+  if (!x || !router_w || !out) return MOE_ERR_INVALID_ARG;
+  if (T < 1 || hidden <= 0 || hidden % 32 || num_experts < 8 || num_experts % 8 ||
+      top_k < 1 || top_k > num_experts)
+    return MOE_ERR_INVALID_ARG;
+  if (T > kMaxTokens || num_experts > kMaxExperts || top_k > 32) return MOE_ERR_CAPACITY;
+  if (!al(x, 16) || !al(router_w, 16) || (router_bias && !al(router_bias, 4)))
+    return MOE_ERR_INVALID_ARG;
+  const void* need[] = {out->topk_idx, out->topk_w, out->counts, out->offsets,
+                        out->tile_offsets, out->perm, out->inv, out->block_map, out->num_tiles};
+  for (const void* q : need)
+    if (!q || !al(q, 4)) return MOE_ERR_INVALID_ARG;
+  if (out->logits && !al(out->logits, 4)) return MOE_ERR_INVALID_ARG;
+
+  int32_t* blk = nullptr;
+  moe_status s = scratch_address(&blk);
+  if (s != MOE_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  const int nblk = (T + moe::kRouterTB - 1) / moe::kRouterTB;
+  if (moe::launch_router_topk(x, T, hidden, router_w, router_bias, num_experts, top_k,
+                              out->topk_idx, out->topk_w, out->logits, blk, st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe::launch_route_scan(blk, nblk, T, top_k, num_experts, out->counts, out->offsets,
+                             out->tile_offsets, out->block_map, out->num_tiles,
+                             st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (moe::launch_route_scatter(out->topk_idx, blk, T, top_k, num_experts, out->perm, out->inv,
+                                st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}

@@ -173,6 +173,28 @@ moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, 
                             float alpha, uint16_t* x_out, uint16_t* xn_out,
                             moe_stream_t stream);
 
+/* Routing without a plan and without any device allocation. The pages have
+ * no counterpart: this entry point exists for callers that cannot call
+ * cudaMalloc -- code running inside another framework's memory pool or
+ * stream-capture region (where an allocation would break the capture or
+ * synchronise the device), allocator-less embedded runtimes, callbacks that
+ * must not block. It computes exactly what moe_route computes, with the
+ * same kernels.
+ * The caller passes x, router_w, router_bias (may be NULL) as for moe_route
+ * and every output buffer in `out` (layouts as in moe_routing; block_map
+ * must hold ceil(T*k/128) + E triples; logits may be NULL). The library's
+ * only scratch for this call is a fixed device array of 128 x 512 int32
+ * (256 KB) in the library image, present on every GPU that loads the
+ * library until the process exits; hence T <= 4096 and num_experts <= 512,
+ * and larger requests return MOE_ERR_CAPACITY. Nothing in that array needs
+ * clearing between calls. The first call on a device looks up the array's
+ * device address (with that device current); make that first call before
+ * any stream capture. All calls share the array: calls that can overlap on
+ * the GPU (different streams without ordering) race and must not be made. */
+moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden, const uint16_t* router_w,
+                             const float* router_bias, int num_experts, int top_k,
+                             const moe_routing* out, moe_stream_t stream);
+
 /* Reads and clears the plan's device error word. Synchronises the device:
  * call it between layers or steps, never inside one. Returns MOE_OK,
  * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA if the context has failed. */

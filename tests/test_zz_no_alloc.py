@@ -1,0 +1,76 @@
+"""moe_route_noalloc (routing with no device allocation inside the library)
+against moe_route, through the C ABI.
+
+Callers that cannot call cudaMalloc -- code inside another framework's
+memory pool or capture region, allocator-less runtimes -- pass every output
+buffer themselves; the library's only scratch for this call is a fixed
+device array. The test allocates the output buffers (the entry point does
+not), runs two calls in a row with different inputs, and requires the same
+routing as the plan-based entry point: integer arrays exactly, top-k weights
+within the 1e-5 tolerance of the other routing tests.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from bit_grouped_gemm_gb300 import binding as bg
+from bit_grouped_gemm_gb300 import stack, synth
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from bit_grouped_gemm_gb300 import build
+    build.build()
+    bg.load_library()
+
+
+def caller_buffers(T, k, E):
+    max_tiles = (T * k + 127) // 128 + E
+    z = lambda n, dt=torch.int32: torch.zeros(n, dtype=dt, device="cuda")
+    bufs = dict(topk_idx=z(T * k), topk_w=z(T * k, torch.float32), counts=z(E),
+                offsets=z(E + 1), tile_offsets=z(E + 1), perm=z(T * k), inv=z(T * k),
+                block_map=z(max_tiles * 3), num_tiles=z(4), logits=z(T * E, torch.float32))
+    r = bg.MoeRouting(**{n: t.data_ptr() for n, t in bufs.items()})
+    return bufs, r
+
+
+@pytest.mark.parametrize("name", ["t512_zipf", "t128_uniform"])
+def test_noalloc_routing_matches_moe_route_twice(name):
+    w = synth.standard_workloads()[name]
+    sh = w.shape
+    layers = [stack.make_layer(w, 0, "cuda"), stack.make_layer(w, 1, "cuda")]
+    xs = [synth.tokens_x(w, "cuda"), synth.decode_pool(w, 1, "cuda")[0]]
+    plan = bg.moe_plan_create(bg.plan_desc(max_tokens=w.tokens), 0)
+    try:
+        for call in range(2):                          # two calls in a row
+            L, x = layers[call], xs[call]
+            ref = parity.routing_to_numpy(
+                bg.moe_route(plan, x, w.tokens, L.router_w, L.router_bias),
+                w.tokens, sh.top_k, sh.num_experts)
+            bufs, r = caller_buffers(w.tokens, sh.top_k, sh.num_experts)
+            bg.moe_route_noalloc(x, w.tokens, sh.hidden, L.router_w, L.router_bias,
+                                 sh.num_experts, sh.top_k, r)
+            got = parity.routing_to_numpy(r, w.tokens, sh.top_k, sh.num_experts)
+            for key in ("topk_idx", "counts", "offsets", "tile_offsets", "perm", "inv",
+                        "block_map"):
+                assert np.array_equal(got[key], ref[key]), (call, key)
+            assert got["num_tiles"] == ref["num_tiles"]
+            assert np.abs(got["topk_w"] - ref["topk_w"]).max() <= parity.W_TOL
+            assert np.abs(got["logits"] - ref["logits"]).max() <= 1e-6
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch():
+    w = synth.standard_workloads()["t128_uniform"]
+    L = stack.make_layer(w, 0, "cuda")
+    x = torch.zeros(4097, 2048, dtype=torch.bfloat16, device="cuda")
+    _, r = caller_buffers(16, 8, 256)
+    with pytest.raises(bg.MoeError) as ei:
+        bg.moe_route_noalloc(x, 4097, 2048, L.router_w, None, 256, 8, r)
+    assert ei.value.status == 4                        # MOE_ERR_CAPACITY
