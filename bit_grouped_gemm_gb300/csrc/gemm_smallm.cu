@@ -19,9 +19,10 @@
 //         sum_k w_k x_k = s * sum_k (1024+q_k) x_k + (b - 1024 s) * sum_k x_k
 //     which is exact algebra of w = q*s + b (the group sums of x are
 //     precomputed in FP32 while the tokens are staged in shared memory);
-//   * tokens are staged in shared memory with each 8-element block stored in
-//     the order (0,4,1,5,2,6,3,7), the order the nibble extraction yields, so
-//     A and B fragments agree on which k each MMA slot holds.
+//   * token rows (gathered activations, SwiGLU activations) are kept with
+//     each 8-element block in the order (0,4,1,5,2,6,3,7), the order the
+//     nibble extraction yields, so A and B fragments agree on which k each
+//     MMA slot holds without any shuffle.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -127,7 +128,8 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
   for (int pass0 = 0; pass0 < rows; pass0 += 8 * NT) {
     const int prow = min(8 * NT, rows - pass0);
     __syncthreads();
-    // stage tokens: word (4*w8 + i) of a row holds (x[8*w8 + i], x[8*w8 + i + 4])
+    // stage tokens: rows arrive in perm8 order, so word (4*w8 + i) of a row
+    // already holds (x[8*w8 + i], x[8*w8 + i + 4])
     for (int idx = threadIdx.x; idx < 8 * NT * G; idx += blockDim.x) {
       const int tr = idx / G, grp = idx - tr * G;
       float sum = 0.f;
@@ -138,10 +140,10 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
           const uint4 x8 = __ldg(src + v);
-          dst[4 * v + 0] = prmt(x8.x, x8.z, 0x5410);   // (x0, x4)
-          dst[4 * v + 1] = prmt(x8.x, x8.z, 0x7632);   // (x1, x5)
-          dst[4 * v + 2] = prmt(x8.y, x8.w, 0x5410);   // (x2, x6)
-          dst[4 * v + 3] = prmt(x8.y, x8.w, 0x7632);   // (x3, x7)
+          dst[4 * v + 0] = x8.x;   // (x0, x4)
+          dst[4 * v + 1] = x8.y;   // (x1, x5)
+          dst[4 * v + 2] = x8.z;   // (x2, x6)
+          dst[4 * v + 3] = x8.w;   // (x3, x7)
           sum += f16_lo(x8.x) + f16_hi(x8.x) + f16_lo(x8.y) + f16_hi(x8.y) +
                  f16_lo(x8.z) + f16_hi(x8.z) + f16_lo(x8.w) + f16_hi(x8.w);
         }
@@ -268,8 +270,8 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
         const int pos = m0 + pass0 + tok;
         const int h = q >> 1;
         if (p.mode == 0) {
-          const float a = silu_f32(tot[0][nt][q]) * tot[1][nt][q];
-          p.out[(size_t)pos * p.out_ld + nrow[0][h]] = f32_to_f16_sat(a);
+          const float a = silu_fast(tot[0][nt][q]) * tot[1][nt][q];
+          p.out[(size_t)pos * p.out_ld + perm8_pos(nrow[0][h])] = f32_to_f16_sat(a);
         } else if (shared) {
           float* o = p.out_sh + (size_t)(pos - p.T * p.k) * p.out_ld;
           o[nrow[0][h]] = tot[0][nt][q];

@@ -39,14 +39,15 @@ namespace tc {
 
 constexpr int kThreads = 512;
 constexpr int kBStages = 4;               // activation chunks (64 K) in flight
-constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
+constexpr int kQStages = 4;               // packed-weight chunks (256 K) in flight
 constexpr int kAStages = 4;               // TMEM weight stages (64 K)
 constexpr int kBTileBytes = 128 * 128;    // 128 token rows x 64 fp16
 constexpr int kQTileBytes = 128 * 128;    // 128 weight rows x 32 words
 constexpr int kQStageBytes = 2 * kQTileBytes;
 constexpr int kOffB = 0;
 constexpr int kOffQ = kOffB + kBStages * kBTileBytes;
-constexpr int kOffBar = kOffQ + kQStages * kQStageBytes;
+constexpr int kOffW = kOffQ + kQStages * kQStageBytes;   // epilogue row weights [4][128]
+constexpr int kOffBar = kOffW + 4 * 128 * 4;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 0, kAccCol1 = 128, kAStageCol = 256;
@@ -98,10 +99,25 @@ __device__ __forceinline__ int block_row0(const Params& p, int j, int blk) {
   return p.mode == 0 ? 128 * j : 256 * j + 128 * blk;
 }
 
+#ifdef MOE_TC_STATS
+// Profiling build only: cycles each role spends in each wait site, and in
+// total, summed over CTAs (read with moe_debug_tc_stats).
+__device__ unsigned long long g_tc_stats[64];   // [mode*32 + site], roles at +16
+#define TC_STAT_BEGIN() const long long tc_t0 = clock64()
+#define TC_STAT_END(site) atomicAdd(&g_tc_stats[tc_stat_base + (site)], (unsigned long long)(clock64() - tc_t0))
+#else
+#define TC_STAT_BEGIN()
+#define TC_STAT_END(site)
+#endif
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          const DevErr& err, int site) {
+                                          const DevErr& err, int site, int tc_stat_base = 0) {
+  TC_STAT_BEGIN();
   bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
   ok = __all_sync(0xffffffffu, ok);
+#ifdef MOE_TC_STATS
+  if ((threadIdx.x & 31) == 0) TC_STAT_END(site);
+#endif
   if (!ok) {
     if ((threadIdx.x & 31) == 0 && !*abort_flag) report_timeout(err, site);
     *abort_flag = 1;
@@ -111,8 +127,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 
 __device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity,
                                             volatile int* abort_flag, const DevErr& err,
-                                            int site) {
+                                            int site, int tc_stat_base = 0) {
+  TC_STAT_BEGIN();
   bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
+  TC_STAT_END(site);
   if (!ok) {
     if (!*abort_flag) report_timeout(err, site);
     *abort_flag = 1;
@@ -175,6 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+#ifdef MOE_TC_STATS
+  const long long role_t0 = clock64();
+#endif
 
   const int n_routed = *p.num_tiles;
   const int n_shared = p.has_shared ? (p.T + kBM - 1) / kBM : 0;
@@ -183,28 +204,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   const int kgroups = p.K / 64;
 
   if (warp == 0) {
-    // ------------------------------------------------------ TMA producer
+    // ------------------------------------------ TMA producer: activations
     if (lane == 0) {
-      uint32_t bcnt = 0, qcnt = 0;
+      uint32_t bcnt = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit U = decode_unit(p, u, n_routed);
-        const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
-        const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
-        const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
-        const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
         for (int c = 0; c < nchunk && ok; ++c) {
-          if ((c & 3) == 0) {
-            const int s = qcnt % kQStages;
-            if (!(ok = thread_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1)))
-              break;
-            mbar_arrive_expect_tx(&q_full[s], kQStageBytes);
-            tma_load_2d(smem_q + s * kQStageBytes, m0, 32 * (c >> 2), y0, &q_full[s]);
-            tma_load_2d(smem_q + s * kQStageBytes + kQTileBytes, m1, 32 * (c >> 2), y1, &q_full[s]);
-            ++qcnt;
-          }
           const int s = bcnt % kBStages;
-          if (!(ok = thread_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2)))
+          if (!(ok = thread_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2, 32 * p.mode)))
             break;
           mbar_arrive_expect_tx(&b_full[s], kBTileBytes);
           tma_load_2d(smem_b + s * kBTileBytes, &p.maps.b, 64 * c, U.m0, &b_full[s]);
@@ -214,11 +222,36 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       if (!ok) {
         // let this CTA's own copies land before shared memory is released
         for (int s = 0; s < kBStages; ++s) {
-          uint32_t uses = (bcnt + kBStages - 1 - s) / kBStages;
+          const uint32_t uses = (bcnt + kBStages - 1 - s) / kBStages;
           if (uses) mbar_wait_drain(&b_full[s], (uses - 1) & 1, p.err.limit_ns);
         }
+      }
+    }
+  } else if (warp == 2) {
+    // ------------------------------------- TMA producer: packed weights
+    // (its own thread, so weight tiles run ahead of the activation ring)
+    if (lane == 0) {
+      uint32_t qcnt = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+        const Unit U = decode_unit(p, u, n_routed);
+        const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
+        const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
+        const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
+        const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
+        for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
+          const int s = qcnt % kQStages;
+          if (!(ok = thread_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1, 32 * p.mode)))
+            break;
+          mbar_arrive_expect_tx(&q_full[s], kQStageBytes);
+          tma_load_2d(smem_q + s * kQStageBytes, m0, 32 * qc, y0, &q_full[s]);
+          tma_load_2d(smem_q + s * kQStageBytes + kQTileBytes, m1, 32 * qc, y1, &q_full[s]);
+          ++qcnt;
+        }
+      }
+      if (!ok) {
         for (int s = 0; s < kQStages; ++s) {
-          uint32_t uses = (qcnt + kQStages - 1 - s) / kQStages;
+          const uint32_t uses = (qcnt + kQStages - 1 - s) / kQStages;
           if (uses) mbar_wait_drain(&q_full[s], (uses - 1) & 1, p.err.limit_ns);
         }
       }
@@ -232,12 +265,12 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         const Unit U = decode_unit(p, u, n_routed);
         const int ntok = (U.rows + 15) & ~15;
         const uint32_t idesc = idesc_f16_f32(128, ntok);
-        if (!(ok = thread_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3))) break;
+        if (!(ok = thread_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
         tc_fence_after();
         for (int c = 0; c < nchunk; ++c) {
           const int bs = bcnt % kBStages, as = acnt % kAStages;
-          if (!(ok = thread_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4))) break;
-          if (!(ok = thread_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5))) break;
+          if (!(ok = thread_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4, 32 * p.mode))) break;
+          if (!(ok = thread_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5, 32 * p.mode))) break;
           tc_fence_after();
           const uint32_t bbase = smem_u32(smem_b + bs * kBTileBytes);
 #pragma unroll
@@ -268,28 +301,43 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     uint32_t qcnt = 0, acnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+    // scale/bias rows of this thread's weight row in unit u
+    auto sb_rows = [&](int u, const uint16_t*& sr, const uint16_t*& br) {
       const Unit U = decode_unit(p, u, n_routed);
       const W4Dev& w = U.shared ? (blk == 0 ? p.sw0 : p.sw1) : (blk == 0 ? p.w0 : p.w1);
       const size_t row = (U.shared ? 0 : (size_t)U.e * p.N) + block_row0(p, U.j, blk) + r;
-      const uint16_t* srow = w.s + row * kgroups;
-      const uint16_t* brow = w.b + row * kgroups;
-      uint2 s4 = __ldg(reinterpret_cast<const uint2*>(srow));
-      uint2 b4 = __ldg(reinterpret_cast<const uint2*>(brow));
-      for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
+      sr = w.s + row * kgroups;
+      br = w.b + row * kgroups;
+    };
+    const uint16_t *srow = nullptr, *brow = nullptr;
+    uint2 s4 = make_uint2(0u, 0u), b4 = make_uint2(0u, 0u);
+    if ((int)blockIdx.x < units) {
+      sb_rows(blockIdx.x, srow, brow);
+      s4 = __ldg(reinterpret_cast<const uint2*>(srow));
+      b4 = __ldg(reinterpret_cast<const uint2*>(brow));
+    }
+    const int nq = nchunk / 4;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const uint16_t *nsrow = nullptr, *nbrow = nullptr;
+      for (int qc = 0; qc < nq && ok; ++qc) {
+        // scales/biases of the next 4 groups, one step ahead (also across units)
         uint2 s4n = s4, b4n = b4;
-        if (qc + 1 < nchunk / 4) {
+        if (qc + 1 < nq) {
           s4n = __ldg(reinterpret_cast<const uint2*>(srow + 4 * (qc + 1)));
           b4n = __ldg(reinterpret_cast<const uint2*>(brow + 4 * (qc + 1)));
+        } else if (u + (int)gridDim.x < units) {
+          sb_rows(u + gridDim.x, nsrow, nbrow);
+          s4n = __ldg(reinterpret_cast<const uint2*>(nsrow));
+          b4n = __ldg(reinterpret_cast<const uint2*>(nbrow));
         }
         const int qs = qcnt % kQStages;
-        if (!(ok = warp_wait(&q_full[qs], (qcnt / kQStages) & 1, abort_flag, p.err, 6))) break;
+        if (!(ok = warp_wait(&q_full[qs], (qcnt / kQStages) & 1, abort_flag, p.err, 6, 32 * p.mode))) break;
         const uint8_t* qrow = smem_q + qs * kQStageBytes + blk * kQTileBytes + r * 128;
         const uint32_t sw = r & 7;
 #pragma unroll
         for (int sub = 0; sub < 4; ++sub) {
           const int as = acnt % kAStages;
-          if (!(ok = warp_wait(&a_empty[as], ((acnt / kAStages) & 1) ^ 1, abort_flag, p.err, 7)))
+          if (!(ok = warp_wait(&a_empty[as], ((acnt / kAStages) & 1) ^ 1, abort_flag, p.err, 7, 32 * p.mode)))
             break;
           tc_fence_after();
           const uint4 wa = *reinterpret_cast<const uint4*>(qrow + (((2 * sub) ^ sw) << 4));
@@ -306,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
             uint32_t o4[4];
-            dequant_word_f16(words[i], s2, b2, o4);
+            dequant_word_f16_perm8(words[i], s2, b2, o4);
             out[4 * i + 0] = o4[0];
             out[4 * i + 1] = o4[1];
             out[4 * i + 2] = o4[2];
@@ -326,32 +374,51 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         s4 = s4n;
         b4 = b4n;
       }
+      srow = nsrow;
+      brow = nbrow;
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
     const int r = 32 * quarter + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
+    float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * quarter;   // this warp's copy
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
       const Unit U = decode_unit(p, u, n_routed);
-      if (!(ok = warp_wait(acc_full, it & 1, abort_flag, p.err, 8))) break;
+      if (p.mode == 1 && !U.shared) {
+        // top-k weights of the tile's rows, fetched while the MMAs still run
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int row = lane + 32 * i;
+          if (row < U.rows) s_w[row] = __ldg(p.topk_w + __ldg(p.perm + U.m0 + row));
+        }
+        __syncwarp();
+      }
+      if (!(ok = warp_wait(acc_full, it & 1, abort_flag, p.err, 8, 32 * p.mode))) break;
       tc_fence_after();
       for (int c0 = 0; c0 < U.rows; c0 += 32) {
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(tmem + lane_base + kAccCol0 + c0, v0);
         tmem_ld_32x32b_x32(tmem + lane_base + kAccCol1 + c0, v1);
         tmem_wait_ld();
+        if (c0 + 32 >= U.rows) {
+          // accumulators fully read: let the next unit's MMAs start now
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_empty);
+        }
         const int nval = min(32, U.rows - c0);
         if (p.mode == 0) {
-          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + r;
+          // act columns are stored in perm8 order (the down pass's K order)
+          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + perm8_pos(r);
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc) {
             if (cc < nval) {
               const float g = __uint_as_float(v0[cc]);
               const float uu = __uint_as_float(v1[cc]);
-              o[(size_t)cc * p.out_ld] = f32_to_f16_sat(silu_f32(g) * uu);
+              o[(size_t)cc * p.out_ld] = f32_to_f16_sat(silu_fast(g) * uu);
             }
           }
         } else if (U.shared) {
@@ -369,20 +436,24 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc) {
             if (cc < nval) {
-              const int pos = U.m0 + c0 + cc;
-              const float wt = __ldg(p.topk_w + __ldg(p.perm + pos));
+              const float wt = s_w[c0 + cc];
               o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * wt);
               o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * wt);
             }
           }
         }
       }
-      tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty);
     }
   }
 
+#ifdef MOE_TC_STATS
+  if (lane == 0) {
+    const int role = warp == 0 ? 0 : warp == 1 ? 1 : warp == 2 ? 2 : warp < 4 ? 3
+                   : warp < 12 ? 4 : 5;
+    atomicAdd(&g_tc_stats[32 * p.mode + 16 + role], (unsigned long long)(clock64() - role_t0));
+  }
+#endif
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
@@ -425,5 +496,14 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, D
   tc::w4_grouped_gemm_tc<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(p);
   return cudaGetLastError();
 }
+
+#ifdef MOE_TC_STATS
+extern "C" int moe_debug_tc_stats(unsigned long long* out) {
+  cudaError_t e = cudaMemcpyFromSymbol(out, tc::g_tc_stats, sizeof(tc::g_tc_stats));
+  unsigned long long z[32] = {};
+  if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_tc_stats, z, sizeof(z));
+  return (int)e;
+}
+#endif
 
 }  // namespace moe

@@ -286,11 +286,46 @@ __device__ __forceinline__ void dequant_word_f16(uint32_t w, __half2 s2, __half2
   out[3] = prmt(r[2], r[3], 0x7632);
 }
 
+// The GEMM operands' K order inside every block of 8: position p holds
+// element perm8[p] = (0,4,1,5,2,6,3,7)[p], the order in which the nibble
+// extraction above yields the eight weights of a packed word. Activations
+// stored in this order meet the dequantised weights without a shuffle.
+// perm8_pos(i) is the position of element i.
+__host__ __device__ __forceinline__ int perm8_pos(int i) {
+  return (i & ~7) | ((i & 3) << 1) | ((i >> 2) & 1);
+}
+
+// Dequantise one packed word to 4 f16x2 words in perm8 order:
+// (q0,q4) (q1,q5) (q2,q6) (q3,q7), each fp16(q * s + b) with one rounding.
+__device__ __forceinline__ void dequant_word_f16_perm8(uint32_t w, __half2 s2, __half2 b2,
+                                                       uint32_t (&out)[4]) {
+  uint32_t p[4];
+  nibbles_to_f16x2_1024(w, p);
+  const __half2 c1024 = __floats2half2_rn(1024.0f, 1024.0f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __half2 v = *reinterpret_cast<__half2*>(&p[i]);
+    v = __hfma2(__hsub2(v, c1024), s2, b2);
+    out[i] = *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// 8 fp16 in natural order (4 words) -> perm8 order
+__device__ __forceinline__ uint4 f16x8_to_perm8(uint4 v) {
+  return make_uint4(prmt(v.x, v.z, 0x5410), prmt(v.x, v.z, 0x7632), prmt(v.y, v.w, 0x5410),
+                    prmt(v.y, v.w, 0x7632));
+}
+
 // bf16 bit pattern -> fp16 (saturating) bits, the pair packed as f16x2
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
   return pack_f16x2_sat(bf16_lo(v), bf16_hi(v));
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
+// silu with the fast exponential and reciprocal (relative error ~1e-6,
+// far below the fp16 rounding of its result)
+__device__ __forceinline__ float silu_fast(float g) {
+  return g * __frcp_rn(1.0f + __expf(-g));
+}
 
 }  // namespace moe

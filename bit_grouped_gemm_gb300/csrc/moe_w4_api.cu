@@ -193,7 +193,7 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
                       cudaStream_t st) {
   const moe_plan_desc& d = p->d;
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
-  float* logits = want_logits ? p->at<float>(p->L.logits) : nullptr;
+  float* logits = p->at<float>(p->L.logits);   // the top-k kernel reads them back
   cudaError_t e;
   e = timed(p, 0, st, [&] {
     return launch_router_topk(x, T, d.hidden, router_w, router_bias, d.num_experts, d.top_k,
@@ -224,7 +224,7 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
     out->inv = p->at<int32_t>(p->L.inv);
     out->block_map = p->at<int32_t>(p->L.bmap);
     out->num_tiles = p->at<int32_t>(p->L.num_tiles);
-    out->logits = logits;
+    out->logits = want_logits ? logits : nullptr;
   }
   return MOE_OK;
 }

@@ -15,16 +15,12 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// Router logits + top-k + per-block histogram.
-//
-// One CTA = 32 tokens, 8 warps. Logits are a bf16 [32 x H] x [H x E] product
-// on mma.sync m16n8k16 (FP32 accumulate); warp w owns experts
-// [8*TPW*w, 8*TPW*(w+1)). Then each warp selects the top k of 4 tokens by k
-// rounds of a warp arg-max (higher logit first, lower index on ties), and the
-// block writes its per-expert counts to blk_cnt[block][E].
+// Router logits: logits[t][e] = sum_h x[t][h] * Wr[h][e] + bias[e], bf16
+// inputs, FP32 accumulation on mma.sync m16n8k16. One CTA computes a 64-token
+// x 64-expert tile (8 warps of 16 tokens x 32 experts) with a 3-stage
+// cp.async pipeline over K in chunks of 64.
 // ---------------------------------------------------------------------------
-constexpr int kRtK = 32;          // K chunk staged per step
-constexpr int kRtXStride = kRtK + 8;
+constexpr int kLgT = 64, kLgE = 64, kLgK = 64, kLgStages = 3, kLgStride = kLgK + 8;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -60,120 +56,94 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
-template <int TPW>  // n8 tiles per warp (E <= 64 * TPW)
-__global__ void __launch_bounds__(256) router_topk_kernel(
+__global__ void __launch_bounds__(256) router_logits_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
-    const float* __restrict__ bias, int E, int k, int32_t* __restrict__ topk_idx,
-    float* __restrict__ topk_w, float* __restrict__ logits_out, int32_t* __restrict__ blk_cnt) {
+    const float* __restrict__ bias, int E, float* __restrict__ logits) {
   extern __shared__ __align__(128) uint8_t smem[];
-  const int wstride = E + 8;                                       // bf16 elements
-  uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);              // [2][32][40]
-  uint16_t* wr_s = xs_s + 2 * kRouterTB * kRtXStride;              // [2][32][E+8]
-  float* lg_s = reinterpret_cast<float*>(smem);                    // reused: [32][E+1]
-  __shared__ int cnt_s[1024];
-
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);                  // [stage][64][72]
+  uint16_t* wr_s = xs_s + kLgStages * kLgT * kLgStride;                 // [stage][64 k][72]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * kRouterTB;
-  const int ntiles = E / 8;
+  const int t0 = blockIdx.x * kLgT, e0 = blockIdx.y * kLgE;
+  const int wm = warp & 3, wn = warp >> 2;
 
   auto stage = [&](int buf, int kc) {
-    const int k0 = kc * kRtK;
-    // x: 32 rows x 32 cols = 128 chunks of 16 B
-    if (tid < kRouterTB * 4) {
-      int r = tid >> 2, c = (tid & 3) * 8;
-      int t = t0 + r;
-      const uint16_t* src = x + (size_t)(t < T ? t : 0) * H + k0 + c;
-      cp_async16(xs_s + (buf * kRouterTB + r) * kRtXStride + c, src, t < T ? 16 : 0);
-    }
-    // Wr: 32 rows x E cols
-    const int chunks_per_row = E / 8;
-    for (int i = tid; i < kRtK * chunks_per_row; i += 256) {
-      int r = i / chunks_per_row, c = (i % chunks_per_row) * 8;
-      cp_async16(wr_s + (buf * kRtK + r) * wstride + c, wr + (size_t)(k0 + r) * E + c, 16);
+    const int k0 = kc * kLgK;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const int c = tid + 256 * i;            // 512 chunks of 16 B each for x and Wr
+      const int r = c >> 3, col = (c & 7) * 8;
+      const int t = t0 + r;
+      cp_async16(xs_s + (buf * kLgT + r) * kLgStride + col,
+                 x + (size_t)(t < T ? t : 0) * H + k0 + col, t < T ? 16 : 0);
+      const int e = e0 + col;
+      cp_async16(wr_s + (buf * kLgK + r) * kLgStride + col,
+                 wr + (size_t)(k0 + r) * E + (e < E ? e : 0), e < E ? 16 : 0);
     }
     cp_async_commit();
   };
 
-  for (int i = tid; i < E; i += 256) cnt_s[i] = 0;
+  float acc[4][4];
+#pragma unroll
+  for (int n = 0; n < 4; ++n)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
 
-  float acc[2][TPW][4];
-#pragma unroll
-  for (int m = 0; m < 2; ++m)
-#pragma unroll
-    for (int n = 0; n < TPW; ++n)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[m][n][i] = 0.f;
-
-  const int nk = H / kRtK;
-  const int tile0 = warp * TPW;
+  const int nk = H / kLgK;
   stage(0, 0);
+  if (nk > 1) stage(1, 1);
   for (int kc = 0; kc < nk; ++kc) {
-    const int buf = kc & 1;
-    if (kc + 1 < nk) {
-      stage(buf ^ 1, kc + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    if (kc + 1 < nk) cp_async_wait<1>(); else cp_async_wait<0>();
     __syncthreads();
-    if (tile0 < ntiles) {
+    if (kc + 2 < nk) stage((kc + 2) % kLgStages, kc + 2);
+    const int buf = kc % kLgStages;
 #pragma unroll
-      for (int ks = 0; ks < kRtK / 16; ++ks) {
-        uint32_t a[2][4];
+    for (int ks = 0; ks < kLgK / 16; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(smem_u32(xs_s + (buf * kLgT + wm * 16 + (lane & 15)) * kLgStride + ks * 16 +
+                       (lane >> 4) * 8), a0, a1, a2, a3);
 #pragma unroll
-        for (int m = 0; m < 2; ++m) {
-          int row = m * 16 + (lane & 15);
-          int col = ks * 16 + (lane >> 4) * 8;
-          ldsm_x4(smem_u32(xs_s + (buf * kRouterTB + row) * kRtXStride + col), a[m][0], a[m][1],
-                  a[m][2], a[m][3]);
-        }
-#pragma unroll
-        for (int np = 0; np < TPW / 2; ++np) {
-          int nt = tile0 + 2 * np;
-          if (nt < ntiles) {
-            // lanes 0-15: k rows 0..15 of tile nt; lanes 16-31: same rows, tile nt+1
-            int krow = ks * 16 + (lane & 15);
-            int ncol = (nt + (lane >> 4)) * 8;
-            uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(smem_u32(wr_s + (buf * kRtK + krow) * wstride + ncol), b0, b1, b2, b3);
-#pragma unroll
-            for (int m = 0; m < 2; ++m) {
-              mma_16816(acc[m][2 * np], a[m][0], a[m][1], a[m][2], a[m][3], b0, b1);
-              mma_16816(acc[m][2 * np + 1], a[m][0], a[m][1], a[m][2], a[m][3], b2, b3);
-            }
-          }
-        }
+      for (int np = 0; np < 2; ++np) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(smem_u32(wr_s + (buf * kLgK + ks * 16 + (lane & 15)) * kLgStride + wn * 32 +
+                           np * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
+        mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
+        mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
       }
     }
-    __syncthreads();
   }
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int n = 0; n < 4; ++n) {
+    const int e = e0 + wn * 32 + n * 8 + 2 * c;
+    if (e >= E) continue;
+    const float b0 = bias ? bias[e] : 0.f, b1 = bias ? bias[e + 1] : 0.f;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int t = t0 + wm * 16 + g + 8 * h;
+      if (t < T)
+        *reinterpret_cast<float2*>(logits + (size_t)t * E + e) =
+            make_float2(acc[n][2 * h] + b0, acc[n][2 * h + 1] + b1);
+    }
+  }
+}
 
-  // logits (+ bias) to shared memory
-  const int lstride = E + 1;
-  {
-    const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-    for (int m = 0; m < 2; ++m)
-#pragma unroll
-      for (int n = 0; n < TPW; ++n) {
-        int nt = tile0 + n;
-        if (nt < ntiles) {
-          int e0 = nt * 8 + 2 * c;
-          float b0 = bias ? bias[e0] : 0.f, b1 = bias ? bias[e0 + 1] : 0.f;
-          int r0 = m * 16 + g;
-          lg_s[r0 * lstride + e0] = acc[m][n][0] + b0;
-          lg_s[r0 * lstride + e0 + 1] = acc[m][n][1] + b1;
-          lg_s[(r0 + 8) * lstride + e0] = acc[m][n][2] + b0;
-          lg_s[(r0 + 8) * lstride + e0 + 1] = acc[m][n][3] + b1;
-        }
-      }
-  }
+// ---------------------------------------------------------------------------
+// Top-k + per-block histogram. One CTA = 32 tokens, 8 warps of 4 tokens;
+// k rounds of a warp arg-max per token (higher logit first, lower index on
+// ties; a NaN logit ranks as -inf, and every round picks some not-yet-selected
+// expert, so indices are always valid). Weights: softmax over the selected
+// logits (equal to softmax over all E renormalised over the k). The block
+// writes its per-expert counts to blk_cnt[block][E].
+// ---------------------------------------------------------------------------
+template <int VPL>   // values per lane, E <= 32 * VPL
+__global__ void __launch_bounds__(256) router_topk_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt) {
+  __shared__ int cnt_s[1024];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kRouterTB;
+  for (int i = tid; i < E; i += 256) cnt_s[i] = 0;
   __syncthreads();
-
-  // top-k: warp w handles local tokens w, w+8, w+16, w+24. A NaN logit
-  // ranks as -inf, and every round picks some not-yet-selected expert, so the
-  // indices are always valid whatever the inputs hold.
-  constexpr int VPL = TPW * 2;   // values per lane (E <= 64*TPW)
   for (int tl = warp; tl < kRouterTB; tl += 8) {
     const int t = t0 + tl;
     if (t >= T) break;
@@ -181,17 +151,13 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
-      const float l = e < E ? lg_s[tl * lstride + e] : -INFINITY;
+      const float l = e < E ? __ldg(logits + (size_t)t * E + e) : -INFINITY;
       v[i] = isnan(l) ? -INFINITY : l;
-    }
-    if (logits_out) {
-      for (int e = lane; e < E; e += 32) logits_out[(size_t)t * E + e] = lg_s[tl * lstride + e];
     }
     uint32_t taken = 0;
     float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
     int my_idx = 0;
     for (int j = 0; j < k; ++j) {
-      // best unselected expert of this lane: highest logit, then lowest index
       float bv = -INFINITY;
       int be = -1;
 #pragma unroll
@@ -234,19 +200,18 @@ cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* 
                                const float* bias, int E, int k, int32_t* topk_idx,
                                float* topk_w, float* logits, int32_t* blk_cnt,
                                cudaStream_t st) {
+  if (!logits) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)kLgStages * (kLgT + kLgK) * kLgStride * 2;
+  cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((T + kLgT - 1) / kLgT, (E + kLgE - 1) / kLgE);
+  router_logits_kernel<<<grid, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
-  size_t stage_bytes = (size_t)2 * kRouterTB * kRtXStride * 2 + (size_t)2 * kRtK * (E + 8) * 2;
-  size_t logit_bytes = (size_t)kRouterTB * (E + 1) * 4;
-  size_t smem = stage_bytes > logit_bytes ? stage_bytes : logit_bytes;
-  if (E <= 256) {
-    auto kern = router_topk_kernel<4>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<nblk, 256, smem, st>>>(x, T, H, wr, bias, E, k, topk_idx, topk_w, logits, blk_cnt);
-  } else {
-    auto kern = router_topk_kernel<8>;
-    cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<nblk, 256, smem, st>>>(x, T, H, wr, bias, E, k, topk_idx, topk_w, logits, blk_cnt);
-  }
+  if (E <= 256)
+    router_topk_kernel<8><<<nblk, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, blk_cnt);
+  else
+    router_topk_kernel<16><<<nblk, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, blk_cnt);
   return cudaGetLastError();
 }
 
@@ -291,22 +256,43 @@ __global__ void route_scan_kernel(int32_t* __restrict__ blk_cnt, int nblk, int T
   __shared__ int tot_rows, tot_tiles;
   const int e = threadIdx.x;
   const bool valid = e < E;
+  // pass 1: expert totals (independent loads, 16 in flight)
   int total = 0;
   if (valid) {
-    for (int b = 0; b < nblk; ++b) {
-      int c = blk_cnt[(size_t)b * E + e];
-      blk_cnt[(size_t)b * E + e] = total;
-      total += c;
+    int b = 0;
+    for (; b + 16 <= nblk; b += 16) {
+      int c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = blk_cnt[(size_t)(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) total += c[i];
     }
+    for (; b < nblk; ++b) total += blk_cnt[(size_t)b * E + e];
   }
-  int tiles = valid ? (total + kBM - 1) / kBM : 0;
-  int o = block_excl_scan(valid ? total : 0, warp_sums, &tot_rows);
-  int to = block_excl_scan(tiles, warp_sums, &tot_tiles);
+  const int tiles = valid ? (total + kBM - 1) / kBM : 0;
+  const int o = block_excl_scan(valid ? total : 0, warp_sums, &tot_rows);
+  const int to = block_excl_scan(tiles, warp_sums, &tot_tiles);
   if (valid) {
     cnt[e] = total;
     off[e] = o;
     tile_off[e] = to;
-    for (int b = 0; b < nblk; ++b) blk_cnt[(size_t)b * E + e] += o;
+    // pass 2: blk_cnt[b][e] <- offset of block b's first slot of expert e
+    int run = o, b = 0;
+    for (; b + 16 <= nblk; b += 16) {
+      int c[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) c[i] = blk_cnt[(size_t)(b + i) * E + e];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        blk_cnt[(size_t)(b + i) * E + e] = run;
+        run += c[i];
+      }
+    }
+    for (; b < nblk; ++b) {
+      const int c = blk_cnt[(size_t)b * E + e];
+      blk_cnt[(size_t)b * E + e] = run;
+      run += c;
+    }
     for (int i = 0; i < tiles; ++i) {
       int rows = total - kBM * i;
       int32_t* m = bmap + 3 * (size_t)(to + i);
@@ -366,8 +352,9 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
 // ---------------------------------------------------------------------------
 // Gather: xs[pos] = x[perm[pos] / k] for routed positions, and
 // xs[T*k + t] = x[t] for the shared expert's rows, converted from bf16 to the
-// GEMMs' fp16 operand type (exact inside fp16's range, saturating outside).
-// One warp per row.
+// GEMMs' fp16 operand type (exact inside fp16's range, saturating outside),
+// each block of 8 stored in perm8 order (the K order of the dequantised
+// weights). One warp per row.
 // ---------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                    int T, int k, int H, int with_shared,
@@ -383,8 +370,8 @@ __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t
     uint4* d = reinterpret_cast<uint4*>(xs + (size_t)r * H);
     for (int i = lane; i < vec; i += 32) {
       const uint4 v = __ldg(s + i);
-      d[i] = make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y),
-                        bf16x2_to_f16x2_sat(v.z), bf16x2_to_f16x2_sat(v.w));
+      d[i] = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y),
+                                       bf16x2_to_f16x2_sat(v.z), bf16x2_to_f16x2_sat(v.w)));
     }
   }
 }

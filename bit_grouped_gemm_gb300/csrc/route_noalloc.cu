@@ -61,11 +61,11 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
   if (T > kMaxTokens || num_experts > kMaxExperts || top_k > 32) return MOE_ERR_CAPACITY;
   if (!al(x, 16) || !al(router_w, 16) || (router_bias && !al(router_bias, 4)))
     return MOE_ERR_INVALID_ARG;
-  const void* need[] = {out->topk_idx, out->topk_w, out->counts, out->offsets,
-                        out->tile_offsets, out->perm, out->inv, out->block_map, out->num_tiles};
+  const void* need[] = {out->topk_idx, out->topk_w, out->counts,    out->offsets,
+                        out->tile_offsets, out->perm, out->inv, out->block_map,
+                        out->num_tiles, out->logits};
   for (const void* q : need)
-    if (!q || !al(q, 4)) return MOE_ERR_INVALID_ARG;
-  if (out->logits && !al(out->logits, 4)) return MOE_ERR_INVALID_ARG;
+    if (!q || !al(q, 8)) return MOE_ERR_INVALID_ARG;
 
   int32_t* blk = nullptr;
   moe_status s = scratch_address(&blk);

@@ -182,7 +182,8 @@ moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, 
  * same kernels.
  * The caller passes x, router_w, router_bias (may be NULL) as for moe_route
  * and every output buffer in `out` (layouts as in moe_routing; block_map
- * must hold ceil(T*k/128) + E triples; logits may be NULL). The library's
+ * must hold ceil(T*k/128) + E triples; logits is required, every buffer
+ * 8-byte aligned). The library's
  * only scratch for this call is a fixed device array of 128 x 512 int32
  * (256 KB) in the library image, present on every GPU that loads the
  * library until the process exits; hence T <= 4096 and num_experts <= 512,
@@ -221,7 +222,8 @@ moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
 /* Introspection of plan scratch for tests and profiling: device address of
  * the gathered activations (which = 0: fp16 [rows][H], routed positions
  * first, then the shared expert's T rows), the SwiGLU activations (1: fp16
- * [rows][I]), the weighted routed expert outputs (2: bf16 [T*k][H]) or the
+ * [rows][I]) -- both with each block of 8 columns stored in the order
+ * (0,4,1,5,2,6,3,7) --, the weighted routed expert outputs (2: bf16 [T*k][H]) or the
  * shared expert's outputs (3: f32 [T][H]) of the last layer. NULL for an
  * unknown `which` or a plan without a shared expert (3). */
 void* moe_debug_buffer(moe_plan_t plan, int which);
