@@ -38,8 +38,8 @@ namespace moe {
 namespace tc {
 
 constexpr int kThreads = 512;
-constexpr int kBStages = 4;               // activation chunks (64 K) in flight
-constexpr int kQStages = 4;               // packed-weight chunks (256 K) in flight
+constexpr int kBStages = 6;               // activation chunks (64 K) in flight
+constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
 constexpr int kAStages = 4;               // TMEM weight stages (64 K)
 constexpr int kBTileBytes = 128 * 128;    // 128 token rows x 64 fp16
 constexpr int kQTileBytes = 128 * 128;    // 128 weight rows x 32 words
@@ -47,7 +47,8 @@ constexpr int kQStageBytes = 2 * kQTileBytes;
 constexpr int kOffB = 0;
 constexpr int kOffQ = kOffB + kBStages * kBTileBytes;
 constexpr int kOffW = kOffQ + kQStages * kQStageBytes;   // epilogue row weights [4][128]
-constexpr int kOffBar = kOffW + 4 * 128 * 4;
+constexpr int kOffX = kOffW + 4 * 128 * 4;               // epilogue transpose [4][32 x 32 x 4 B]
+constexpr int kOffBar = kOffX + 4 * 4096;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 0, kAccCol1 = 128, kAStageCol = 256;
@@ -177,7 +178,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    tma_prefetch_desc(&p.maps.b);
+    for (int i = 0; i < 4; ++i) tma_prefetch_desc(&p.maps.b[i]);
     tma_prefetch_desc(&p.maps.q0);
     tma_prefetch_desc(&p.maps.q1);
     if (p.has_shared) {
@@ -210,12 +211,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       bool ok = true;
       for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
         const Unit U = decode_unit(p, u, n_routed);
+        // smallest box covering the tile's rows: fewer bytes for small groups
+        const int bi = U.rows > 64 ? 0 : U.rows > 32 ? 1 : U.rows > 16 ? 2 : 3;
+        const uint32_t bytes = (uint32_t)kBTileBytes >> bi;
         for (int c = 0; c < nchunk && ok; ++c) {
           const int s = bcnt % kBStages;
           if (!(ok = thread_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2, 32 * p.mode)))
             break;
-          mbar_arrive_expect_tx(&b_full[s], kBTileBytes);
-          tma_load_2d(smem_b + s * kBTileBytes, &p.maps.b, 64 * c, U.m0, &b_full[s]);
+          mbar_arrive_expect_tx(&b_full[s], bytes);
+          tma_load_2d(smem_b + s * kBTileBytes, &p.maps.b[bi], 64 * c, U.m0, &b_full[s]);
           ++bcnt;
         }
       }
@@ -383,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     const int r = 32 * quarter + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * quarter;   // this warp's copy
+    uint32_t* s_x = reinterpret_cast<uint32_t*>(smem + kOffX + 4096 * quarter);  // transpose
     uint32_t it = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
@@ -410,36 +415,67 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           if (lane == 0) mbar_arrive(acc_empty);
         }
         const int nval = min(32, U.rows - c0);
+        // This warp holds a 32 (weight rows = output columns) x 32 (tokens)
+        // block; it is transposed through shared memory so every lane writes
+        // 16-byte pieces of token rows.
         if (p.mode == 0) {
-          // act columns are stored in perm8 order (the down pass's K order)
-          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + perm8_pos(r);
+          // act = silu(gate) * up in fp16; columns in perm8 order
+          uint16_t* t16 = reinterpret_cast<uint16_t*>(s_x);
+          const int col = perm8_pos(lane);
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            if (cc < nval) {
-              const float g = __uint_as_float(v0[cc]);
-              const float uu = __uint_as_float(v1[cc]);
-              o[(size_t)cc * p.out_ld] = f32_to_f16_sat(silu_fast(g) * uu);
-            }
+          for (int cc = 0; cc < 32; ++cc)
+            t16[cc * 32 + col] = f32_to_f16_sat(silu_fast(__uint_as_float(v0[cc])) *
+                                                __uint_as_float(v1[cc]));
+          __syncwarp();
+          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + 32 * quarter;
+#pragma unroll
+          for (int it4 = 0; it4 < 4; ++it4) {
+            const int cc = it4 * 8 + (lane >> 2), seg = lane & 3;
+            if (cc < nval)
+              *reinterpret_cast<uint4*>(o + (size_t)cc * p.out_ld + 8 * seg) =
+                  *reinterpret_cast<const uint4*>(t16 + cc * 32 + 8 * seg);
           }
+          __syncwarp();
         } else if (U.shared) {
           // shared expert (weight 1): kept in fp32, it is as large as the output
-          float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j + r;
+          float* tf = reinterpret_cast<float*>(s_x);
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            if (cc < nval) {
-              o[(size_t)cc * p.out_ld] = __uint_as_float(v0[cc]);
-              o[(size_t)cc * p.out_ld + 128] = __uint_as_float(v1[cc]);
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              tf[cc * 32 + lane] = __uint_as_float(half ? v1[cc] : v0[cc]);
+            __syncwarp();
+            float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j +
+                       128 * half + 32 * quarter;
+#pragma unroll
+            for (int it8 = 0; it8 < 8; ++it8) {
+              const int cc = it8 * 4 + (lane >> 3), seg = lane & 7;
+              if (cc < nval)
+                *reinterpret_cast<float4*>(o + (size_t)cc * p.out_ld + 4 * seg) =
+                    *reinterpret_cast<const float4*>(tf + cc * 32 + 4 * seg);
             }
+            __syncwarp();
           }
         } else {
-          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + r;
+          // routed expert: weighted by its top-k weight, bf16
+          uint16_t* t16 = reinterpret_cast<uint16_t*>(s_x);
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            if (cc < nval) {
-              const float wt = s_w[c0 + cc];
-              o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * wt);
-              o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * wt);
+          for (int half = 0; half < 2; ++half) {
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              t16[cc * 32 + lane] =
+                  f32_to_bf16(__uint_as_float(half ? v1[cc] : v0[cc]) * s_w[(c0 + cc) & 127]);
+            __syncwarp();
+            uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + 128 * half +
+                          32 * quarter;
+#pragma unroll
+            for (int it4 = 0; it4 < 4; ++it4) {
+              const int cc = it4 * 8 + (lane >> 2), seg = lane & 3;
+              if (cc < nval)
+                *reinterpret_cast<uint4*>(o + (size_t)cc * p.out_ld + 8 * seg) =
+                    *reinterpret_cast<const uint4*>(t16 + cc * 32 + 8 * seg);
             }
+            __syncwarp();
           }
         }
       }

@@ -67,7 +67,8 @@ struct GemmProblem {
 // tcgen05 tensor-core path. `maps` holds the encoded tensor maps the kernel
 // needs (B operand, routed q for w0/w1, shared q for sw0/sw1).
 struct TcMaps {
-  CUtensorMap b;            // act_in, bf16 [rows][K], box 64 x 128, swizzle 128B
+  CUtensorMap b[4];         // act_in, fp16 [rows][K], boxes 64 x {128,64,32,16} rows,
+                            // swizzle 128B (the smallest box covering a tile is used)
   CUtensorMap q0, q1;       // routed q of w0/w1, uint32 [E*N][K/8], box 32 x 128
   CUtensorMap sq0, sq1;     // shared q
 };

@@ -126,7 +126,7 @@ struct moe_plan {
   int num_sms = 0;
   Layout L;
   uint8_t* scratch = nullptr;
-  CUtensorMap tm_xs, tm_act;
+  CUtensorMap tm_xs[4], tm_act[4];   // box rows 128, 64, 32, 16
   bool timing = false;
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> ev_pool;
@@ -288,8 +288,10 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
 
   if (path == 1) {
     TcMaps m0{}, m1{};
-    m0.b = p->tm_xs;
-    m1.b = p->tm_act;
+    for (int i = 0; i < 4; ++i) {
+      m0.b[i] = p->tm_xs[i];
+      m1.b[i] = p->tm_act[i];
+    }
     const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
     bool ok = encode_2d(&m0.q0, U32, 4, routed->gate.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
               encode_2d(&m0.q1, U32, 4, routed->up.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
@@ -399,10 +401,14 @@ moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* ou
     return MOE_ERR_CUDA;
   }
   cudaMemset(p->scratch + p->L.err, 0, 16);
-  bool ok = encode_2d(&p->tm_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->at<uint16_t>(p->L.xs),
-                      p->L.rows_cap, desc->hidden, 64, 128) &&
-            encode_2d(&p->tm_act, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-                      p->at<uint16_t>(p->L.act), p->L.rows_cap, desc->inter, 64, 128);
+  bool ok = true;
+  for (int i = 0; i < 4 && ok; ++i) {
+    const uint32_t box_rows = 128u >> i;
+    ok = encode_2d(&p->tm_xs[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, p->at<uint16_t>(p->L.xs),
+                   p->L.rows_cap, desc->hidden, 64, box_rows) &&
+         encode_2d(&p->tm_act[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                   p->at<uint16_t>(p->L.act), p->L.rows_cap, desc->inter, 64, box_rows);
+  }
   if (!ok || cudaDeviceSynchronize() != cudaSuccess) {
     cudaFree(p->scratch);
     delete p;

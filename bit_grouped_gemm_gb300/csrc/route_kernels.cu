@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 }
 
 // ---------------------------------------------------------------------------
-// Top-k + per-block histogram. One CTA = 32 tokens, 8 warps of 4 tokens;
+// Top-k + per-block histogram. One CTA = 32 tokens, one warp per token;
 // k rounds of a warp arg-max per token (higher logit first, lower index on
 // ties; a NaN logit ranks as -inf, and every round picks some not-yet-selected
 // expert, so indices are always valid). Weights: softmax over the selected
@@ -136,17 +136,16 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 // writes its per-expert counts to blk_cnt[block][E].
 // ---------------------------------------------------------------------------
 template <int VPL>   // values per lane, E <= 32 * VPL
-__global__ void __launch_bounds__(256) router_topk_kernel(
+__global__ void __launch_bounds__(1024) router_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt) {
   __shared__ int cnt_s[1024];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kRouterTB;
-  for (int i = tid; i < E; i += 256) cnt_s[i] = 0;
+  for (int i = tid; i < E; i += blockDim.x) cnt_s[i] = 0;
   __syncthreads();
-  for (int tl = warp; tl < kRouterTB; tl += 8) {
-    const int t = t0 + tl;
-    if (t >= T) break;
+  if (t0 + warp < T) {
+    const int t = t0 + warp;
     float v[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
@@ -193,7 +192,7 @@ __global__ void __launch_bounds__(256) router_topk_kernel(
     }
   }
   __syncthreads();
-  for (int e = tid; e < E; e += 256) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
+  for (int e = tid; e < E; e += blockDim.x) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
 }
 
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
@@ -209,9 +208,11 @@ cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* 
   router_logits_kernel<<<grid, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   if (E <= 256)
-    router_topk_kernel<8><<<nblk, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, blk_cnt);
+    router_topk_kernel<8><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
+                                                           blk_cnt);
   else
-    router_topk_kernel<16><<<nblk, 256, 0, st>>>(logits, T, E, k, topk_idx, topk_w, blk_cnt);
+    router_topk_kernel<16><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
+                                                            blk_cnt);
   return cudaGetLastError();
 }
 
