@@ -126,19 +126,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
-__device__ __forceinline__ bool thread_wait(uint64_t* bar, uint32_t parity,
-                                            volatile int* abort_flag, const DevErr& err,
-                                            int site, int tc_stat_base = 0) {
-  TC_STAT_BEGIN();
-  bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
-  TC_STAT_END(site);
-  if (!ok) {
-    if (!*abort_flag) report_timeout(err, site);
-    *abort_flag = 1;
-  }
-  return ok;
-}
-
 __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_constant__ Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -206,76 +193,80 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
 
   if (warp == 0) {
     // ------------------------------------------ TMA producer: activations
-    if (lane == 0) {
-      uint32_t bcnt = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit U = decode_unit(p, u, n_routed);
-        // smallest box covering the tile's rows: fewer bytes for small groups
-        const int bi = U.rows > 64 ? 0 : U.rows > 32 ? 1 : U.rows > 16 ? 2 : 3;
-        const uint32_t bytes = (uint32_t)kBTileBytes >> bi;
-        for (int c = 0; c < nchunk && ok; ++c) {
-          const int s = bcnt % kBStages;
-          if (!(ok = thread_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2, 32 * p.mode)))
-            break;
+    uint32_t bcnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit U = decode_unit(p, u, n_routed);
+      // smallest box covering the tile's rows: fewer bytes for small groups
+      const int bi = U.rows > 64 ? 0 : U.rows > 32 ? 1 : U.rows > 16 ? 2 : 3;
+      const uint32_t bytes = (uint32_t)kBTileBytes >> bi;
+      for (int c = 0; c < nchunk && ok; ++c) {
+        const int s = bcnt % kBStages;
+        if (!(ok = warp_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2, 32 * p.mode)))
+          break;
+        if (elect_one_sync()) {
           mbar_arrive_expect_tx(&b_full[s], bytes);
           tma_load_2d(smem_b + s * kBTileBytes, &p.maps.b[bi], 64 * c, U.m0, &b_full[s]);
-          ++bcnt;
         }
+        __syncwarp();
+        ++bcnt;
       }
-      if (!ok) {
-        // let this CTA's own copies land before shared memory is released
-        for (int s = 0; s < kBStages; ++s) {
-          const uint32_t uses = (bcnt + kBStages - 1 - s) / kBStages;
-          if (uses) mbar_wait_drain(&b_full[s], (uses - 1) & 1, p.err.limit_ns);
-        }
+    }
+    if (!ok) {
+      // let this CTA's own copies land before shared memory is released
+      for (int s = 0; s < kBStages; ++s) {
+        const uint32_t uses = (bcnt + kBStages - 1 - s) / kBStages;
+        if (uses) mbar_wait_drain(&b_full[s], (uses - 1) & 1, p.err.limit_ns);
       }
     }
   } else if (warp == 2) {
     // ------------------------------------- TMA producer: packed weights
-    // (its own thread, so weight tiles run ahead of the activation ring)
-    if (lane == 0) {
-      uint32_t qcnt = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-        const Unit U = decode_unit(p, u, n_routed);
-        const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
-        const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
-        const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
-        const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
-        for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
-          const int s = qcnt % kQStages;
-          if (!(ok = thread_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1, 32 * p.mode)))
-            break;
+    // (its own warp, so weight tiles run ahead of the activation ring)
+    uint32_t qcnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      const Unit U = decode_unit(p, u, n_routed);
+      const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
+      const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
+      const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
+      const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
+      for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
+        const int s = qcnt % kQStages;
+        if (!(ok = warp_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1, 32 * p.mode)))
+          break;
+        if (elect_one_sync()) {
           mbar_arrive_expect_tx(&q_full[s], kQStageBytes);
           tma_load_2d(smem_q + s * kQStageBytes, m0, 32 * qc, y0, &q_full[s]);
           tma_load_2d(smem_q + s * kQStageBytes + kQTileBytes, m1, 32 * qc, y1, &q_full[s]);
-          ++qcnt;
         }
+        __syncwarp();
+        ++qcnt;
       }
-      if (!ok) {
-        for (int s = 0; s < kQStages; ++s) {
-          const uint32_t uses = (qcnt + kQStages - 1 - s) / kQStages;
-          if (uses) mbar_wait_drain(&q_full[s], (uses - 1) & 1, p.err.limit_ns);
-        }
+    }
+    if (!ok) {
+      for (int s = 0; s < kQStages; ++s) {
+        const uint32_t uses = (qcnt + kQStages - 1 - s) / kQStages;
+        if (uses) mbar_wait_drain(&q_full[s], (uses - 1) & 1, p.err.limit_ns);
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      uint32_t bcnt = 0, acnt = 0, it = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-        const Unit U = decode_unit(p, u, n_routed);
-        const int ntok = (U.rows + 15) & ~15;
-        const uint32_t idesc = idesc_f16_f32(128, ntok);
-        if (!(ok = thread_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
+    // The whole warp runs the loop and takes the waits; one elected lane
+    // issues the MMAs and the commits that track them.
+    uint32_t bcnt = 0, acnt = 0, it = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
+      const Unit U = decode_unit(p, u, n_routed);
+      const int ntok = (U.rows + 15) & ~15;
+      const uint32_t idesc = idesc_f16_f32(128, ntok);
+      if (!(ok = warp_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
+      tc_fence_after();
+      for (int c = 0; c < nchunk; ++c) {
+        const int bs = bcnt % kBStages, as = acnt % kAStages;
+        if (!(ok = warp_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4, 32 * p.mode))) break;
+        if (!(ok = warp_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5, 32 * p.mode))) break;
         tc_fence_after();
-        for (int c = 0; c < nchunk; ++c) {
-          const int bs = bcnt % kBStages, as = acnt % kAStages;
-          if (!(ok = thread_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4, 32 * p.mode))) break;
-          if (!(ok = thread_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5, 32 * p.mode))) break;
-          tc_fence_after();
+        if (elect_one_sync()) {
           const uint32_t bbase = smem_u32(smem_b + bs * kBTileBytes);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk) {
@@ -287,16 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           }
           mma_commit(&b_empty[bs]);
           mma_commit(&a_empty[as]);
-          ++bcnt;
-          ++acnt;
         }
-        if (!ok) break;
-        mma_commit(acc_full);
+        __syncwarp();
+        ++bcnt;
+        ++acnt;
       }
-      // all MMAs of this thread complete before TMEM is released
-      mma_commit(drain);
-      mbar_wait_drain(drain, 0, p.err.limit_ns);
+      if (!ok) break;
+      if (elect_one_sync()) mma_commit(acc_full);
+      __syncwarp();
     }
+    // all MMAs of this warp complete before TMEM is released
+    if (elect_one_sync()) mma_commit(drain);
+    __syncwarp();
+    mbar_wait_drain(drain, 0, p.err.limit_ns);
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------ dequant warps
     const int blk = (warp - 4) >> 2;

@@ -94,6 +94,19 @@ __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
   }
 }
 
+// Elects one lane of the converged warp (the lowest active one): the lane that
+// issues a role's single-thread operations while the whole warp runs the loop.
+// Waits are taken by all 32 lanes; a wait by one lane whose siblings sit
+// elsewhere costs hundreds of cycles per call on sm_103a.
+__device__ __forceinline__ bool elect_one_sync() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 // ------------------------------------------------------------------- TMA ---
 __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
