@@ -75,15 +75,32 @@ struct Unit {
   bool shared;
 };
 
-__device__ __forceinline__ Unit decode_unit(const Params& p, int u, int n_routed) {
+// The block-map entry of unit u (zeros for a shared-expert unit), fetched a
+// unit ahead so that its global-load latency hides behind the current unit.
+struct UnitRaw {
+  int e, m0, rows;
+};
+
+__device__ __forceinline__ UnitRaw fetch_unit(const Params& p, int u, int n_routed) {
+  UnitRaw r = {0, 0, 0};
+  const int tile = u / p.nblk;
+  if (tile < n_routed) {
+    const int32_t* m = p.bmap + 3 * (size_t)tile;
+    r.e = __ldg(m);
+    r.m0 = __ldg(m + 1);
+    r.rows = __ldg(m + 2);
+  }
+  return r;
+}
+
+__device__ __forceinline__ Unit make_unit(const Params& p, int u, int n_routed, const UnitRaw& raw) {
   Unit r;
   const int tile = u / p.nblk;
   r.j = u - tile * p.nblk;
   if (tile < n_routed) {
-    const int32_t* m = p.bmap + 3 * (size_t)tile;
-    r.e = m[0];
-    r.m0 = m[1];
-    r.rows = m[2];
+    r.e = raw.e;
+    r.m0 = raw.m0;
+    r.rows = raw.rows;
     r.shared = false;
   } else {
     const int i = tile - n_routed;
@@ -102,17 +119,19 @@ __device__ __forceinline__ int block_row0(const Params& p, int j, int blk) {
 
 #ifdef MOE_TC_STATS
 // Profiling build only: cycles each role spends in each wait site, and in
-// total, summed over CTAs (read with moe_debug_tc_stats).
+// total, summed over CTAs (read with moe_debug_tc_stats). Each CTA sums in
+// shared memory and adds its totals to the global counters once, at exit.
 __device__ unsigned long long g_tc_stats[64];   // [mode*32 + site], roles at +16
+__shared__ unsigned long long s_tc_stats[32];
 #define TC_STAT_BEGIN() const long long tc_t0 = clock64()
-#define TC_STAT_END(site) atomicAdd(&g_tc_stats[tc_stat_base + (site)], (unsigned long long)(clock64() - tc_t0))
+#define TC_STAT_END(site) atomicAdd(&s_tc_stats[(site)], (unsigned long long)(clock64() - tc_t0))
 #else
 #define TC_STAT_BEGIN()
 #define TC_STAT_END(site)
 #endif
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          const DevErr& err, int site, int tc_stat_base = 0) {
+                                          const DevErr& err, int site, int = 0) {
   TC_STAT_BEGIN();
   bool ok = mbar_wait(bar, parity, abort_flag, err.limit_ns);
   ok = __all_sync(0xffffffffu, ok);
@@ -138,8 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   uint64_t* q_full = b_empty + kBStages;
   uint64_t* q_empty = q_full + kQStages;
   uint64_t* a_full = q_empty + kQStages;
-  uint64_t* a_empty = a_full + kAStages;
-  uint64_t* acc_full = a_empty + kAStages;
+  uint64_t* acc_full = a_full + kAStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -157,8 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       mbar_init(&q_empty[i], 8);
     }
     for (int i = 0; i < kAStages; ++i) {
-      mbar_init(&a_full[i], 8);
-      mbar_init(&a_empty[i], 1);
+      mbar_init(&a_full[i], 9);   // 8 dequant warps + the activation forwarder
     }
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 4);
@@ -178,6 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     tmem_relinquish();
     tc_fence_before();
   }
+#ifdef MOE_TC_STATS
+  if (threadIdx.x < 32) s_tc_stats[threadIdx.x] = 0;
+#endif
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -195,8 +215,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // ------------------------------------------ TMA producer: activations
     uint32_t bcnt = 0;
     bool ok = true;
+    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit U = decode_unit(p, u, n_routed);
+      const Unit U = make_unit(p, u, n_routed, nxt);
+      nxt = fetch_unit(p, u + gridDim.x, n_routed);
       // smallest box covering the tile's rows: fewer bytes for small groups
       const int bi = U.rows > 64 ? 0 : U.rows > 32 ? 1 : U.rows > 16 ? 2 : 3;
       const uint32_t bytes = (uint32_t)kBTileBytes >> bi;
@@ -224,8 +246,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // (its own warp, so weight tiles run ahead of the activation ring)
     uint32_t qcnt = 0;
     bool ok = true;
+    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit U = decode_unit(p, u, n_routed);
+      const Unit U = make_unit(p, u, n_routed, nxt);
+      nxt = fetch_unit(p, u + gridDim.x, n_routed);
       const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
       const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
       const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
@@ -255,15 +279,17 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // issues the MMAs and the commits that track them.
     uint32_t bcnt = 0, acnt = 0, it = 0;
     bool ok = true;
+    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-      const Unit U = decode_unit(p, u, n_routed);
+      const Unit U = make_unit(p, u, n_routed, nxt);
+      nxt = fetch_unit(p, u + gridDim.x, n_routed);
       const int ntok = (U.rows + 15) & ~15;
       const uint32_t idesc = idesc_f16_f32(128, ntok);
       if (!(ok = warp_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
       tc_fence_after();
       for (int c = 0; c < nchunk; ++c) {
         const int bs = bcnt % kBStages, as = acnt % kAStages;
-        if (!(ok = warp_wait(&b_full[bs], (bcnt / kBStages) & 1, abort_flag, p.err, 4, 32 * p.mode))) break;
+        // a_full also covers the activation chunk (the forwarder saw it land)
         if (!(ok = warp_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5, 32 * p.mode))) break;
         tc_fence_after();
         if (elect_one_sync()) {
@@ -276,8 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
             mma_f16_ts(tmem + kAccCol0, a0, bd, idesc, acc);
             mma_f16_ts(tmem + kAccCol1, a0 + 32, bd, idesc, acc);
           }
+          // one commit frees both the activation slot and the TMEM weight stage
           mma_commit(&b_empty[bs]);
-          mma_commit(&a_empty[as]);
         }
         __syncwarp();
         ++bcnt;
@@ -291,6 +317,30 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     if (elect_one_sync()) mma_commit(drain);
     __syncwarp();
     mbar_wait_drain(drain, 0, p.err.limit_ns);
+  } else if (warp == 3) {
+    // --------------------------------------------- activation forwarder
+    // Waits for each activation chunk to land and adds the last arrival to
+    // the chunk's TMEM weight stage, so the MMA warp takes one wait per
+    // chunk and the dequant warps none for activations. It arrives for
+    // chunk c only after the stage's phase for chunk c - kAStages is over,
+    // so an early arrival can never count toward the previous phase.
+    uint32_t cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      for (int c = 0; c < nchunk; ++c, ++cnt) {
+        if (!(ok = warp_wait(&b_full[cnt % kBStages], (cnt / kBStages) & 1, abort_flag, p.err, 4,
+                             32 * p.mode)))
+          break;
+        if (cnt >= (uint32_t)kAStages) {
+          const uint32_t prev = cnt - kAStages;
+          if (!(ok = warp_wait(&a_full[prev % kAStages], (prev / kAStages) & 1, abort_flag, p.err, 10,
+                               32 * p.mode)))
+            break;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&a_full[cnt % kAStages]);
+      }
+    }
   } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------ dequant warps
     const int blk = (warp - 4) >> 2;
@@ -300,8 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     uint32_t qcnt = 0, acnt = 0;
     bool ok = true;
     // scale/bias rows of this thread's weight row in unit u
-    auto sb_rows = [&](int u, const uint16_t*& sr, const uint16_t*& br) {
-      const Unit U = decode_unit(p, u, n_routed);
+    auto sb_rows = [&](const Unit& U, const uint16_t*& sr, const uint16_t*& br) {
       const W4Dev& w = U.shared ? (blk == 0 ? p.sw0 : p.sw1) : (blk == 0 ? p.w0 : p.w1);
       const size_t row = (U.shared ? 0 : (size_t)U.e * p.N) + block_row0(p, U.j, blk) + r;
       sr = w.s + row * kgroups;
@@ -309,13 +358,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     };
     const uint16_t *srow = nullptr, *brow = nullptr;
     uint2 s4 = make_uint2(0u, 0u), b4 = make_uint2(0u, 0u);
+    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
     if ((int)blockIdx.x < units) {
-      sb_rows(blockIdx.x, srow, brow);
+      sb_rows(make_unit(p, blockIdx.x, n_routed, nxt), srow, brow);
       s4 = __ldg(reinterpret_cast<const uint2*>(srow));
       b4 = __ldg(reinterpret_cast<const uint2*>(brow));
     }
     const int nq = nchunk / 4;
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
+      nxt = fetch_unit(p, u + gridDim.x, n_routed);
       const uint16_t *nsrow = nullptr, *nbrow = nullptr;
       for (int qc = 0; qc < nq && ok; ++qc) {
         // scales/biases of the next 4 groups, one step ahead (also across units)
@@ -324,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           s4n = __ldg(reinterpret_cast<const uint2*>(srow + 4 * (qc + 1)));
           b4n = __ldg(reinterpret_cast<const uint2*>(brow + 4 * (qc + 1)));
         } else if (u + (int)gridDim.x < units) {
-          sb_rows(u + gridDim.x, nsrow, nbrow);
+          sb_rows(make_unit(p, u + gridDim.x, n_routed, nxt), nsrow, nbrow);
           s4n = __ldg(reinterpret_cast<const uint2*>(nsrow));
           b4n = __ldg(reinterpret_cast<const uint2*>(nbrow));
         }
@@ -333,11 +384,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         const uint8_t* qrow = smem_q + qs * kQStageBytes + blk * kQTileBytes + r * 128;
         const uint32_t sw = r & 7;
 #pragma unroll
-        for (int sub = 0; sub < 4; ++sub) {
-          const int as = acnt % kAStages;
-          if (!(ok = warp_wait(&a_empty[as], ((acnt / kAStages) & 1) ^ 1, abort_flag, p.err, 7, 32 * p.mode)))
-            break;
-          tc_fence_after();
+        // this thread's 64 weights of chunk `sub` of the stage, as fp16
+        auto dequant_chunk = [&](int sub, uint32_t (&out)[32]) {
           const uint4 wa = *reinterpret_cast<const uint4*>(qrow + (((2 * sub) ^ sw) << 4));
           const uint4 wb = *reinterpret_cast<const uint4*>(qrow + (((2 * sub + 1) ^ sw) << 4));
           const uint32_t sbits = (sub & 1) ? (((sub >> 1) ? s4.y : s4.x) >> 16)
@@ -347,7 +395,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           // bf16 scale and bias as fp16 (exact inside fp16's normal range)
           const __half2 s2 = __half2half2(__float2half_rn(bf16_to_f32((uint16_t)sbits)));
           const __half2 b2 = __half2half2(__float2half_rn(bf16_to_f32((uint16_t)bbits)));
-          uint32_t out[32];
           const uint32_t words[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
 #pragma unroll
           for (int i = 0; i < 8; ++i) {
@@ -358,12 +405,42 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
             out[4 * i + 2] = o4[2];
             out[4 * i + 3] = o4[3];
           }
-          tmem_st_32x32b_x32(tmem + lane_base + kAStageCol + 64 * as + 32 * blk, out);
+        };
+        // Chunks go in pairs: one wait for two free TMEM stages, one wait for
+        // the stores, and the second chunk's arithmetic overlaps the first
+        // chunk's store.
+#pragma unroll 1
+        for (int pair = 0; pair < 2; ++pair) {
+          uint32_t out[32];
+          dequant_chunk(2 * pair, out);
+          // Stage (acnt + 1) % kAStages is free once the MMAs of chunk
+          // acnt + 1 - kAStages are done (their commit is the one on that
+          // chunk's activation slot); MMAs complete in order, so that also
+          // frees the stage of chunk acnt.
+          if (acnt + 1 >= (uint32_t)kAStages) {
+            const uint32_t prev = acnt + 1 - kAStages;
+            if (!(ok = warp_wait(&b_empty[prev % kBStages], (prev / kBStages) & 1, abort_flag, p.err, 7,
+                                 32 * p.mode)))
+              break;
+          }
+          tc_fence_after();
+          tmem_st_32x32b_x32(tmem + lane_base + kAStageCol + 64 * (acnt % kAStages) + 32 * blk, out);
+          dequant_chunk(2 * pair + 1, out);
+          tmem_st_32x32b_x32(tmem + lane_base + kAStageCol + 64 * ((acnt + 1) % kAStages) + 32 * blk, out);
+#ifdef MOE_TC_STATS
+          const long long st_t0 = clock64();
+#endif
           tmem_wait_st();
+#ifdef MOE_TC_STATS
+          if (lane == 0) atomicAdd(&s_tc_stats[9], (unsigned long long)(clock64() - st_t0));
+#endif
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(&a_full[as]);
-          ++acnt;
+          if (lane == 0) {
+            mbar_arrive(&a_full[acnt % kAStages]);
+            mbar_arrive(&a_full[(acnt + 1) % kAStages]);
+          }
+          acnt += 2;
         }
         if (!ok) break;
         __syncwarp();
@@ -384,8 +461,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     uint32_t* s_x = reinterpret_cast<uint32_t*>(smem + kOffX + 4096 * quarter);  // transpose
     uint32_t it = 0;
     bool ok = true;
+    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
     for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-      const Unit U = decode_unit(p, u, n_routed);
+      const Unit U = make_unit(p, u, n_routed, nxt);
+      nxt = fetch_unit(p, u + gridDim.x, n_routed);
       if (p.mode == 1 && !U.shared) {
         // top-k weights of the tile's rows, fetched while the MMAs still run
 #pragma unroll
@@ -406,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           // accumulators fully read: let the next unit's MMAs start now
           tc_fence_before();
           __syncwarp();
-          if (lane == 0) mbar_arrive(acc_empty);
+          if (lane == 0) mbar_arrive_relaxed(acc_empty);
         }
         const int nval = min(32, U.rows - c0);
         // This warp holds a 32 (weight rows = output columns) x 32 (tokens)
@@ -481,10 +560,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   if (lane == 0) {
     const int role = warp == 0 ? 0 : warp == 1 ? 1 : warp == 2 ? 2 : warp < 4 ? 3
                    : warp < 12 ? 4 : 5;
-    atomicAdd(&g_tc_stats[32 * p.mode + 16 + role], (unsigned long long)(clock64() - role_t0));
+    atomicAdd(&s_tc_stats[16 + role], (unsigned long long)(clock64() - role_t0));
   }
 #endif
   __syncthreads();
+#ifdef MOE_TC_STATS
+  if (threadIdx.x < 32) atomicAdd(&g_tc_stats[32 * p.mode + threadIdx.x], s_tc_stats[threadIdx.x]);
+#endif
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
@@ -530,7 +612,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, D
 #ifdef MOE_TC_STATS
 extern "C" int moe_debug_tc_stats(unsigned long long* out) {
   cudaError_t e = cudaMemcpyFromSymbol(out, tc::g_tc_stats, sizeof(tc::g_tc_stats));
-  unsigned long long z[32] = {};
+  unsigned long long z[64] = {};
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(tc::g_tc_stats, z, sizeof(z));
   return (int)e;
 }

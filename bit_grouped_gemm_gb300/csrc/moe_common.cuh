@@ -46,6 +46,14 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
                : "memory");
 }
 
+// Arrival without release ordering: for a consumer whose reads have already
+// completed (e.g. tcgen05.ld after tcgen05.wait::ld), so that the arrival does
+// not wait for the thread's earlier global stores to drain.
+__device__ __forceinline__ void mbar_arrive_relaxed(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.relaxed.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar))
+               : "memory");
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                    smem_u32(bar)),
@@ -65,20 +73,34 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps until the phase completes or about `hint_ns` pass, instead of
+// spinning and taking issue slots from the warps that do the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n"
+      " mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+constexpr uint32_t kWaitSleepNs = 100000;
+
 // Bounded wait for the phase with the given parity. Returns false when the
 // limit ran out or another role of the CTA raised `abort_flag`.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           volatile int* abort_flag,
                                           unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = globaltimer_ns();
-  uint32_t it = 0;
+  const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++it & 15u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
 
@@ -87,9 +109,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
 __device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity,
                                                 unsigned long long limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  unsigned long long t0 = globaltimer_ns();
+  const unsigned long long t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
@@ -335,10 +357,11 @@ __device__ __forceinline__ uint32_t bf16x2_to_f16x2_sat(uint32_t v) {
 }
 
 __device__ __forceinline__ float silu_f32(float g) { return g / (1.0f + expf(-g)); }
-// silu with the fast exponential and reciprocal (relative error ~1e-6,
-// far below the fp16 rounding of its result)
+// silu with the fast exponential and division (relative error ~1e-6, far
+// below the fp16 rounding of its result); for g below about -88 the
+// denominator overflows and the result is -0.
 __device__ __forceinline__ float silu_fast(float g) {
-  return g * __frcp_rn(1.0f + __expf(-g));
+  return __fdividef(g, 1.0f + __expf(-g));
 }
 
 }  // namespace moe
