@@ -47,8 +47,8 @@ constexpr int kQStageBytes = 2 * kQTileBytes;
 constexpr int kOffB = 0;
 constexpr int kOffQ = kOffB + kBStages * kBTileBytes;
 constexpr int kOffW = kOffQ + kQStages * kQStageBytes;   // epilogue row weights [4][128]
-constexpr int kOffX = kOffW + 4 * 128 * 4;               // epilogue transpose [4][32 x 32 x 4 B]
-constexpr int kOffBar = kOffX + 4 * 4096;
+constexpr int kOffX = kOffW + 4 * 128 * 4;               // epilogue transpose [4][32 x 32 fp16]
+constexpr int kOffBar = kOffX + 4 * 2048;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 0, kAccCol1 = 128, kAStageCol = 256;
@@ -383,7 +383,6 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         if (!(ok = warp_wait(&q_full[qs], (qcnt / kQStages) & 1, abort_flag, p.err, 6, 32 * p.mode))) break;
         const uint8_t* qrow = smem_q + qs * kQStageBytes + blk * kQTileBytes + r * 128;
         const uint32_t sw = r & 7;
-#pragma unroll
         // this thread's 64 weights of chunk `sub` of the stage, as fp16
         auto dequant_chunk = [&](int sub, uint32_t (&out)[32]) {
           const uint4 wa = *reinterpret_cast<const uint4*>(qrow + (((2 * sub) ^ sw) << 4));
@@ -455,10 +454,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   } else if (warp >= 12) {
     // ------------------------------------------------------ epilogue warps
     const int quarter = warp & 3;
-    const int r = 32 * quarter + lane;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * quarter;   // this warp's copy
-    uint32_t* s_x = reinterpret_cast<uint32_t*>(smem + kOffX + 4096 * quarter);  // transpose
+    uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + kOffX) + 1024 * quarter;  // 32 x 32 fp16
     uint32_t it = 0;
     bool ok = true;
     UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
@@ -488,12 +486,15 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           if (lane == 0) mbar_arrive_relaxed(acc_empty);
         }
         const int nval = min(32, U.rows - c0);
-        // This warp holds a 32 (weight rows = output columns) x 32 (tokens)
-        // block; it is transposed through shared memory so every lane writes
-        // 16-byte pieces of token rows.
+        // Lane l holds output column 32 * quarter + l for 32 consecutive
+        // tokens, so one register stored by the whole warp writes 32 adjacent
+        // columns of one token row: 64 (or 128) contiguous bytes.
         if (p.mode == 0) {
-          // act = silu(gate) * up in fp16; columns in perm8 order
-          uint16_t* t16 = reinterpret_cast<uint16_t*>(s_x);
+          // act = silu(gate) * up in fp16, columns in perm8 order. The 32 x 32
+          // block goes through shared memory so that each lane stores 16-byte
+          // pieces of token rows (measured faster here than one 2-byte store
+          // per element).
+          uint16_t* t16 = s_x;
           const int col = perm8_pos(lane);
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc)
@@ -511,45 +512,23 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           __syncwarp();
         } else if (U.shared) {
           // shared expert (weight 1): kept in fp32, it is as large as the output
-          float* tf = reinterpret_cast<float*>(s_x);
+          float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-              tf[cc * 32 + lane] = __uint_as_float(half ? v1[cc] : v0[cc]);
-            __syncwarp();
-            float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j +
-                       128 * half + 32 * quarter;
-#pragma unroll
-            for (int it8 = 0; it8 < 8; ++it8) {
-              const int cc = it8 * 4 + (lane >> 3), seg = lane & 7;
-              if (cc < nval)
-                *reinterpret_cast<float4*>(o + (size_t)cc * p.out_ld + 4 * seg) =
-                    *reinterpret_cast<const float4*>(tf + cc * 32 + 4 * seg);
+          for (int cc = 0; cc < 32; ++cc)
+            if (cc < nval) {
+              o[(size_t)cc * p.out_ld] = __uint_as_float(v0[cc]);
+              o[(size_t)cc * p.out_ld + 128] = __uint_as_float(v1[cc]);
             }
-            __syncwarp();
-          }
         } else {
           // routed expert: weighted by its top-k weight, bf16
-          uint16_t* t16 = reinterpret_cast<uint16_t*>(s_x);
+          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc)
-              t16[cc * 32 + lane] =
-                  f32_to_bf16(__uint_as_float(half ? v1[cc] : v0[cc]) * s_w[(c0 + cc) & 127]);
-            __syncwarp();
-            uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + 128 * half +
-                          32 * quarter;
-#pragma unroll
-            for (int it4 = 0; it4 < 4; ++it4) {
-              const int cc = it4 * 8 + (lane >> 2), seg = lane & 3;
-              if (cc < nval)
-                *reinterpret_cast<uint4*>(o + (size_t)cc * p.out_ld + 8 * seg) =
-                    *reinterpret_cast<const uint4*>(t16 + cc * 32 + 8 * seg);
+          for (int cc = 0; cc < 32; ++cc)
+            if (cc < nval) {
+              const float w = s_w[(c0 + cc) & 127];
+              o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * w);
+              o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * w);
             }
-            __syncwarp();
-          }
         }
       }
       __syncwarp();
