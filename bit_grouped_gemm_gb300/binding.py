@@ -20,7 +20,7 @@ MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY", 5: "MOE_ERR_DEVICE_TIMEOUT"}
 KERNEL_KINDS = ("router", "scan", "scatter", "gather", "gate_up_gemm", "down_gemm",
-                "combine", "residual")
+                "combine", "residual", "topk")
 
 
 class MoeError(RuntimeError):
@@ -54,7 +54,8 @@ class MoeRouting(ctypes.Structure):
 
 
 class MoeTiming(ctypes.Structure):
-    _fields_ = [("ms", ctypes.c_double * 8), ("launches", ctypes.c_longlong * 8)]
+    _fields_ = [("ms", ctypes.c_double * len(KERNEL_KINDS)),
+                ("launches", ctypes.c_longlong * len(KERNEL_KINDS))]
 
 
 _lib = None

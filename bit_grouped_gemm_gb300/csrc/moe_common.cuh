@@ -334,15 +334,29 @@ __host__ __device__ __forceinline__ int perm8_pos(int i) {
 // (q0,q4) (q1,q5) (q2,q6) (q3,q7), each fp16(q * s + b) with one rounding.
 __device__ __forceinline__ void dequant_word_f16_perm8(uint32_t w, __half2 s2, __half2 b2,
                                                        uint32_t (&out)[4]) {
-  uint32_t p[4];
-  nibbles_to_f16x2_1024(w, p);
+  // Nibbles 0/4 and 2/6 land in the low mantissa bits of 1024.0 (value
+  // 1024 + q); nibbles 1/5 and 3/7 are masked in place, four bits higher
+  // (value 1024 + 16 q), which saves two shifts on the integer pipe. Both
+  // forms are turned back into q exactly before the one rounding of q*s + b.
+  const uint32_t w8 = w >> 8;
+  const uint32_t p0 = lop3_and_or(w, 0x000F000Fu, 0x64006400u);
+  const uint32_t p1 = lop3_and_or(w, 0x00F000F0u, 0x64006400u);
+  const uint32_t p2 = lop3_and_or(w8, 0x000F000Fu, 0x64006400u);
+  const uint32_t p3 = lop3_and_or(w8, 0x00F000F0u, 0x64006400u);
   const __half2 c1024 = __floats2half2_rn(1024.0f, 1024.0f);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    __half2 v = *reinterpret_cast<__half2*>(&p[i]);
-    v = __hfma2(__hsub2(v, c1024), s2, b2);
-    out[i] = *reinterpret_cast<uint32_t*>(&v);
-  }
+  const __half2 c16th = __floats2half2_rn(0.0625f, 0.0625f);
+  const __half2 cm64 = __floats2half2_rn(-64.0f, -64.0f);
+  // (1024 + q) - 1024 = q and (1024 + 16 q) / 16 - 64 = q, both exact
+  const __half2 q0 = __hsub2(*reinterpret_cast<const __half2*>(&p0), c1024);
+  const __half2 q1 = __hfma2(*reinterpret_cast<const __half2*>(&p1), c16th, cm64);
+  const __half2 q2 = __hsub2(*reinterpret_cast<const __half2*>(&p2), c1024);
+  const __half2 q3 = __hfma2(*reinterpret_cast<const __half2*>(&p3), c16th, cm64);
+  const __half2 r0 = __hfma2(q0, s2, b2), r1 = __hfma2(q1, s2, b2);
+  const __half2 r2 = __hfma2(q2, s2, b2), r3 = __hfma2(q3, s2, b2);
+  out[0] = *reinterpret_cast<const uint32_t*>(&r0);
+  out[1] = *reinterpret_cast<const uint32_t*>(&r1);
+  out[2] = *reinterpret_cast<const uint32_t*>(&r2);
+  out[3] = *reinterpret_cast<const uint32_t*>(&r3);
 }
 
 // 8 fp16 in natural order (4 words) -> perm8 order

@@ -27,6 +27,10 @@ struct W4Dev {                    // one matrix set (device pointers)
 };
 
 // -------------------------------------------------------------- routing ---
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
+                                 const float* bias, int E, float* logits, cudaStream_t st);
+cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                                 float* topk_w, int32_t* blk_cnt, cudaStream_t st);
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
                                float* topk_w, float* logits, int32_t* blk_cnt,

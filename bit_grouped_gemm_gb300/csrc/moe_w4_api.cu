@@ -196,9 +196,12 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   float* logits = p->at<float>(p->L.logits);   // the top-k kernel reads them back
   cudaError_t e;
   e = timed(p, 0, st, [&] {
-    return launch_router_topk(x, T, d.hidden, router_w, router_bias, d.num_experts, d.top_k,
-                              p->at<int32_t>(p->L.topk_idx), p->at<float>(p->L.topk_w), logits,
-                              p->at<int32_t>(p->L.blk_cnt), st);
+    return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
+  });
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  e = timed(p, 8, st, [&] {
+    return launch_router_select(logits, T, d.num_experts, d.top_k, p->at<int32_t>(p->L.topk_idx),
+                                p->at<float>(p->L.topk_w), p->at<int32_t>(p->L.blk_cnt), st);
   });
   if (e != cudaSuccess) return MOE_ERR_CUDA;
   e = timed(p, 1, st, [&] {

@@ -17,10 +17,13 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // Router logits: logits[t][e] = sum_h x[t][h] * Wr[h][e] + bias[e], bf16
 // inputs, FP32 accumulation on mma.sync m16n8k16. One CTA computes a 64-token
-// x 64-expert tile (8 warps of 16 tokens x 32 experts) with a 3-stage
-// cp.async pipeline over K in chunks of 64.
+// x 128-expert tile: 8 warps of 32 tokens x 32 experts each (4 ldmatrix feed
+// 8 MMAs per 16-wide K step), with a 4-stage cp.async pipeline over K in
+// chunks of 64.
 // ---------------------------------------------------------------------------
-constexpr int kLgT = 64, kLgE = 64, kLgK = 64, kLgStages = 3, kLgStride = kLgK + 8;
+constexpr int kLgT = 64, kLgE = 128, kLgK = 64, kLgStages = 4;
+constexpr int kLgXStride = kLgK + 8, kLgWStride = kLgE + 8;   // padded rows (bank spread)
+constexpr int kLgXStage = kLgT * kLgXStride, kLgWStage = kLgK * kLgWStride;
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
@@ -60,57 +63,72 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, float* __restrict__ logits) {
   extern __shared__ __align__(128) uint8_t smem[];
-  uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);                  // [stage][64][72]
-  uint16_t* wr_s = xs_s + kLgStages * kLgT * kLgStride;                 // [stage][64 k][72]
+  uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);              // [stage][64 t][72]
+  uint16_t* wr_s = xs_s + kLgStages * kLgXStage;                    // [stage][64 k][136]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kLgT, e0 = blockIdx.y * kLgE;
-  const int wm = warp & 3, wn = warp >> 2;
+  const int wm = warp & 1, wn = warp >> 1;   // 2 x 4 warps: 32 tokens x 32 experts each
 
   auto stage = [&](int buf, int kc) {
     const int k0 = kc * kLgK;
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-      const int c = tid + 256 * i;            // 512 chunks of 16 B each for x and Wr
+    for (int i = 0; i < 2; ++i) {   // x: 64 rows x 8 pieces of 16 B
+      const int c = tid + 256 * i;
       const int r = c >> 3, col = (c & 7) * 8;
       const int t = t0 + r;
-      cp_async16(xs_s + (buf * kLgT + r) * kLgStride + col,
+      cp_async16(xs_s + buf * kLgXStage + r * kLgXStride + col,
                  x + (size_t)(t < T ? t : 0) * H + k0 + col, t < T ? 16 : 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {   // Wr: 64 k-rows x 16 pieces of 16 B
+      const int c = tid + 256 * i;
+      const int r = c >> 4, col = (c & 15) * 8;
       const int e = e0 + col;
-      cp_async16(wr_s + (buf * kLgK + r) * kLgStride + col,
+      cp_async16(wr_s + buf * kLgWStage + r * kLgWStride + col,
                  wr + (size_t)(k0 + r) * E + (e < E ? e : 0), e < E ? 16 : 0);
     }
     cp_async_commit();
   };
 
-  float acc[4][4];
+  float acc[2][4][4];
 #pragma unroll
-  for (int n = 0; n < 4; ++n)
+  for (int m = 0; m < 2; ++m)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) acc[n][i] = 0.f;
+    for (int n = 0; n < 4; ++n)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[m][n][i] = 0.f;
 
   const int nk = H / kLgK;
-  stage(0, 0);
-  if (nk > 1) stage(1, 1);
+#pragma unroll
+  for (int s = 0; s < kLgStages - 1; ++s)
+    if (s < nk) stage(s, s);
+    else cp_async_commit();
   for (int kc = 0; kc < nk; ++kc) {
-    if (kc + 1 < nk) cp_async_wait<1>(); else cp_async_wait<0>();
+    cp_async_wait<kLgStages - 2>();
     __syncthreads();
-    if (kc + 2 < nk) stage((kc + 2) % kLgStages, kc + 2);
-    const int buf = kc % kLgStages;
+    if (kc + kLgStages - 1 < nk) stage((kc + kLgStages - 1) % kLgStages, kc + kLgStages - 1);
+    else cp_async_commit();
+    const uint16_t* xb = xs_s + (kc % kLgStages) * kLgXStage;
+    const uint16_t* wb = wr_s + (kc % kLgStages) * kLgWStage;
 #pragma unroll
     for (int ks = 0; ks < kLgK / 16; ++ks) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(smem_u32(xs_s + (buf * kLgT + wm * 16 + (lane & 15)) * kLgStride + ks * 16 +
-                       (lane >> 4) * 8), a0, a1, a2, a3);
+      uint32_t a[2][4], b[4][2];
 #pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(smem_u32(wr_s + (buf * kLgK + ks * 16 + (lane & 15)) * kLgStride + wn * 32 +
-                           np * 16 + (lane >> 4) * 8), b0, b1, b2, b3);
-        mma_16816(acc[2 * np], a0, a1, a2, a3, b0, b1);
-        mma_16816(acc[2 * np + 1], a0, a1, a2, a3, b2, b3);
-      }
+      for (int m = 0; m < 2; ++m)
+        ldsm_x4(smem_u32(xb + (wm * 32 + m * 16 + (lane & 15)) * kLgXStride + ks * 16 + (lane >> 4) * 8),
+                a[m][0], a[m][1], a[m][2], a[m][3]);
+#pragma unroll
+      for (int np = 0; np < 2; ++np)
+        ldsm_x4_t(smem_u32(wb + (ks * 16 + (lane & 15)) * kLgWStride + wn * 32 + np * 16 + (lane >> 4) * 8),
+                  b[2 * np][0], b[2 * np][1], b[2 * np + 1][0], b[2 * np + 1][1]);
+#pragma unroll
+      for (int m = 0; m < 2; ++m)
+#pragma unroll
+        for (int n = 0; n < 4; ++n)
+          mma_16816(acc[m][n], a[m][0], a[m][1], a[m][2], a[m][3], b[n][0], b[n][1]);
     }
   }
+  cp_async_wait<0>();
   const int g = lane >> 2, c = lane & 3;
 #pragma unroll
   for (int n = 0; n < 4; ++n) {
@@ -118,23 +136,36 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
     if (e >= E) continue;
     const float b0 = bias ? bias[e] : 0.f, b1 = bias ? bias[e + 1] : 0.f;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int t = t0 + wm * 16 + g + 8 * h;
-      if (t < T)
-        *reinterpret_cast<float2*>(logits + (size_t)t * E + e) =
-            make_float2(acc[n][2 * h] + b0, acc[n][2 * h + 1] + b1);
-    }
+    for (int m = 0; m < 2; ++m)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const int t = t0 + wm * 32 + m * 16 + g + 8 * h;
+        if (t < T)
+          *reinterpret_cast<float2*>(logits + (size_t)t * E + e) =
+              make_float2(acc[m][n][2 * h] + b0, acc[m][n][2 * h + 1] + b1);
+      }
   }
 }
 
 // ---------------------------------------------------------------------------
-// Top-k + per-block histogram. One CTA = 32 tokens, one warp per token;
-// k rounds of a warp arg-max per token (higher logit first, lower index on
-// ties; a NaN logit ranks as -inf, and every round picks some not-yet-selected
-// expert, so indices are always valid). Weights: softmax over the selected
+// Top-k + per-block histogram. One CTA = 32 tokens, one warp per token.
+// Each of the k rounds takes the largest not-yet-selected logit (a lower
+// expert index first on ties; a NaN logit ranks as -inf; -0 counts as +0),
+// with the warp's choice made by two redux.sync reductions over an
+// order-preserving integer key: the maximum key, then the lowest expert index
+// holding it. Every round selects some expert not selected before, so the
+// indices are always valid and distinct. Weights: softmax over the selected
 // logits (equal to softmax over all E renormalised over the k). The block
 // writes its per-expert counts to blk_cnt[block][E].
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t order_key(float f) {   // monotone float -> uint32
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
+}
+
 template <int VPL>   // values per lane, E <= 32 * VPL
 __global__ void __launch_bounds__(1024) router_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
@@ -146,37 +177,35 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
   __syncthreads();
   if (t0 + warp < T) {
     const int t = t0 + warp;
-    float v[VPL];
+    uint32_t key[VPL];
 #pragma unroll
     for (int i = 0; i < VPL; ++i) {
       const int e = lane + 32 * i;
       const float l = e < E ? __ldg(logits + (size_t)t * E + e) : -INFINITY;
-      v[i] = isnan(l) ? -INFINITY : l;
+      key[i] = order_key(isnan(l) ? -INFINITY : l + 0.0f);   // + 0 turns -0 into +0
     }
-    uint32_t taken = 0;
+    uint32_t live = 0;   // bit i: lane's value i not selected yet and e < E
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (lane + 32 * i < E) live |= 1u << i;
     float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
     int my_idx = 0;
     for (int j = 0; j < k; ++j) {
-      float bv = -INFINITY;
-      int be = -1;
+      // this lane's best live value (lowest i, i.e. lowest expert, on ties)
+      uint32_t bk = 0;
+      int bi = -1;
 #pragma unroll
-      for (int i = 0; i < VPL; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E && !((taken >> i) & 1u) && (be < 0 || v[i] > bv || (v[i] == bv && e < be))) {
-          bv = v[i];
-          be = e;
+      for (int i = 0; i < VPL; ++i)
+        if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+          bk = key[i];
+          bi = i;
         }
-      }
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-        const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-        if (oe >= 0 && (be < 0 || ov > bv || (ov == bv && oe < be))) {
-          bv = ov;
-          be = oe;
-        }
-      }
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      // every real key is above 0, so a lane with nothing live never wins
+      const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+      const uint32_t cand = (bi >= 0 && bk == m) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+      const int be = (int)__reduce_min_sync(0xffffffffu, cand);
+      if ((be & 31) == lane) live &= ~(1u << (be >> 5));
+      const float bv = key_value(m);
       if (j == 0) sel_v0 = bv;
       const float pj = expf(bv - sel_v0);
       zsum += pj;
@@ -195,17 +224,20 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
   for (int e = tid; e < E; e += blockDim.x) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
 }
 
-cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
-                               const float* bias, int E, int k, int32_t* topk_idx,
-                               float* topk_w, float* logits, int32_t* blk_cnt,
-                               cudaStream_t st) {
+cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
+                                 const float* bias, int E, float* logits, cudaStream_t st) {
   if (!logits) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)kLgStages * (kLgT + kLgK) * kLgStride * 2;
+  const size_t smem = (size_t)kLgStages * (kLgXStage + kLgWStage) * 2;
   cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((T + kLgT - 1) / kLgT, (E + kLgE - 1) / kLgE);
   router_logits_kernel<<<grid, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                                 float* topk_w, int32_t* blk_cnt, cudaStream_t st) {
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   if (E <= 256)
     router_topk_kernel<8><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
@@ -214,6 +246,15 @@ cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* 
     router_topk_kernel<16><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
                                                             blk_cnt);
   return cudaGetLastError();
+}
+
+cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
+                               const float* bias, int E, int k, int32_t* topk_idx,
+                               float* topk_w, float* logits, int32_t* blk_cnt,
+                               cudaStream_t st) {
+  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, st);
+  if (e != cudaSuccess) return e;
+  return launch_router_select(logits, T, E, k, topk_idx, topk_w, blk_cnt, st);
 }
 
 // ---------------------------------------------------------------------------

@@ -209,9 +209,9 @@ moe_status moe_debug_wait_timeout(moe_plan_t plan, int limit_us, moe_stream_t st
 /* Kernel timing for profiling. When enabled, every kernel the plan launches
  * is bracketed by CUDA events on its stream. moe_read_timing synchronises,
  * adds up the elapsed times per kernel kind since the last read, and resets.
- * Kinds: 0 router, 1 scan, 2 scatter, 3 gather, 4 gate/up GEMM, 5 down GEMM,
- * 6 combine, 7 residual. */
-#define MOE_NUM_KERNEL_KINDS 8
+ * Kinds: 0 router logits, 1 scan, 2 scatter, 3 gather, 4 gate/up GEMM,
+ * 5 down GEMM, 6 combine, 7 residual, 8 top-k selection. */
+#define MOE_NUM_KERNEL_KINDS 9
 typedef struct {
   double ms[MOE_NUM_KERNEL_KINDS];
   long long launches[MOE_NUM_KERNEL_KINDS];
