@@ -16,6 +16,12 @@ the result copied back, inside the timed region.
 roofline: the dominant kernel (grouped gate/up GEMM) against the measured
 dense bf16 peak. cpu_baseline: the fp64 oracle on a bounded sample.
 
+--workload decode_t{1,4,8}_l40: the same 40-layer stack on a decode batch of
+T tokens through the small-M path. Every step copies a fresh batch from a
+pool of 64 pre-generated device batches and replays the 40-layer step from
+a CUDA graph; the roofline is HBM bandwidth over the packed bytes of the
+experts each layer's routing selects (counted from the routing itself).
+
 --impl reference times the oracle (the CPU reference of this build) on the
 same workload, a bounded sample per step.
 Multi-GPU: independent replicas (the block does not shard), one per rank.
@@ -37,6 +43,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-block prefill tokens/s (W4A16, 1 GB300) + % of tensor/HBM roofline"
+METRIC_DECODE = "MoE-block decode tokens/s (W4A16, 1 GB300) + % of HBM roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 PROFILE_GATEUP = os.path.join(ROOT, "profiles", "w4_grouped_gemm_tc_gateup_t4096.txt")
 GEMM_SRC = os.path.join(ROOT, "bit_grouped_gemm_gb300", "csrc", "gemm_tc.cu")
@@ -221,6 +228,8 @@ def main(argv=None):
     bg.load_library()
 
     w = workload(args)
+    if w.tokens <= 16:
+        return run_decode(args, w, ws, rank, local, pg)
     sh = w.shape
     T = w.tokens
     from bit_grouped_gemm_gb300 import synth
@@ -349,6 +358,154 @@ def main(argv=None):
         "kernels": kernels,
         "gpu_launches": gpu_launches,
         "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clk.summary(),
+    }
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    bg.moe_plan_destroy(plan)
+    if pg:
+        pg.destroy_process_group()
+
+
+def decode_step_bytes(w, layers, plan, pool, samples=8):
+    """Algorithmic HBM bytes of one decode step: for every layer, the packed
+    weights, scales and biases of each distinct routed expert the layer's
+    routing selects plus the shared expert's, and the router weight. Counted
+    by running the stack layer by layer (untimed) on `samples` pool batches
+    and averaging."""
+    import torch
+    from bit_grouped_gemm_gb300 import binding as bg, stack
+    from tests import parity
+    sh = w.shape
+    T = w.tokens
+    per_expert = 3 * (sh.hidden * sh.inter // 2 + 2 * 2 * sh.hidden * sh.inter // sh.group_size)
+    router = sh.hidden * sh.num_experts * 2
+    alpha = stack.residual_alpha(w.layers)
+    x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
+    xn = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+    total, experts = 0.0, 0
+    for i in range(samples):
+        x.copy_(pool[i])
+        bg.moe_residual_add(plan, x, None, T, 0.0, x, xn)
+        for L in layers:
+            r = bg.moe_route(plan, xn, T, L.router_w, L.router_bias)
+            active = int((parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)["counts"] > 0).sum())
+            experts += active
+            total += (active + int(sh.has_shared)) * per_expert + router
+            bg.moe_grouped_w4_ffn(plan, xn, T, r, L.routed_c, L.shared_c, y)
+            bg.moe_residual_add(plan, x, y, T, alpha, x, xn)
+    torch.cuda.synchronize()
+    return total / samples, experts / samples / w.layers
+
+
+def run_decode(args, w, ws, rank, local, pg):
+    """Decode: the 40-layer step on T <= 16 tokens, replayed from a CUDA graph
+    with a fresh batch per step; roofline = HBM bandwidth over the selected
+    experts' packed bytes."""
+    import torch
+    from bit_grouped_gemm_gb300 import binding as bg, stack, synth
+    sh = w.shape
+    T = w.tokens
+    layers = stack.make_layers(w, "cuda")
+    alpha = stack.residual_alpha(w.layers)
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), local)
+    pool = synth.decode_pool(w, 64, "cuda")
+    x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
+    xn = torch.empty_like(x)
+    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+    for i in range(3):
+        x.copy_(pool[i])
+        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+    torch.cuda.synchronize()
+    assert bg.moe_get_error(plan) == 0
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        x.copy_(pool[i % pool.shape[0]], non_blocking=True)
+        graph.replay()
+
+    for i in range(max(args.warmup, 0)):
+        step(i)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        ev0.record(stream)
+        for i in range(args.steps):
+            step(i)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = max_over_ranks(ev0.elapsed_time(ev1), pg)
+    assert bg.moe_get_error(plan) == 0
+    ms_per_step = ms / args.steps
+
+    # per-kernel breakdown: the same steps without the graph, library timing on
+    bg.moe_enable_timing(plan, True)
+    bg.moe_read_timing(plan)
+    for i in range(min(args.steps, 50)):
+        x.copy_(pool[i % pool.shape[0]])
+        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+    torch.cuda.synchronize()
+    kt = bg.moe_read_timing(plan)
+    bg.moe_enable_timing(plan, False)
+    nk = min(args.steps, 50)
+    kernels = {k: {"ms_per_step": v[0] / nk, "launches_per_step": v[1] / nk} for k, v in kt.items()}
+    gpu_launches = int(round(sum(v[1] for v in kt.values()) / nk)) * args.steps
+
+    # end to end: x from pinned host memory, result back, around each replay
+    e2e = None
+    if not args.no_e2e:
+        xh = pool[: min(64, pool.shape[0])].cpu().pin_memory()
+        out_h = torch.empty((T, sh.hidden), dtype=torch.bfloat16).pin_memory()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(args.steps):
+            x.copy_(xh[i % xh.shape[0]], non_blocking=True)
+            graph.replay()
+            out_h.copy_(x, non_blocking=True)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ems = max_over_ranks(e0.elapsed_time(e1), pg)
+        e2e = {"value": ws * T * args.steps / (ems / 1e3), "unit": "tokens/s",
+               "h2d_bytes_per_step": T * sh.hidden * 2, "d2h_bytes_per_step": T * sh.hidden * 2}
+
+    step_bytes, experts_per_layer = decode_step_bytes(w, layers, plan, pool)
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+    out = {
+        "metric": METRIC_DECODE, "value": ws * T * args.steps / (ms / 1e3), "unit": "tokens/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "tokens": T, "layers": w.layers, "hidden": sh.hidden,
+                   "inter": sh.inter, "experts": sh.num_experts, "top_k": sh.top_k,
+                   "shared_experts": int(sh.has_shared), "group_size": sh.group_size,
+                   "routing": w.routing + (f"(s={w.zipf_s})" if w.routing == "zipf" else ""),
+                   "graph": "40-layer step replayed from one CUDA graph",
+                   "inputs": "fresh batch per step from a pool of 64 device batches",
+                   "l2": "the selected experts' packed bytes per step "
+                         f"({step_bytes / 1e9:.2f} GB) exceed L2; weights of 40 layers (18.2 GB) rotate",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "whole 40-layer decode step (small-M grouped GEMMs + routing)",
+                     "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+                     "algorithmic_bytes_per_step": step_bytes,
+                     "distinct_routed_experts_per_layer": experts_per_layer},
+        "kernels": kernels,
+        "gpu_launches": gpu_launches,
+        "cpu_baseline": None,
         "e2e": e2e,
         "clocks": clk.summary(),
     }
