@@ -102,12 +102,21 @@ def profiled_traffic(profile_path, kernel_src):
 
 
 def max_over_ranks(v, pg):
+    """The largest of every rank's v (the job is as slow as its slowest
+    replica); v itself on a single process."""
     if pg is None:
         return v
     import torch
-    t = torch.tensor([float(v)], device="cuda")
+    dev = "cuda" if pg.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([float(v)], device=dev)
     pg.all_reduce(t, op=pg.ReduceOp.MAX)
     return float(t.item())
+
+
+def replica_value(world_size, tokens, steps, ms):
+    """Whole-job tokens/s of `world_size` replicas, each pushing `tokens`
+    tokens through `steps` steps, timed by the slowest rank (`ms`)."""
+    return world_size * tokens * steps / (ms / 1e3)
 
 
 class ClockSampler:
@@ -269,7 +278,7 @@ def main(argv=None):
     ms = max_over_ranks(ev0.elapsed_time(ev1), pg)
     assert bg.moe_get_error(plan) == 0
     ms_per_step = ms / args.steps
-    value = ws * T * args.steps / (ms / 1e3)
+    value = replica_value(ws, T, args.steps, ms)
 
     # --- the same steps again with CUDA events around every kernel launch
     # (library timing mode, events on the launching stream): the per-kernel
@@ -306,7 +315,7 @@ def main(argv=None):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), pg)
-        e2e = {"value": ws * T * args.steps / (ems / 1e3), "unit": "tokens/s",
+        e2e = {"value": replica_value(ws, T, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": xh.numel() * xh.element_size(),
                "d2h_bytes_per_step": out_h.numel() * out_h.element_size()}
 
@@ -476,7 +485,7 @@ def run_decode(args, w, ws, rank, local, pg):
         e1.record(stream)
         torch.cuda.synchronize()
         ems = max_over_ranks(e0.elapsed_time(e1), pg)
-        e2e = {"value": ws * T * args.steps / (ems / 1e3), "unit": "tokens/s",
+        e2e = {"value": replica_value(ws, T, args.steps, ems), "unit": "tokens/s",
                "h2d_bytes_per_step": T * sh.hidden * 2, "d2h_bytes_per_step": T * sh.hidden * 2}
 
     step_bytes, experts_per_layer = decode_step_bytes(w, layers, plan, pool)
@@ -484,7 +493,7 @@ def run_decode(args, w, ws, rank, local, pg):
     peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     achieved = step_bytes / (ms_per_step / 1e3) / 1e9
     out = {
-        "metric": METRIC_DECODE, "value": ws * T * args.steps / (ms / 1e3), "unit": "tokens/s",
+        "metric": METRIC_DECODE, "value": replica_value(ws, T, args.steps, ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
         "data": "synthetic",
