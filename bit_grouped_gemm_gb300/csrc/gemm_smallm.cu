@@ -12,8 +12,14 @@
 //     owns two 16-row m16n8k16 A tiles (gate and up rows for the gate/up
 //     pass, two down row slabs for the down pass); the tile's tokens are the
 //     n8 side, in passes of 8*NT tokens;
-//   * each thread streams 8 bytes of packed weights per row per group with a
-//     4-group register prefetch, and converts nibbles to fp16 "1024 + q" with
+//   * the unit's whole weight slab (128 rows of packed words, scales and
+//     biases) is copied into shared memory with cp.async at the start, all of
+//     it in flight at once and overlapped with the token staging, so HBM sees
+//     every CTA's bytes together (rows padded by 32 bytes so the fragment
+//     reads are conflict-free); when the slab and the tokens do not fit in
+//     shared memory, each thread streams its rows from global memory instead;
+//   * each thread reads 8 bytes of packed weights per row per group, and
+//     converts nibbles to fp16 "1024 + q" with
 //     one LOP3 per pair (exact); the MMA sums (1024+q)*x over one group of 64
 //     in FP32, and the group's affine map is applied to the 4 partial sums:
 //         sum_k w_k x_k = s * sum_k (1024+q_k) x_k + (b - 1024 s) * sum_k x_k
@@ -57,7 +63,19 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], uint32_t a0, uint32_t a
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-template <int NT>
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// Shared-memory slab of a unit: 128 weight rows (gate rows then up rows, or
+// 128 down rows) of K/8 words plus 8 words of padding, then the rows' scales
+// and biases. Bytes for reduction size K.
+__host__ __device__ __forceinline__ size_t slab_bytes(int K) {
+  return (size_t)128 * (K / 8 + 8) * 4 + (size_t)2 * 128 * (K / 64) * 2;
+}
+
+template <int NT, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = p.K;
@@ -65,6 +83,10 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
   const int xstride = K / 2 + 1;                  // words per staged token row
   uint32_t* xw = reinterpret_cast<uint32_t*>(smem);            // [8*NT][xstride]
   float* xg = reinterpret_cast<float*>(xw + 8 * NT * xstride);  // [8*NT][G]
+  const int wstride = K / 8 + 8;                  // words per slab row
+  uint32_t* slab = reinterpret_cast<uint32_t*>(xg + 8 * NT * G);  // [128][wstride]
+  uint16_t* slab_s = reinterpret_cast<uint16_t*>(slab + 128 * wstride);  // [128][G]
+  uint16_t* slab_b = slab_s + 128 * G;                                   // [128][G]
 
   const int n_routed = *p.num_tiles;
   const int n_shared = p.has_shared ? (p.T + kBM - 1) / kBM : 0;
@@ -112,6 +134,32 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
     nrow[1][0] = n0 + 16 + g;
     nrow[1][1] = n0 + 16 + g + 8;
   }
+  // slab row of (A tile mt, half h): gate rows 0..63 then up rows 64..127,
+  // or the 128 down rows in order
+  const int n0base = p.rows_per_unit * ch;
+  auto slab_row = [&](int mt, int h) {
+    return p.mode == 0 ? 64 * mt + (nrow[mt][h] - n0base) : nrow[mt][h] - n0base;
+  };
+  if (STAGE) {
+    // the whole slab in flight at once (16-byte cp.async, L2 only)
+    const int cpr = K / 32;                                 // 16-byte pieces per row
+    for (int idx = threadIdx.x; idx < 128 * cpr; idx += blockDim.x) {
+      const int r = idx / cpr, pc = idx - r * cpr;
+      const W4Dev& w = (p.mode == 0 && r >= 64) ? wb : wa;
+      const int grow = n0base + (p.mode == 0 ? (r & 63) : r);
+      cp_async16(slab + r * wstride + 4 * pc, w.q + (ebase + grow) * (size_t)(K / 8) + 4 * pc);
+    }
+    const int cps = G / 8;                                  // pieces of one row's scales
+    for (int idx = threadIdx.x; idx < 2 * 128 * cps; idx += blockDim.x) {
+      const int which = idx / (128 * cps), rem = idx - which * 128 * cps;
+      const int r = rem / cps, pc = rem - r * cps;
+      const W4Dev& w = (p.mode == 0 && r >= 64) ? wb : wa;
+      const int grow = n0base + (p.mode == 0 ? (r & 63) : r);
+      const uint16_t* src = (which ? w.b : w.s) + (ebase + grow) * (size_t)G + 8 * pc;
+      cp_async16((which ? slab_b : slab_s) + r * G + 8 * pc, src);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  }
   const uint2* qp[2][2];
   const uint2* sp[2][2];
   const uint2* bp[2][2];
@@ -120,10 +168,19 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const size_t row = ebase + nrow[mt][h];
-      qp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->q + row * (K / 8)) + c;
-      sp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->s + row * G);
-      bp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->b + row * G);
+      if (STAGE) {
+        const int r = slab_row(mt, h);
+        qp[mt][h] = reinterpret_cast<const uint2*>(slab + r * wstride) + c;
+        sp[mt][h] = reinterpret_cast<const uint2*>(slab_s + r * G);
+        bp[mt][h] = reinterpret_cast<const uint2*>(slab_b + r * G);
+      } else {
+        qp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->q + row * (K / 8)) + c;
+        sp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->s + row * G);
+        bp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->b + row * G);
+      }
     }
+  // global weights through the read-only path; the slab with plain loads
+  auto ld = [](const uint2* ptr) { return STAGE ? *ptr : __ldg(ptr); };
 
   for (int pass0 = 0; pass0 < rows; pass0 += 8 * NT) {
     const int prow = min(8 * NT, rows - pass0);
@@ -153,6 +210,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
       }
       xg[tr * G + grp] = sum;
     }
+    if (STAGE && pass0 == 0) asm volatile("cp.async.wait_all;" ::: "memory");
     __syncthreads();
 
     float tot[2][NT][4];
@@ -169,14 +227,14 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
 #pragma unroll
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-        for (int h = 0; h < 2; ++h) qr[i][mt][h] = __ldg(qp[mt][h] + 4 * i);
+        for (int h = 0; h < 2; ++h) qr[i][mt][h] = ld(qp[mt][h] + 4 * i);
     uint2 sr[2][2], br[2][2];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        sr[mt][h] = __ldg(sp[mt][h]);
-        br[mt][h] = __ldg(bp[mt][h]);
+        sr[mt][h] = ld(sp[mt][h]);
+        br[mt][h] = ld(bp[mt][h]);
       }
 
     for (int g0 = 0; g0 < G; g0 += kPF) {
@@ -186,8 +244,8 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
       for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
-          srn[mt][h] = more ? __ldg(sp[mt][h] + (g0 + kPF) / 4) : sr[mt][h];
-          brn[mt][h] = more ? __ldg(bp[mt][h] + (g0 + kPF) / 4) : br[mt][h];
+          srn[mt][h] = more ? ld(sp[mt][h] + (g0 + kPF) / 4) : sr[mt][h];
+          brn[mt][h] = more ? ld(bp[mt][h] + (g0 + kPF) / 4) : br[mt][h];
         }
 #pragma unroll
       for (int i = 0; i < kPF; ++i) {
@@ -205,7 +263,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-            for (int h = 0; h < 2; ++h) qr[i][mt][h] = __ldg(qp[mt][h] + 4 * (grp + kPF));
+            for (int h = 0; h < 2; ++h) qr[i][mt][h] = ld(qp[mt][h] + 4 * (grp + kPF));
         }
         float acc[2][NT][4];
 #pragma unroll
@@ -315,26 +373,26 @@ cudaError_t launch_gemm_smallm(int mode, const GemmProblem& g, cudaStream_t st) 
   if (grid < 1) return cudaSuccess;
   const int maxrows = g.T < kBM ? g.T : kBM;
   const int G = p.K / 64;
+  const int nt = maxrows <= 8 ? 1 : maxrows <= 16 ? 2 : 4;
+  const size_t base = (size_t)8 * nt * (p.K / 2 + 1) * 4 + (size_t)8 * nt * G * 4;
+  const size_t staged = base + sm::slab_bytes(p.K);
+  // staging copies scales in 16-byte pieces (8 groups): K a multiple of 512
+  const bool stage = staged <= 227 * 1024 && p.K % 512 == 0;
+  const size_t smem = stage ? staged : base;
+  auto launch = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, sm::kWarps * 32, smem, st>>>(p);
+    return cudaSuccess;
+  };
   cudaError_t e;
-  if (maxrows <= 8) {
-    const size_t smem = (size_t)8 * (p.K / 2 + 1) * 4 + (size_t)8 * G * 4;
-    e = cudaFuncSetAttribute(sm::w4_grouped_gemm_smallm<1>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    sm::w4_grouped_gemm_smallm<1><<<grid, sm::kWarps * 32, smem, st>>>(p);
-  } else if (maxrows <= 16) {
-    const size_t smem = (size_t)16 * (p.K / 2 + 1) * 4 + (size_t)16 * G * 4;
-    e = cudaFuncSetAttribute(sm::w4_grouped_gemm_smallm<2>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    sm::w4_grouped_gemm_smallm<2><<<grid, sm::kWarps * 32, smem, st>>>(p);
-  } else {
-    const size_t smem = (size_t)32 * (p.K / 2 + 1) * 4 + (size_t)32 * G * 4;
-    e = cudaFuncSetAttribute(sm::w4_grouped_gemm_smallm<4>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    sm::w4_grouped_gemm_smallm<4><<<grid, sm::kWarps * 32, smem, st>>>(p);
-  }
+  if (nt == 1)
+    e = stage ? launch(sm::w4_grouped_gemm_smallm<1, true>) : launch(sm::w4_grouped_gemm_smallm<1, false>);
+  else if (nt == 2)
+    e = stage ? launch(sm::w4_grouped_gemm_smallm<2, true>) : launch(sm::w4_grouped_gemm_smallm<2, false>);
+  else
+    e = stage ? launch(sm::w4_grouped_gemm_smallm<4, true>) : launch(sm::w4_grouped_gemm_smallm<4, false>);
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

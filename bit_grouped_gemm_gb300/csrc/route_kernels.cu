@@ -224,9 +224,102 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
   for (int e = tid; e < E; e += blockDim.x) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
 }
 
+// Router logits for decode-sized batches (T <= 16): a GEMV over the router
+// weight spread over E/16 CTAs, each taking 16 experts and all of K. Lane l
+// of warp w owns experts e0 + 8 (l & 1) .. +7 and the K slice
+// k = 16 w + (l >> 1) + 128 i: it issues all its 16-byte weight loads at once
+// (64 KiB in flight per CTA), sums its slice in FP32 for every token (x rows
+// staged in shared memory), and the 128 slices are added in a fixed order
+// (shuffles within the warp, then the 8 warps): deterministic.
+constexpr int kRsMaxT = 16;
+
+template <int NK>   // H / 128: 16-byte weight loads per thread
+__global__ void __launch_bounds__(256) router_logits_small_kernel(
+    const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
+    const float* __restrict__ bias, int E, float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                      // [T][H]
+  float* part = reinterpret_cast<float*>(smem + (size_t)kRsMaxT * H * 2);  // [8][16][kRsMaxT]
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int eo = lane & 1, ks = 16 * warp + (lane >> 1);
+  const int e0 = blockIdx.x * 16 + 8 * eo;
+  const bool valid = e0 < E;
+  uint4 wv[NK];
+#pragma unroll
+  for (int i = 0; i < NK; ++i)
+    if (valid) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(ks + 128 * i) * E + e0));
+  for (int i = tid; i < T * H / 8; i += blockDim.x)
+    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+  __syncthreads();
+  for (int t0 = 0; t0 < T; t0 += 4) {
+    float acc[4][8];
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
+    if (valid) {
+#pragma unroll
+      for (int i = 0; i < NK; ++i) {
+        const int k = ks + 128 * i;
+        const uint32_t wq[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
+        float w[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          w[2 * j] = __uint_as_float(wq[j] << 16);
+          w[2 * j + 1] = __uint_as_float(wq[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float xv = (t0 + t < T) ? bf16_to_f32(xs[(t0 + t) * H + k]) : 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(xv, w[j], acc[t][j]);
+        }
+      }
+    }
+    // add the 16 slices of this warp that share eo (lanes differing in bits 1..4)
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float v = acc[t][j];
+#pragma unroll
+        for (int off = 2; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        acc[t][j] = v;
+      }
+    if (lane < 2) {
+#pragma unroll
+      for (int t = 0; t < 4; ++t)
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (t0 + t < T) part[(warp * 16 + 8 * eo + j) * kRsMaxT + t0 + t] = acc[t][j];
+    }
+  }
+  __syncthreads();
+  if (tid < 16 * kRsMaxT) {
+    const int el = tid & 15, t = tid >> 4;
+    const int ee = blockIdx.x * 16 + el;
+    if (t < T && ee < E) {
+      float sum = 0.f;
+      for (int w8 = 0; w8 < 8; ++w8) sum += part[(w8 * 16 + el) * kRsMaxT + t];
+      logits[(size_t)t * E + ee] = sum + (bias ? bias[ee] : 0.f);
+    }
+  }
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
                                  const float* bias, int E, float* logits, cudaStream_t st) {
   if (!logits) return cudaErrorInvalidValue;
+  if (T <= kRsMaxT && (H == 512 || H == 1024 || H == 2048)) {
+    const size_t smem = (size_t)kRsMaxT * H * 2 + (size_t)8 * 16 * kRsMaxT * 4;
+    auto launch = [&](auto kern) -> cudaError_t {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      kern<<<(E + 15) / 16, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
+      return cudaGetLastError();
+    };
+    return H == 512 ? launch(router_logits_small_kernel<4>)
+           : H == 1024 ? launch(router_logits_small_kernel<8>) : launch(router_logits_small_kernel<16>);
+  }
   const size_t smem = (size_t)kLgStages * (kLgXStage + kLgWStage) * 2;
   cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

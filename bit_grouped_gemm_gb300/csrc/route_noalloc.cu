@@ -55,7 +55,7 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
                                         int num_experts, int top_k, const moe_routing* out,
                                         moe_stream_t stream) {
   if (!x || !router_w || !out) return MOE_ERR_INVALID_ARG;
-  if (T < 1 || hidden <= 0 || hidden % 32 || num_experts < 8 || num_experts % 8 ||
+  if (T < 1 || hidden <= 0 || hidden % 64 || num_experts < 8 || num_experts % 8 ||
       top_k < 1 || top_k > num_experts)
     return MOE_ERR_INVALID_ARG;
   if (T > kMaxTokens || num_experts > kMaxExperts || top_k > 32) return MOE_ERR_CAPACITY;

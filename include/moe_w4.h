@@ -183,7 +183,8 @@ moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, 
  * The caller passes x, router_w, router_bias (may be NULL) as for moe_route
  * and every output buffer in `out` (layouts as in moe_routing; block_map
  * must hold ceil(T*k/128) + E triples; logits is required, every buffer
- * 8-byte aligned). The library's
+ * 8-byte aligned; hidden a multiple of 64, num_experts a multiple of 8,
+ * otherwise MOE_ERR_INVALID_ARG). The library's
  * only scratch for this call is a fixed device array of 128 x 512 int32
  * (256 KB) in the library image, present on every GPU that loads the
  * library until the process exits; hence T <= 4096 and num_experts <= 512,

@@ -70,8 +70,11 @@ WL = synth.standard_workloads()
 SMALL = synth.MoEShape(hidden=256, inter=256, num_experts=16, top_k=4)
 
 
-@pytest.mark.parametrize("name", ["t128_uniform", "t512_zipf", "t2048_uniform", "t2048_zipf"])
+@pytest.mark.parametrize("name", ["t128_uniform", "t512_zipf", "t2048_uniform", "t2048_zipf",
+                                  "decode_t1_l40", "decode_t8_l40"])
 def test_route_bit_exact(name):
+    """Routing against the oracle; the decode sizes exercise the router's
+    GEMV path for batches of at most 16 tokens."""
     w = WL[name]
     c = Case(w)
     plan = make_plan(w)
