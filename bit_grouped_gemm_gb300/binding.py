@@ -81,6 +81,8 @@ def load_library(path: Optional[str] = None):
                                    ctypes.POINTER(MoeExperts), P, P]),
         "moe_forward_layer": (S, [P, P, I, P, P, ctypes.POINTER(MoeExperts),
                                   ctypes.POINTER(MoeExperts), P, P]),
+        "moe_forward_layer_residual": (S, [P, P, I, P, P, ctypes.POINTER(MoeExperts),
+                                           ctypes.POINTER(MoeExperts), ctypes.c_float, P, P, P]),
         "moe_residual_add": (S, [P, P, P, I, ctypes.c_float, P, P, P]),
         "moe_get_error": (S, [P]),
         "moe_debug_wait_timeout": (S, [P, I, P]),
@@ -175,6 +177,15 @@ def moe_forward_layer(plan: int, x, T: int, router_w, router_bias, routed: MoeEx
         plan, _ptr(x), T, _ptr(router_w), _ptr(router_bias), ctypes.byref(routed),
         ctypes.byref(shared) if shared is not None else None, _ptr(y), _stream(stream)),
         "moe_forward_layer")
+
+
+def moe_forward_layer_residual(plan: int, xn, T: int, router_w, router_bias, routed: MoeExperts,
+                               shared: Optional[MoeExperts], alpha: float, x, xn_out,
+                               stream=None) -> None:
+    _check(load_library().moe_forward_layer_residual(
+        plan, _ptr(xn), T, _ptr(router_w), _ptr(router_bias), ctypes.byref(routed),
+        ctypes.byref(shared) if shared is not None else None, float(alpha), _ptr(x),
+        _ptr(xn_out), _stream(stream)), "moe_forward_layer_residual")
 
 
 def moe_route_noalloc(x, T: int, hidden: int, router_w, router_bias, num_experts: int,

@@ -44,6 +44,11 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, in
                                int with_shared, uint16_t* xs, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
                            int k, int H, float* y, cudaStream_t st);
+// combine, then x = bf16(x + alpha * y) in place and xn = bf16(rmsnorm(x)),
+// without writing y (bit-identical to launch_combine + launch_residual_norm)
+cudaError_t launch_combine_residual_norm(const uint16_t* d, const float* d_sh, const int32_t* inv,
+                                         int T, int k, int H, float alpha, uint16_t* x,
+                                         uint16_t* xn, float eps, cudaStream_t st);
 cudaError_t launch_residual_norm(const uint16_t* x, const float* y, int T, int H, float alpha,
                                  uint16_t* x_out, uint16_t* xn, float eps, cudaStream_t st);
 cudaError_t launch_debug_wait(DevErr e, cudaStream_t st);

@@ -232,9 +232,17 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   return MOE_OK;
 }
 
+// The stack update fused into the combine (moe_forward_layer_residual).
+struct ResidualUpdate {
+  float alpha;
+  uint16_t* x;    // residual stream, updated in place
+  uint16_t* xn;   // next layer's RMS-normalised input
+};
+
+// Exactly one of y (the block output) and res (the fused stack update) is set.
 moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
                     const moe_experts* routed, const moe_experts* shared, float* y,
-                    cudaStream_t st) {
+                    const ResidualUpdate* res, cudaStream_t st) {
   const moe_plan_desc& d = p->d;
   const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
   const int hs = d.has_shared;
@@ -322,6 +330,10 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = timed(p, 6, st, [&] {
+    if (res)
+      return launch_combine_residual_norm(p->at<uint16_t>(p->L.d),
+                                          hs ? p->at<float>(p->L.dsh) : nullptr, r->inv, T, k, H,
+                                          res->alpha, res->x, res->xn, kRmsEps, st);
     return launch_combine(p->at<uint16_t>(p->L.d), hs ? p->at<float>(p->L.dsh) : nullptr,
                           r->inv, T, k, H, y, st);
   });
@@ -455,7 +467,7 @@ moe_status moe_grouped_w4_ffn(moe_plan_t p, const uint16_t* x, int T, const moe_
   if (!p || !r) return MOE_ERR_INVALID_ARG;
   moe_status s = check_ffn_args(p, x, T, r, routed, shared, y);
   if (s != MOE_OK) return s;
-  return ffn_impl(p, x, T, r, routed, shared, y, reinterpret_cast<cudaStream_t>(stream));
+  return ffn_impl(p, x, T, r, routed, shared, y, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint16_t* router_w,
@@ -470,7 +482,31 @@ moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint1
   moe_routing r;
   s = route_impl(p, x, T, router_w, router_bias, &r, false, st);
   if (s != MOE_OK) return s;
-  return ffn_impl(p, x, T, &r, routed, shared, y, st);
+  return ffn_impl(p, x, T, &r, routed, shared, y, nullptr, st);
+}
+
+moe_status moe_forward_layer_residual(moe_plan_t p, const uint16_t* xn, int T,
+                                      const uint16_t* router_w, const float* router_bias,
+                                      const moe_experts* routed, const moe_experts* shared,
+                                      float alpha, uint16_t* x, uint16_t* xn_out,
+                                      moe_stream_t stream) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  moe_status s = check_route_args(p, xn, T, router_w, router_bias);
+  if (s != MOE_OK) return s;
+  if (!x || !xn_out || !aligned16(x) || !aligned16(xn_out) || x == xn || x == xn_out)
+    return MOE_ERR_INVALID_ARG;
+  if ((s = check_experts(routed)) != MOE_OK) return s;
+  if (p->d.has_shared) {
+    if ((s = check_experts(shared)) != MOE_OK) return s;
+  } else if (shared) {
+    return MOE_ERR_INVALID_ARG;
+  }
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  moe_routing r;
+  s = route_impl(p, xn, T, router_w, router_bias, &r, false, st);
+  if (s != MOE_OK) return s;
+  const ResidualUpdate res{alpha, x, xn_out};
+  return ffn_impl(p, xn, T, &r, routed, shared, nullptr, &res, st);
 }
 
 moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const float* y, int T,

@@ -633,6 +633,94 @@ __global__ void __launch_bounds__(256) residual_norm_kernel(
   }
 }
 
+// Combine and stack update in one pass, one CTA per token row:
+//   y     = d_sh[t] + sum_j d[inv[t*k + j]]      (FP32, shared first, j in order)
+//   x     = bf16(x + alpha * y)                  (in place)
+//   xn    = bf16(x / sqrt(mean(x^2) + eps))      (mean over the bf16-rounded x)
+// Every FP32 operation is the one combine_kernel then residual_norm_kernel
+// perform, in the same order, so the result is bit-identical to the two
+// separate passes; y itself is never written.
+__global__ void __launch_bounds__(256) combine_residual_norm_kernel(
+    const uint16_t* __restrict__ d, const float* __restrict__ d_sh,
+    const int32_t* __restrict__ inv, int T, int k, int H, float alpha, uint16_t* x,
+    uint16_t* __restrict__ xn, float eps) {
+  __shared__ int rows_s[33];
+  __shared__ float warp_ss[8];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  for (int t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < k) rows_s[threadIdx.x] = inv[(size_t)t * k + threadIdx.x];
+    __syncthreads();
+    uint16_t* xr = x + (size_t)t * H;
+    float ss = 0.f;
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+      float acc[8];
+      if (d_sh) {
+        const float4* s4 = reinterpret_cast<const float4*>(d_sh + (size_t)t * H + h0);
+        const float4 a = __ldg(s4), b = __ldg(s4 + 1);
+        acc[0] = a.x; acc[1] = a.y; acc[2] = a.z; acc[3] = a.w;
+        acc[4] = b.x; acc[5] = b.y; acc[6] = b.z; acc[7] = b.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      }
+      for (int j = 0; j < k; ++j) {
+        uint4 v = __ldg(reinterpret_cast<const uint4*>(d + (size_t)rows_s[j] * H + h0));
+        const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          acc[2 * i] += bf16_lo(w[i]);
+          acc[2 * i + 1] += bf16_hi(w[i]);
+        }
+      }
+      const uint4 a = *reinterpret_cast<const uint4*>(xr + h0);
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+      float v[8];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        v[2 * j] = fmaf(alpha, acc[2 * j], bf16_lo(aw[j]));
+        v[2 * j + 1] = fmaf(alpha, acc[2 * j + 1], bf16_hi(aw[j]));
+      }
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        ow[j] = pack_bf16x2(v[2 * j], v[2 * j + 1]);
+        const float r0 = bf16_lo(ow[j]), r1 = bf16_hi(ow[j]);
+        ss = fmaf(r0, r0, fmaf(r1, r1, ss));
+      }
+      *reinterpret_cast<uint4*>(xr + h0) = o;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+    __syncthreads();
+    if (lane == 0) warp_ss[warp] = ss;
+    __syncthreads();
+    float tot = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += warp_ss[w];
+    const float rinv = 1.0f / sqrtf(tot / (float)H + eps);
+    // second pass over the row this thread wrote (its own values)
+    for (int h0 = threadIdx.x * 8; h0 < H; h0 += blockDim.x * 8) {
+      const uint4 a = *reinterpret_cast<const uint4*>(xr + h0);
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a);
+      uint4 o;
+      uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        ow[j] = pack_bf16x2(bf16_lo(aw[j]) * rinv, bf16_hi(aw[j]) * rinv);
+      *reinterpret_cast<uint4*>(xn + (size_t)t * H + h0) = o;
+    }
+  }
+}
+
+cudaError_t launch_combine_residual_norm(const uint16_t* d, const float* d_sh, const int32_t* inv,
+                                         int T, int k, int H, float alpha, uint16_t* x,
+                                         uint16_t* xn, float eps, cudaStream_t st) {
+  int blocks = T < 4096 ? T : 4096;
+  combine_residual_norm_kernel<<<blocks, 256, 0, st>>>(d, d_sh, inv, T, k, H, alpha, x, xn, eps);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_residual_norm(const uint16_t* x, const float* y, int T, int H, float alpha,
                                  uint16_t* x_out, uint16_t* xn, float eps, cudaStream_t st) {
   int blocks = T < 8192 ? T : 8192;

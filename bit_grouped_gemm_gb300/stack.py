@@ -56,17 +56,26 @@ def residual_alpha(num_layers: int) -> float:
 
 
 def run_stack(plan: int, x: torch.Tensor, xn: torch.Tensor, layers: List[DeviceLayer], T: int,
-              y_buf: torch.Tensor, alpha: float, stream=None) -> torch.Tensor:
+              y_buf: torch.Tensor, alpha: float, stream=None, fused: bool = True) -> torch.Tensor:
     """Run the layers in order on the residual stream ``x`` (bf16, updated in
     place) and return it. Every layer sees the RMS-normalised stream ``xn``
-    (bf16 scratch of x's shape); ``y_buf`` is the fp32 [T, H] layer output.
+    (bf16 scratch of x's shape); ``y_buf`` is the fp32 [T, H] layer output
+    (written only when ``fused`` is False).
 
         xn = rmsnorm(x)
         for each layer: y = moe(xn); x = bf16(x + alpha * y); xn = rmsnorm(x)
+
+    ``fused`` takes each layer and its update in one call
+    (moe_forward_layer_residual, y never written); otherwise
+    moe_forward_layer then moe_residual_add. Both give identical bits.
     """
     binding.moe_residual_add(plan, x, None, T, 0.0, x, xn, stream)
     for L in layers:
-        binding.moe_forward_layer(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
-                                  L.shared_c, y_buf, stream)
-        binding.moe_residual_add(plan, x, y_buf, T, alpha, x, xn, stream)
+        if fused:
+            binding.moe_forward_layer_residual(plan, xn, T, L.router_w, L.router_bias,
+                                               L.routed_c, L.shared_c, alpha, x, xn, stream)
+        else:
+            binding.moe_forward_layer(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
+                                      L.shared_c, y_buf, stream)
+            binding.moe_residual_add(plan, x, y_buf, T, alpha, x, xn, stream)
     return x

@@ -160,6 +160,19 @@ moe_status moe_forward_layer(moe_plan_t plan, const uint16_t* x, int T,
                              const moe_experts* routed, const moe_experts* shared,
                              float* y, moe_stream_t stream);
 
+/* moe_forward_layer followed by moe_residual_add(x, y, T, alpha, x, xn_out)
+ * in one call whose last pass updates the stack directly from the experts'
+ * outputs, so y is never written (the FP32 [T][H] round trip is saved):
+ *   y = moe(xn); x = bf16(x + alpha * y); xn_out = bf16(rmsnorm(x))
+ * Bit-identical to the two calls. xn (the layer's input) and xn_out may be
+ * the same buffer (the update runs after every read of xn); x must differ
+ * from both. Layouts as in moe_forward_layer and moe_residual_add. */
+moe_status moe_forward_layer_residual(moe_plan_t plan, const uint16_t* xn, int T,
+                                      const uint16_t* router_w, const float* router_bias,
+                                      const moe_experts* routed, const moe_experts* shared,
+                                      float alpha, uint16_t* x, uint16_t* xn_out,
+                                      moe_stream_t stream);
+
 /* Update between stacked layers (not part of the expert block itself):
  *   x_out[t] = bf16(x[t] + alpha * y[t])                 (skipped if y == NULL)
  *   xn_out[t] = bf16(x_out[t] / sqrt(mean_h x_out[t][h]^2 + 1e-6))

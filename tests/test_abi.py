@@ -80,4 +80,6 @@ def test_null_arguments_rejected(lib):
     assert lib.moe_plan_create(None, 0, None) == 1
     assert lib.moe_route(None, None, 1, None, None, None, None) == 1
     assert lib.moe_forward_layer(None, None, 1, None, None, None, None, None, None) == 1
+    assert lib.moe_forward_layer_residual(None, None, 1, None, None, None, None, 0.0, None, None,
+                                          None) == 1
     assert lib.moe_get_error(None) == 1

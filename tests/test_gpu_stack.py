@@ -17,6 +17,7 @@ routing map has.
 
 The decode stack (T = 8, 40 layers) is checked the same way on all 8 rows.
 """
+import dataclasses
 import os
 
 import numpy as np
@@ -127,3 +128,39 @@ def test_decode_stack_t8_l40():
     w = synth.standard_workloads()["decode_t8_l40"]
     stats = run_chain_check(w, np.arange(8, dtype=np.int32))
     assert sum(n for _, n, _ in stats) >= 0.9 * 8 * w.layers, stats
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("T", [8, 512])
+def test_fused_layer_update_bit_identical(T):
+    """moe_forward_layer_residual (combine and stack update in one pass, y never
+    written) gives the same bits as moe_forward_layer + moe_residual_add, on
+    the small-M path (T=8) and the tensor-core path (T=512), over 3 layers."""
+    from bit_grouped_gemm_gb300 import stack
+    w = dataclasses.replace(synth.standard_workloads()["prefill_t4096_l40_zipf"], tokens=T, layers=3)
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
+    try:
+        x0 = synth.tokens_x(w, "cuda")
+        y = torch.empty(x0.shape, dtype=torch.float32, device="cuda")
+        outs = []
+        for fused in (False, True):
+            x, xn = x0.clone(), torch.empty_like(x0)
+            stack.run_stack(plan, x, xn, layers, T, y, stack.residual_alpha(40), fused=fused)
+            torch.cuda.synchronize()
+            assert bg.moe_get_error(plan) == 0
+            outs.append((x.view(torch.int16).cpu().numpy(), xn.view(torch.int16).cpu().numpy()))
+        assert np.array_equal(outs[0][0], outs[1][0])
+        assert np.array_equal(outs[0][1], outs[1][1])
+        # argument errors of the fused call: x may alias neither the layer's
+        # input nor xn_out (status 1 = MOE_ERR_INVALID_ARG)
+        L = layers[0]
+        for x_arg, xn_out in ((xn, x), (x, x)):
+            with pytest.raises(bg.MoeError) as ei:
+                bg.moe_forward_layer_residual(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
+                                              L.shared_c, 0.1, x_arg, xn_out)
+            assert ei.value.status == 1
+    finally:
+        bg.moe_plan_destroy(plan)
