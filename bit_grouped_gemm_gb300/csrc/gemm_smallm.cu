@@ -77,6 +77,7 @@ __host__ __device__ __forceinline__ size_t slab_bytes(int K) {
 
 template <int NT, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Params p) {
+  pdl_begin();
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = p.K;
   const int G = K / 64;                           // groups
@@ -382,8 +383,7 @@ cudaError_t launch_gemm_smallm(int mode, const GemmProblem& g, cudaStream_t st) 
   auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    kern<<<grid, sm::kWarps * 32, smem, st>>>(p);
-    return cudaSuccess;
+    return launch_pdl(kern, dim3(grid), dim3(sm::kWarps * 32), smem, st, p);
   };
   cudaError_t e;
   if (nt == 1)

@@ -146,6 +146,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 }
 
 __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_constant__ Params p) {
+  pdl_begin();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024 - (raw_addr & 1023)) & 1023);
@@ -584,8 +585,7 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, D
   cudaError_t e = cudaFuncSetAttribute(tc::w4_grouped_gemm_tc,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  tc::w4_grouped_gemm_tc<<<grid, tc::kThreads, tc::kSmemBytes, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(tc::w4_grouped_gemm_tc, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, st, p);
 }
 
 #ifdef MOE_TC_STATS

@@ -12,6 +12,35 @@
 
 namespace moe {
 
+// ------------------------------------------------ programmatic dependent launch ---
+// Every kernel of this library is launched with launch_pdl and starts with
+// pdl_begin(): it waits until the previous kernel on the stream has completed
+// and its writes are visible, then lets the next kernel launch. The next
+// kernel can thus be scheduled while this one runs instead of after it
+// exits; it launches only once every CTA of this kernel has started, and
+// waits for this kernel's completion before touching memory, so stream order
+// is kept (and stays transitive along the stream).
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- errors ---
 // Device error word bits (latched with atomicOr, read by moe_get_error).
 enum : int { DEVERR_TIMEOUT = 1 };

@@ -62,6 +62,7 @@ __device__ __forceinline__ void cp_async_wait() {
 __global__ void __launch_bounds__(256) router_logits_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, float* __restrict__ logits) {
+  pdl_begin();
   extern __shared__ __align__(128) uint8_t smem[];
   uint16_t* xs_s = reinterpret_cast<uint16_t*>(smem);              // [stage][64 t][72]
   uint16_t* wr_s = xs_s + kLgStages * kLgXStage;                    // [stage][64 k][136]
@@ -170,6 +171,7 @@ template <int VPL>   // values per lane, E <= 32 * VPL
 __global__ void __launch_bounds__(1024) router_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt) {
+  pdl_begin();
   __shared__ int cnt_s[1024];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kRouterTB;
@@ -237,6 +239,7 @@ template <int NK>   // H / 128: 16-byte weight loads per thread
 __global__ void __launch_bounds__(256) router_logits_small_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, float* __restrict__ logits) {
+  pdl_begin();
   extern __shared__ __align__(16) uint8_t smem[];
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                      // [T][H]
   float* part = reinterpret_cast<float*>(smem + (size_t)kRsMaxT * H * 2);  // [8][16][kRsMaxT]
@@ -314,8 +317,7 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t
     auto launch = [&](auto kern) -> cudaError_t {
       cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
-      kern<<<(E + 15) / 16, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
-      return cudaGetLastError();
+      return launch_pdl(kern, dim3((E + 15) / 16), dim3(256), smem, st, x, T, H, wr, bias, E, logits);
     };
     return H == 512 ? launch(router_logits_small_kernel<4>)
            : H == 1024 ? launch(router_logits_small_kernel<8>) : launch(router_logits_small_kernel<16>);
@@ -325,20 +327,17 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   dim3 grid((T + kLgT - 1) / kLgT, (E + kLgE - 1) / kLgE);
-  router_logits_kernel<<<grid, 256, smem, st>>>(x, T, H, wr, bias, E, logits);
-  return cudaGetLastError();
+  return launch_pdl(router_logits_kernel, grid, dim3(256), smem, st, x, T, H, wr, bias, E, logits);
 }
 
 cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32_t* topk_idx,
                                  float* topk_w, int32_t* blk_cnt, cudaStream_t st) {
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   if (E <= 256)
-    router_topk_kernel<8><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
-                                                           blk_cnt);
-  else
-    router_topk_kernel<16><<<nblk, 32 * kRouterTB, 0, st>>>(logits, T, E, k, topk_idx, topk_w,
-                                                            blk_cnt);
-  return cudaGetLastError();
+    return launch_pdl(router_topk_kernel<8>, dim3(nblk), dim3(32 * kRouterTB), 0, st, logits, T, E,
+                      k, topk_idx, topk_w, blk_cnt);
+  return launch_pdl(router_topk_kernel<16>, dim3(nblk), dim3(32 * kRouterTB), 0, st, logits, T, E,
+                    k, topk_idx, topk_w, blk_cnt);
 }
 
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
@@ -387,6 +386,7 @@ __global__ void route_scan_kernel(int32_t* __restrict__ blk_cnt, int nblk, int T
                                   int32_t* __restrict__ cnt, int32_t* __restrict__ off,
                                   int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
                                   int32_t* __restrict__ num_tiles) {
+  pdl_begin();
   __shared__ int warp_sums[32];
   __shared__ int tot_rows, tot_tiles;
   const int e = threadIdx.x;
@@ -447,9 +447,7 @@ cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E, i
                               int32_t* off, int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
                               cudaStream_t st) {
   int threads = ((E + 31) / 32) * 32;
-  route_scan_kernel<<<1, threads, 0, st>>>(blk_cnt, nblk, T, k, E, cnt, off, tile_off, bmap,
-                                           num_tiles);
-  return cudaGetLastError();
+  return launch_pdl(route_scan_kernel, dim3(1), dim3(threads), 0, st, blk_cnt, nblk, T, k, E, cnt, off, tile_off, bmap, num_tiles);
 }
 
 // ---------------------------------------------------------------------------
@@ -459,6 +457,7 @@ cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E, i
 __global__ void __launch_bounds__(256) route_scatter_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_off, int T, int k,
     int E, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+  pdl_begin();
   __shared__ int idx_s[kRouterTB * 32];
   const int t0 = blockIdx.x * kRouterTB;
   const int nt = min(kRouterTB, T - t0);
@@ -480,8 +479,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(
 cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off, int T, int k,
                                  int E, int32_t* perm, int32_t* inv, cudaStream_t st) {
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
-  route_scatter_kernel<<<nblk, 256, 0, st>>>(topk_idx, blk_off, T, k, E, perm, inv);
-  return cudaGetLastError();
+  return launch_pdl(route_scatter_kernel, dim3(nblk), dim3(256), 0, st, topk_idx, blk_off, T, k, E, perm, inv);
 }
 
 // ---------------------------------------------------------------------------
@@ -494,6 +492,7 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                    int T, int k, int H, int with_shared,
                                    uint16_t* __restrict__ xs) {
+  pdl_begin();
   const int rows = T * k + (with_shared ? T : 0);
   const int lane = threadIdx.x & 31;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -516,8 +515,7 @@ cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, in
   const int rows = T * k + (with_shared ? T : 0);
   int blocks = (rows + 7) / 8;
   if (blocks > 4096) blocks = 4096;
-  gather_rows_kernel<<<blocks, 256, 0, st>>>(x, perm, T, k, H, with_shared, xs);
-  return cudaGetLastError();
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, x, perm, T, k, H, with_shared, xs);
 }
 
 // ---------------------------------------------------------------------------
@@ -530,6 +528,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ d_sh,
                                                       const int32_t* __restrict__ inv, int T,
                                                       int k, int H, float* __restrict__ y) {
+  pdl_begin();
   __shared__ int rows_s[33];
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
@@ -565,8 +564,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
                            int k, int H, float* y, cudaStream_t st) {
   int blocks = T < 4096 ? T : 4096;
-  combine_kernel<<<blocks, 256, 0, st>>>(d, d_sh, inv, T, k, H, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3(blocks), dim3(256), 0, st, d, d_sh, inv, T, k, H, y);
 }
 
 // ---------------------------------------------------------------------------
@@ -578,6 +576,7 @@ cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* 
 __global__ void __launch_bounds__(256) residual_norm_kernel(
     const uint16_t* __restrict__ x, const float* __restrict__ y, int T, int H, float alpha,
     uint16_t* __restrict__ x_out, uint16_t* __restrict__ xn, float eps) {
+  pdl_begin();
   __shared__ float warp_ss[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -644,6 +643,7 @@ __global__ void __launch_bounds__(256) combine_residual_norm_kernel(
     const uint16_t* __restrict__ d, const float* __restrict__ d_sh,
     const int32_t* __restrict__ inv, int T, int k, int H, float alpha, uint16_t* x,
     uint16_t* __restrict__ xn, float eps) {
+  pdl_begin();
   __shared__ int rows_s[33];
   __shared__ float warp_ss[8];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -717,15 +717,13 @@ cudaError_t launch_combine_residual_norm(const uint16_t* d, const float* d_sh, c
                                          int T, int k, int H, float alpha, uint16_t* x,
                                          uint16_t* xn, float eps, cudaStream_t st) {
   int blocks = T < 4096 ? T : 4096;
-  combine_residual_norm_kernel<<<blocks, 256, 0, st>>>(d, d_sh, inv, T, k, H, alpha, x, xn, eps);
-  return cudaGetLastError();
+  return launch_pdl(combine_residual_norm_kernel, dim3(blocks), dim3(256), 0, st, d, d_sh, inv, T, k, H, alpha, x, xn, eps);
 }
 
 cudaError_t launch_residual_norm(const uint16_t* x, const float* y, int T, int H, float alpha,
                                  uint16_t* x_out, uint16_t* xn, float eps, cudaStream_t st) {
   int blocks = T < 8192 ? T : 8192;
-  residual_norm_kernel<<<blocks, 256, 0, st>>>(x, y, T, H, alpha, x_out, xn, eps);
-  return cudaGetLastError();
+  return launch_pdl(residual_norm_kernel, dim3(blocks), dim3(256), 0, st, x, y, T, H, alpha, x_out, xn, eps);
 }
 
 // ---------------------------------------------------------------------------
