@@ -46,6 +46,7 @@ struct Params {
   const int32_t* bmap;
   const int32_t* num_tiles;
   const uint16_t* act_in;
+  const uint16_t* gather_x;   // gate/up: bf16 token rows read through perm (no gathered copy)
   uint16_t* out;
   float* out_sh;
   int out_ld;
@@ -77,7 +78,12 @@ __host__ __device__ __forceinline__ size_t slab_bytes(int K) {
 
 template <int NT, bool STAGE>
 __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Params p) {
-  pdl_begin();
+  // The down pass follows the gate/up pass, which writes neither the block
+  // map nor any weight: it finds its tile and starts its weight slab copy
+  // before waiting for that launch. The gate/up pass follows the routing and
+  // waits first.
+  const bool early = p.mode == 1;
+  if (!early) pdl_begin();
   extern __shared__ __align__(16) uint8_t smem[];
   const int K = p.K;
   const int G = K / 64;                           // groups
@@ -89,7 +95,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
   uint16_t* slab_s = reinterpret_cast<uint16_t*>(slab + 128 * wstride);  // [128][G]
   uint16_t* slab_b = slab_s + 128 * G;                                   // [128][G]
 
-  const int n_routed = *p.num_tiles;
+  const int n_routed = __ldcg(p.num_tiles);
   const int n_shared = p.has_shared ? (p.T + kBM - 1) / kBM : 0;
   const int u = blockIdx.x;
   if (u >= (n_routed + n_shared) * p.nchunk) return;
@@ -97,9 +103,9 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
   int e, m0, rows;
   bool shared;
   if (tile < n_routed) {
-    e = p.bmap[3 * tile];
-    m0 = p.bmap[3 * tile + 1];
-    rows = p.bmap[3 * tile + 2];
+    e = __ldcg(p.bmap + 3 * tile);
+    m0 = __ldcg(p.bmap + 3 * tile + 1);
+    rows = __ldcg(p.bmap + 3 * tile + 2);
     shared = false;
   } else {
     const int i = tile - n_routed;
@@ -180,6 +186,7 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
         bp[mt][h] = reinterpret_cast<const uint2*>(wm[mt]->b + row * G);
       }
     }
+  if (early) pdl_begin();
   // global weights through the read-only path; the slab with plain loads
   auto ld = [](const uint2* ptr) { return STAGE ? *ptr : __ldg(ptr); };
 
@@ -193,11 +200,21 @@ __global__ void __launch_bounds__(kWarps * 32) w4_grouped_gemm_smallm(const Para
       float sum = 0.f;
       uint32_t* dst = xw + tr * xstride + grp * 32;
       if (tr < prow) {
-        const uint4* src =
-            reinterpret_cast<const uint4*>(p.act_in + (size_t)(m0 + pass0 + tr) * K + grp * 64);
+        const int pos = m0 + pass0 + tr;
+        const uint16_t* row;
+        if (p.gather_x) {
+          const int src = pos < p.T * p.k ? __ldg(p.perm + pos) / p.k : pos - p.T * p.k;
+          row = p.gather_x + (size_t)src * K;
+        } else {
+          row = p.act_in + (size_t)pos * K;
+        }
+        const uint4* src = reinterpret_cast<const uint4*>(row + grp * 64);
 #pragma unroll
         for (int v = 0; v < 8; ++v) {
-          const uint4 x8 = __ldg(src + v);
+          uint4 x8 = __ldg(src + v);
+          if (p.gather_x)   // bf16 token values -> the fp16 perm8 operand of a gathered row
+            x8 = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(x8.x), bf16x2_to_f16x2_sat(x8.y),
+                                           bf16x2_to_f16x2_sat(x8.z), bf16x2_to_f16x2_sat(x8.w)));
           dst[4 * v + 0] = x8.x;   // (x0, x4)
           dst[4 * v + 1] = x8.y;   // (x1, x5)
           dst[4 * v + 2] = x8.z;   // (x2, x6)
@@ -360,6 +377,7 @@ cudaError_t launch_gemm_smallm(int mode, const GemmProblem& g, cudaStream_t st) 
   p.bmap = g.bmap;
   p.num_tiles = g.num_tiles;
   p.act_in = g.act_in;
+  p.gather_x = mode == 0 ? g.gather_x : nullptr;
   p.out = g.out;
   p.out_sh = g.out_sh;
   p.out_ld = g.out_ld;

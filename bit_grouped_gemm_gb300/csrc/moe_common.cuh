@@ -20,9 +20,20 @@ namespace moe {
 // exits; it launches only once every CTA of this kernel has started, and
 // waits for this kernel's completion before touching memory, so stream order
 // is kept (and stays transitive along the stream).
-__device__ __forceinline__ void pdl_begin() {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+//
+// Because every kernel here lets its dependents launch only after its own
+// wait, all launches before the previous one have completed by the time a
+// kernel starts. A kernel may therefore read, before pdl_wait(), memory that
+// the previous launch does not write: the weights (written by no launch of
+// this library), and buffers the launch before the previous one wrote (read
+// through L2 with ld.global.cg, never from L1).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_begin() {
+  pdl_wait();
+  pdl_trigger();
 }
 
 template <typename... KArgs, typename... Args>

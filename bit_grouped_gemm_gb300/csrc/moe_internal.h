@@ -40,6 +40,15 @@ cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E,
                               int32_t* num_tiles, cudaStream_t st);
 cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off, int T, int k,
                                  int E, int32_t* perm, int32_t* inv, cudaStream_t st);
+// The whole routing of a decode-sized batch in one launch (logits, top-k,
+// counts, scans, block map, scatter; bit-identical to the separate launches).
+// `arrive` is a device word that is 0 between launches.
+bool route_small_fits(int T, int H, int E, int k);
+cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* wr,
+                               const float* bias, int E, int k, float* logits,
+                               int32_t* topk_idx, float* topk_w, int32_t* cnt, int32_t* off,
+                               int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
+                               int32_t* perm, int32_t* inv, unsigned* arrive, cudaStream_t st);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
                                int with_shared, uint16_t* xs, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
@@ -63,7 +72,10 @@ struct GemmProblem {
   const int32_t* bmap;      // routed block map [tiles][3]
   const int32_t* num_tiles; // device count of routed tiles
   int max_routed_tiles;     // host upper bound (grid sizing)
-  const uint16_t* act_in;   // B operand rows [rows][K] bf16 (xs or act)
+  const uint16_t* act_in;   // B operand rows [rows][K] fp16 perm8 (xs or act)
+  const uint16_t* gather_x; // small-M gate/up only: when set, B row `pos` is read from
+                            // these bf16 token rows [T][K] (token perm[pos] / k, or
+                            // pos - T*k for the shared expert) instead of act_in
   uint16_t* out;            // output rows [rows][out_ld] bf16 (down: routed rows only)
   float* out_sh;            // down: the shared expert's rows, fp32 [T][out_ld]
   int out_ld;

@@ -24,7 +24,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
   size_t topk_idx, topk_w, logits, blk_cnt, cnt, off, tile_off, num_tiles, perm, inv, bmap,
-      err, xs, act, d, dsh, total;
+      err, arrive, xs, act, d, dsh, total;
   int nblk_max, max_tiles, rows_cap;
 };
 
@@ -52,6 +52,7 @@ Layout make_layout(const moe_plan_desc& d) {
   L.inv = take(Tm * k * 4);
   L.bmap = take((size_t)L.max_tiles * 3 * 4);
   L.err = take(16);
+  L.arrive = take(16);
   L.xs = take((size_t)L.rows_cap * d.hidden * 2);
   L.act = take((size_t)L.rows_cap * d.inter * 2);
   L.d = take(Tm * k * d.hidden * 2);
@@ -195,28 +196,40 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   float* logits = p->at<float>(p->L.logits);   // the top-k kernel reads them back
   cudaError_t e;
-  e = timed(p, 0, st, [&] {
-    return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
-  });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = timed(p, 8, st, [&] {
-    return launch_router_select(logits, T, d.num_experts, d.top_k, p->at<int32_t>(p->L.topk_idx),
-                                p->at<float>(p->L.topk_w), p->at<int32_t>(p->L.blk_cnt), st);
-  });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = timed(p, 1, st, [&] {
-    return launch_route_scan(p->at<int32_t>(p->L.blk_cnt), nblk, T, d.top_k, d.num_experts,
-                             p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
-                             p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
-                             p->at<int32_t>(p->L.num_tiles), st);
-  });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  e = timed(p, 2, st, [&] {
-    return launch_route_scatter(p->at<int32_t>(p->L.topk_idx), p->at<int32_t>(p->L.blk_cnt), T,
-                                d.top_k, d.num_experts, p->at<int32_t>(p->L.perm),
-                                p->at<int32_t>(p->L.inv), st);
-  });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (route_small_fits(T, d.hidden, d.num_experts, d.top_k)) {
+    e = timed(p, 0, st, [&] {
+      return launch_route_small(x, T, d.hidden, router_w, router_bias, d.num_experts, d.top_k,
+                                logits, p->at<int32_t>(p->L.topk_idx), p->at<float>(p->L.topk_w),
+                                p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
+                                p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
+                                p->at<int32_t>(p->L.num_tiles), p->at<int32_t>(p->L.perm),
+                                p->at<int32_t>(p->L.inv), p->at<unsigned>(p->L.arrive), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    e = timed(p, 0, st, [&] {
+      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 8, st, [&] {
+      return launch_router_select(logits, T, d.num_experts, d.top_k, p->at<int32_t>(p->L.topk_idx),
+                                  p->at<float>(p->L.topk_w), p->at<int32_t>(p->L.blk_cnt), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 1, st, [&] {
+      return launch_route_scan(p->at<int32_t>(p->L.blk_cnt), nblk, T, d.top_k, d.num_experts,
+                               p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
+                               p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
+                               p->at<int32_t>(p->L.num_tiles), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 2, st, [&] {
+      return launch_route_scatter(p->at<int32_t>(p->L.topk_idx), p->at<int32_t>(p->L.blk_cnt), T,
+                                  d.top_k, d.num_experts, p->at<int32_t>(p->L.perm),
+                                  p->at<int32_t>(p->L.inv), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
   if (out) {
     out->topk_idx = p->at<int32_t>(p->L.topk_idx);
     out->topk_w = p->at<float>(p->L.topk_w);
@@ -250,10 +263,15 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   const int path = d.gemm_path != 0 ? d.gemm_path : (T <= small_max ? 2 : 1);
   p->last_path = path;
 
-  cudaError_t e = timed(p, 3, st, [&] {
-    return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), st);
-  });
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  // the tensor-core path reads gathered rows with TMA; the small-M path reads
+  // the token rows itself
+  cudaError_t e = cudaSuccess;
+  if (path == 1) {
+    e = timed(p, 3, st, [&] {
+      return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
 
   long long bound = ((long long)T * k + kBM - 1) / kBM + E;
   if (bound > (long long)T * k) bound = (long long)T * k;
@@ -274,6 +292,7 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   g0.K = H;
   g0.N = I;
   g0.act_in = p->at<uint16_t>(p->L.xs);
+  g0.gather_x = path == 2 ? x : nullptr;
   g0.out = p->at<uint16_t>(p->L.act);
   g0.out_ld = I;
   g0.w0 = dev(routed->gate);
@@ -416,6 +435,7 @@ moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* ou
     return MOE_ERR_CUDA;
   }
   cudaMemset(p->scratch + p->L.err, 0, 16);
+  cudaMemset(p->scratch + p->L.arrive, 0, 16);
   bool ok = true;
   for (int i = 0; i < 4 && ok; ++i) {
     const uint32_t box_rows = 128u >> i;

@@ -167,7 +167,55 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
+// One token's selection by one warp, from its logits row (read through L2:
+// the row may have been written by other CTAs of the same launch). Lane j < k
+// gets the j-th selected expert and its renormalised softmax weight.
 template <int VPL>   // values per lane, E <= 32 * VPL
+__device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k,
+                                          int& idx, float& w) {
+  const int lane = threadIdx.x & 31;
+  uint32_t key[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    const float l = e < E ? __ldcg(row + e) : -INFINITY;
+    key[i] = order_key(isnan(l) ? -INFINITY : l + 0.0f);   // + 0 turns -0 into +0
+  }
+  uint32_t live = 0;   // bit i: lane's value i not selected yet and e < E
+#pragma unroll
+  for (int i = 0; i < VPL; ++i)
+    if (lane + 32 * i < E) live |= 1u << i;
+  float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
+  int my_idx = 0;
+  for (int j = 0; j < k; ++j) {
+    // this lane's best live value (lowest i, i.e. lowest expert, on ties)
+    uint32_t bk = 0;
+    int bi = -1;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i)
+      if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
+        bk = key[i];
+        bi = i;
+      }
+    // every real key is above 0, so a lane with nothing live never wins
+    const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
+    const uint32_t cand = (bi >= 0 && bk == m) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
+    const int be = (int)__reduce_min_sync(0xffffffffu, cand);
+    if ((be & 31) == lane) live &= ~(1u << (be >> 5));
+    const float bv = key_value(m);
+    if (j == 0) sel_v0 = bv;
+    const float pj = expf(bv - sel_v0);
+    zsum += pj;
+    if (lane == j) {
+      my_idx = be;
+      my_val = pj;
+    }
+  }
+  idx = my_idx;
+  w = my_val / zsum;
+}
+
+template <int VPL>
 __global__ void __launch_bounds__(1024) router_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
     float* __restrict__ topk_w, int32_t* __restrict__ blk_cnt) {
@@ -179,47 +227,13 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
   __syncthreads();
   if (t0 + warp < T) {
     const int t = t0 + warp;
-    uint32_t key[VPL];
-#pragma unroll
-    for (int i = 0; i < VPL; ++i) {
-      const int e = lane + 32 * i;
-      const float l = e < E ? __ldg(logits + (size_t)t * E + e) : -INFINITY;
-      key[i] = order_key(isnan(l) ? -INFINITY : l + 0.0f);   // + 0 turns -0 into +0
-    }
-    uint32_t live = 0;   // bit i: lane's value i not selected yet and e < E
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (lane + 32 * i < E) live |= 1u << i;
-    float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
-    int my_idx = 0;
-    for (int j = 0; j < k; ++j) {
-      // this lane's best live value (lowest i, i.e. lowest expert, on ties)
-      uint32_t bk = 0;
-      int bi = -1;
-#pragma unroll
-      for (int i = 0; i < VPL; ++i)
-        if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
-          bk = key[i];
-          bi = i;
-        }
-      // every real key is above 0, so a lane with nothing live never wins
-      const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
-      const uint32_t cand = (bi >= 0 && bk == m) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
-      const int be = (int)__reduce_min_sync(0xffffffffu, cand);
-      if ((be & 31) == lane) live &= ~(1u << (be >> 5));
-      const float bv = key_value(m);
-      if (j == 0) sel_v0 = bv;
-      const float pj = expf(bv - sel_v0);
-      zsum += pj;
-      if (lane == j) {
-        my_idx = be;
-        my_val = pj;
-      }
-    }
+    int idx;
+    float w;
+    topk_warp<VPL>(logits + (size_t)t * E, E, k, idx, w);
     if (lane < k) {
-      topk_idx[(size_t)t * k + lane] = my_idx;
-      topk_w[(size_t)t * k + lane] = my_val / zsum;
-      atomicAdd(&cnt_s[my_idx], 1);
+      topk_idx[(size_t)t * k + lane] = idx;
+      topk_w[(size_t)t * k + lane] = w;
+      atomicAdd(&cnt_s[idx], 1);
     }
   }
   __syncthreads();
@@ -230,27 +244,35 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
 // weight spread over E/16 CTAs, each taking 16 experts and all of K. Lane l
 // of warp w owns experts e0 + 8 (l & 1) .. +7 and the K slice
 // k = 16 w + (l >> 1) + 128 i: it issues all its 16-byte weight loads at once
-// (64 KiB in flight per CTA), sums its slice in FP32 for every token (x rows
-// staged in shared memory), and the 128 slices are added in a fixed order
-// (shuffles within the warp, then the 8 warps): deterministic.
+// (64 KiB in flight per CTA, before waiting for the previous launch, since
+// no launch writes the weights), sums its slice in FP32 for every token (x
+// rows staged in shared memory), and the 128 slices are added in a fixed
+// order (shuffles within the warp, then the 8 warps): deterministic.
 constexpr int kRsMaxT = 16;
 
+// The thread's weight slice (NK 16-byte loads, all issued at once).
 template <int NK>   // H / 128: 16-byte weight loads per thread
-__global__ void __launch_bounds__(256) router_logits_small_kernel(
-    const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
-    const float* __restrict__ bias, int E, float* __restrict__ logits) {
-  pdl_begin();
-  extern __shared__ __align__(16) uint8_t smem[];
+__device__ __forceinline__ void rs_load_w(const uint16_t* __restrict__ wr, int E, uint4 (&wv)[NK]) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int ks = 16 * warp + (lane >> 1), e0 = blockIdx.x * 16 + 8 * (lane & 1);
+  if (e0 < E) {
+#pragma unroll
+    for (int i = 0; i < NK; ++i)
+      wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(ks + 128 * i) * E + e0));
+  }
+}
+
+// Logits of this CTA's 16 experts for all T tokens, from the loaded slices.
+template <int NK>
+__device__ __forceinline__ void rs_logits(const uint16_t* __restrict__ x, int T, int H,
+                                          const uint4 (&wv)[NK], const float* __restrict__ bias,
+                                          int E, float* __restrict__ logits, uint8_t* smem) {
   uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                      // [T][H]
   float* part = reinterpret_cast<float*>(smem + (size_t)kRsMaxT * H * 2);  // [8][16][kRsMaxT]
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int eo = lane & 1, ks = 16 * warp + (lane >> 1);
   const int e0 = blockIdx.x * 16 + 8 * eo;
   const bool valid = e0 < E;
-  uint4 wv[NK];
-#pragma unroll
-  for (int i = 0; i < NK; ++i)
-    if (valid) wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(ks + 128 * i) * E + e0));
   for (int i = tid; i < T * H / 8; i += blockDim.x)
     reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
   __syncthreads();
@@ -307,6 +329,17 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
       logits[(size_t)t * E + ee] = sum + (bias ? bias[ee] : 0.f);
     }
   }
+}
+
+template <int NK>
+__global__ void __launch_bounds__(256) router_logits_small_kernel(
+    const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
+    const float* __restrict__ bias, int E, float* __restrict__ logits) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  uint4 wv[NK];
+  rs_load_w<NK>(wr, E, wv);   // weights: written by no launch of this library
+  pdl_begin();
+  rs_logits<NK>(x, T, H, wv, bias, E, logits, smem);
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
@@ -480,6 +513,131 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
                                  int E, int32_t* perm, int32_t* inv, cudaStream_t st) {
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   return launch_pdl(route_scatter_kernel, dim3(nblk), dim3(256), 0, st, topk_idx, blk_off, T, k, E, perm, inv);
+}
+
+// ---------------------------------------------------------------------------
+// The whole routing of a decode-sized batch (T <= 16) in one launch. The E/16
+// CTAs of the small-T logits GEMV each write their experts' logits; the CTA
+// that finishes last (an arrival counter, which that CTA sets back to 0 for
+// the next launch; no CTA ever waits) then does, in shared memory, each
+// token's top-k, the expert counts, both prefix scans, the block map and the
+// scatter. Same arithmetic in the same order as router_logits_small_kernel,
+// router_topk_kernel, route_scan_kernel and route_scatter_kernel, so every
+// output is bit-identical to theirs (one token block: its offsets are the
+// expert offsets).
+// ---------------------------------------------------------------------------
+constexpr int kRsThreads = 256;
+
+template <int NK, int VPL>
+__global__ void __launch_bounds__(kRsThreads) route_small_kernel(
+    const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
+    const float* __restrict__ bias, int E, int k, float* __restrict__ logits,
+    int32_t* __restrict__ topk_idx, float* __restrict__ topk_w, int32_t* __restrict__ cnt,
+    int32_t* __restrict__ off, int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
+    int32_t* __restrict__ num_tiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+    unsigned* __restrict__ arrive) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  __shared__ int idx_s[kRsMaxT * 32];
+  __shared__ int cnt_s[512], off_s[512];
+  __shared__ int warp_sums[32];
+  __shared__ int tot_rows, tot_tiles, is_last;
+  uint4 wv[NK];
+  rs_load_w<NK>(wr, E, wv);   // weights: written by no launch of this library
+  pdl_begin();
+  rs_logits<NK>(x, T, H, wv, bias, E, logits, smem);
+
+  __threadfence();   // this CTA's logits, before its arrival
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(arrive, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();   // the other CTAs' logits, after their arrivals
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) *arrive = 0u;
+  for (int e = tid; e < E; e += kRsThreads) cnt_s[e] = 0;
+  __syncthreads();
+
+  // top-k, one warp per token
+  for (int t = warp; t < T; t += kRsThreads / 32) {
+    int idx;
+    float w;
+    topk_warp<VPL>(logits + (size_t)t * E, E, k, idx, w);
+    if (lane < k) {
+      topk_idx[t * k + lane] = idx;
+      topk_w[t * k + lane] = w;
+      idx_s[t * k + lane] = idx;
+      atomicAdd(&cnt_s[idx], 1);
+    }
+  }
+  __syncthreads();
+
+  // scans and block map, one thread per expert (256 experts per pass)
+  int carry_rows = 0, carry_tiles = 0;
+  for (int e0 = 0; e0 < E; e0 += kRsThreads) {
+    const int e = e0 + tid;
+    const bool valid = e < E;
+    const int total = valid ? cnt_s[e] : 0;
+    const int tiles = (total + kBM - 1) / kBM;
+    const int o = block_excl_scan(total, warp_sums, &tot_rows) + carry_rows;
+    const int to = block_excl_scan(tiles, warp_sums, &tot_tiles) + carry_tiles;
+    if (valid) {
+      cnt[e] = total;
+      off[e] = o;
+      off_s[e] = o;
+      tile_off[e] = to;
+      for (int i = 0; i < tiles; ++i) {
+        const int rows = total - kBM * i;
+        int32_t* m = bmap + 3 * (size_t)(to + i);
+        m[0] = e;
+        m[1] = o + kBM * i;
+        m[2] = rows < kBM ? rows : kBM;
+      }
+    }
+    carry_rows += tot_rows;
+    carry_tiles += tot_tiles;
+  }
+  if (tid == 0) {
+    off[E] = carry_rows;
+    tile_off[E] = carry_tiles;
+    num_tiles[0] = carry_tiles;
+  }
+  __syncthreads();
+
+  // stable scatter: rank = earlier tokens that selected the same expert
+  for (int i = tid; i < T * k; i += kRsThreads) {
+    const int e = idx_s[i];
+    const int tl = i / k;
+    int rank = 0;
+    for (int s = 0; s < tl * k; ++s) rank += (idx_s[s] == e);
+    const int pos = off_s[e] + rank;
+    perm[pos] = i;
+    inv[i] = pos;
+  }
+}
+
+bool route_small_fits(int T, int H, int E, int k) {
+  return T <= kRsMaxT && (H == 512 || H == 1024 || H == 2048) && E <= 512 && k <= 32;
+}
+
+cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* wr,
+                               const float* bias, int E, int k, float* logits,
+                               int32_t* topk_idx, float* topk_w, int32_t* cnt, int32_t* off,
+                               int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
+                               int32_t* perm, int32_t* inv, unsigned* arrive, cudaStream_t st) {
+  if (!route_small_fits(T, H, E, k) || !arrive) return cudaErrorInvalidValue;
+  const size_t smem = (size_t)kRsMaxT * H * 2 + (size_t)8 * 16 * kRsMaxT * 4;
+  auto launch = [&](auto kern) -> cudaError_t {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3((E + 15) / 16), dim3(kRsThreads), smem, st, x, T, H, wr, bias, E,
+                      k, logits, topk_idx, topk_w, cnt, off, tile_off, bmap, num_tiles, perm, inv,
+                      arrive);
+  };
+  if (E <= 256)
+    return H == 512 ? launch(route_small_kernel<4, 8>)
+           : H == 1024 ? launch(route_small_kernel<8, 8>) : launch(route_small_kernel<16, 8>);
+  return H == 512 ? launch(route_small_kernel<4, 16>)
+         : H == 1024 ? launch(route_small_kernel<8, 16>) : launch(route_small_kernel<16, 16>);
 }
 
 // ---------------------------------------------------------------------------

@@ -74,3 +74,39 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     with pytest.raises(bg.MoeError) as ei:
         bg.moe_route_noalloc(x, 4097, 2048, L.router_w, None, 256, 8, r)
     assert ei.value.status == 4                        # MOE_ERR_CAPACITY
+
+
+# For batches of at most 16 tokens a plan routes in one launch (logits GEMV,
+# then top-k, scans, block map and scatter by the CTA that finishes last);
+# moe_route_noalloc always takes the separate launches. Same arithmetic in
+# the same order: every array, logits and weights included, must agree bit
+# for bit, over each width the fused kernel is specialised on, with and
+# without a bias, on two calls in a row (the arrival counter rearms).
+FUSED_CASES = [
+    # T, hidden, experts, top_k, routing
+    (1, 2048, 256, 8, "zipf"), (5, 2048, 256, 8, "uniform"), (16, 2048, 256, 8, "zipf"),
+    (3, 1024, 512, 8, "uniform"), (16, 512, 8, 2, "zipf"), (9, 1024, 64, 32, "uniform"),
+]
+
+
+@pytest.mark.parametrize("T,H,E,k,routing", FUSED_CASES)
+def test_fused_decode_routing_matches_separate_launches(T, H, E, k, routing):
+    sh = synth.MoEShape(hidden=H, inter=256, num_experts=E, top_k=k)
+    w = synth.Workload(f"fused{T}", T, 2, routing, seed=500 + T + E, shape=sh)
+    plan = bg.moe_plan_create(bg.plan_desc(hidden=H, inter=256, num_experts=E, top_k=k,
+                                           max_tokens=T), 0)
+    try:
+        for call in range(2):
+            wr = synth.router_weight(w, call, "cuda")
+            rb = synth.router_bias(w, call, "cuda")
+            x = synth.decode_pool(w, 2, "cuda")[call]
+            ref = parity.routing_to_numpy(bg.moe_route(plan, x, T, wr, rb), T, k, E)
+            bufs, r = caller_buffers(T, k, E)
+            bg.moe_route_noalloc(x, T, H, wr, rb, E, k, r)
+            got = parity.routing_to_numpy(r, T, k, E)
+            for key in ("logits", "topk_idx", "topk_w", "counts", "offsets", "tile_offsets",
+                        "perm", "inv", "block_map"):
+                assert np.array_equal(got[key], ref[key]), (call, key)
+            assert got["num_tiles"] == ref["num_tiles"]
+    finally:
+        bg.moe_plan_destroy(plan)
