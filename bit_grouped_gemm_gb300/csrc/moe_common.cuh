@@ -174,6 +174,17 @@ __device__ __forceinline__ void tma_prefetch_desc(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
 
+// Contiguous global -> shared copy by the TMA unit; both addresses 16-byte
+// aligned, `bytes` a multiple of 16; completion counted on `bar` (bytes).
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_u32(smem_dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
 // 2D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
                                             uint64_t* bar) {

@@ -96,7 +96,15 @@ struct TcMaps {
 cudaError_t launch_gemm_tc(int mode, const GemmProblem& p, const TcMaps& maps, DevErr err,
                            int num_sms, cudaStream_t st);
 
-// small-M mma.sync path (decode-sized token groups).
-cudaError_t launch_gemm_smallm(int mode, const GemmProblem& p, cudaStream_t st);
+// small-M mma.sync path (decode-sized token groups). `maps` holds the packed
+// words of w0/w1 (routed) and sw0/sw1 (shared) as uint32 [rows][K/8] maps with
+// 128-byte swizzle and boxes of 32 words x smallm_rows_per_unit(mode) rows.
+struct SmallMaps {
+  CUtensorMap q0, q1, sq0, sq1;
+};
+int smallm_rows_per_unit(int mode);
+bool smallm_fits(int H, int I);
+cudaError_t launch_gemm_smallm(int mode, const GemmProblem& p, const SmallMaps& maps, DevErr err,
+                               int num_sms, cudaStream_t st);
 
 }  // namespace moe

@@ -4,7 +4,9 @@
 // down GEMM, combine), all on the caller's stream with no host sync.
 #include <cstdio>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 #include <vector>
 
 #include "moe_internal.h"
@@ -75,6 +77,7 @@ moe_status check_desc(const moe_plan_desc* d) {
   if (d->top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
   if (d->gemm_path < 0 || d->gemm_path > 2) return MOE_ERR_INVALID_ARG;
+  if (d->gemm_path == 2 && !smallm_fits(d->hidden, d->inter)) return MOE_ERR_UNSUPPORTED;
   if (d->small_m_max_tokens < 0 || d->wait_limit_ms < 0) return MOE_ERR_INVALID_ARG;
   // 32-bit row/element indices inside the kernels
   if ((long long)d->max_tokens * (d->top_k + 1) * d->hidden >= (1LL << 31))
@@ -132,6 +135,23 @@ struct moe_plan {
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> ev_pool;
   int last_path = 0;
+  // encoded uint32 [rows][cols] maps of packed weights, by (base, rows, cols,
+  // box rows): a layer's maps are encoded on its first call only
+  std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t>, CUtensorMap> qmaps;
+
+  bool qmap(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    const auto key = std::make_tuple(base, rows, cols, box_rows);
+    auto it = qmaps.find(key);
+    if (it == qmaps.end()) {
+      CUtensorMap m;
+      if (!encode_2d(&m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 4, base, rows, cols, 32, box_rows))
+        return false;
+      if (qmaps.size() >= 4096) qmaps.clear();
+      it = qmaps.emplace(key, m).first;
+    }
+    *out = it->second;
+    return true;
+  }
 
   template <class T>
   T* at(size_t off) const {
@@ -260,7 +280,8 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
   const int hs = d.has_shared;
   const int small_max = d.small_m_max_tokens > 0 ? d.small_m_max_tokens : 16;
-  const int path = d.gemm_path != 0 ? d.gemm_path : (T <= small_max ? 2 : 1);
+  const int path =
+      d.gemm_path != 0 ? d.gemm_path : (T <= small_max && smallm_fits(H, I) ? 2 : 1);
   p->last_path = path;
 
   // the tensor-core path reads gathered rows with TMA; the small-M path reads
@@ -322,15 +343,14 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
       m0.b[i] = p->tm_xs[i];
       m1.b[i] = p->tm_act[i];
     }
-    const CUtensorMapDataType U32 = CU_TENSOR_MAP_DATA_TYPE_UINT32;
-    bool ok = encode_2d(&m0.q0, U32, 4, routed->gate.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
-              encode_2d(&m0.q1, U32, 4, routed->up.qweight, (uint64_t)E * I, H / 8, 32, 128) &&
-              encode_2d(&m1.q0, U32, 4, routed->down.qweight, (uint64_t)E * H, I / 8, 32, 128);
+    bool ok = p->qmap(&m0.q0, routed->gate.qweight, (uint64_t)E * I, H / 8, 128) &&
+              p->qmap(&m0.q1, routed->up.qweight, (uint64_t)E * I, H / 8, 128) &&
+              p->qmap(&m1.q0, routed->down.qweight, (uint64_t)E * H, I / 8, 128);
     m1.q1 = m1.q0;
     if (ok && hs) {
-      ok = encode_2d(&m0.sq0, U32, 4, shared->gate.qweight, I, H / 8, 32, 128) &&
-           encode_2d(&m0.sq1, U32, 4, shared->up.qweight, I, H / 8, 32, 128) &&
-           encode_2d(&m1.sq0, U32, 4, shared->down.qweight, H, I / 8, 32, 128);
+      ok = p->qmap(&m0.sq0, shared->gate.qweight, I, H / 8, 128) &&
+           p->qmap(&m0.sq1, shared->up.qweight, I, H / 8, 128) &&
+           p->qmap(&m1.sq0, shared->down.qweight, H, I / 8, 128);
       m1.sq1 = m1.sq0;
     } else if (ok) {
       m0.sq0 = m0.q0;
@@ -343,9 +363,26 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
     e = timed(p, 5, st, [&] { return launch_gemm_tc(1, g1, m1, p->err(), p->num_sms, st); });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
-    e = timed(p, 4, st, [&] { return launch_gemm_smallm(0, g0, st); });
+    const uint32_t r0 = smallm_rows_per_unit(0), r1 = smallm_rows_per_unit(1);
+    SmallMaps s0{}, s1{};
+    bool ok = p->qmap(&s0.q0, routed->gate.qweight, (uint64_t)E * I, H / 8, r0) &&
+              p->qmap(&s0.q1, routed->up.qweight, (uint64_t)E * I, H / 8, r0) &&
+              p->qmap(&s1.q0, routed->down.qweight, (uint64_t)E * H, I / 8, r1);
+    s1.q1 = s1.q0;
+    if (ok && hs) {
+      ok = p->qmap(&s0.sq0, shared->gate.qweight, I, H / 8, r0) &&
+           p->qmap(&s0.sq1, shared->up.qweight, I, H / 8, r0) &&
+           p->qmap(&s1.sq0, shared->down.qweight, H, I / 8, r1);
+      s1.sq1 = s1.sq0;
+    } else if (ok) {
+      s0.sq0 = s0.q0;
+      s0.sq1 = s0.q1;
+      s1.sq0 = s1.sq1 = s1.q0;
+    }
+    if (!ok) return MOE_ERR_CUDA;
+    e = timed(p, 4, st, [&] { return launch_gemm_smallm(0, g0, s0, p->err(), p->num_sms, st); });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = timed(p, 5, st, [&] { return launch_gemm_smallm(1, g1, st); });
+    e = timed(p, 5, st, [&] { return launch_gemm_smallm(1, g1, s1, p->err(), p->num_sms, st); });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   e = timed(p, 6, st, [&] {

@@ -240,120 +240,109 @@ __global__ void __launch_bounds__(1024) router_topk_kernel(
   for (int e = tid; e < E; e += blockDim.x) blk_cnt[(size_t)blockIdx.x * E + e] = cnt_s[e];
 }
 
-// Router logits for decode-sized batches (T <= 16): a GEMV over the router
-// weight spread over E/16 CTAs, each taking 16 experts and all of K. Lane l
-// of warp w owns experts e0 + 8 (l & 1) .. +7 and the K slice
-// k = 16 w + (l >> 1) + 128 i: it issues all its 16-byte weight loads at once
-// (64 KiB in flight per CTA, before waiting for the previous launch, since
-// no launch writes the weights), sums its slice in FP32 for every token (x
-// rows staged in shared memory), and the 128 slices are added in a fixed
-// order (shuffles within the warp, then the 8 warps): deterministic.
+// Router logits for decode-sized batches (T <= 16) on mma.sync: each of the
+// E/16 CTAs multiplies the (padded) 16 x H token block by its 16 experts'
+// H x 16 weight columns. The weight columns are copied into shared memory
+// (two arrays of 8 experts, 16 bytes per k) before waiting for the previous
+// launch, since no launch writes the weights; the tokens after it. Warp w
+// takes the K steps [w H/8, (w+1) H/8): B fragments by ldmatrix.trans, FP32
+// accumulation, and the 8 warps' partial sums are added in a fixed order:
+// deterministic. Rows of the token block past T are never read back (a
+// product row depends on its own token row only).
 constexpr int kRsMaxT = 16;
 
-// The thread's weight slice (NK 16-byte loads, all issued at once).
-template <int NK>   // H / 128: 16-byte weight loads per thread
-__device__ __forceinline__ void rs_load_w(const uint16_t* __restrict__ wr, int E, uint4 (&wv)[NK]) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int ks = 16 * warp + (lane >> 1), e0 = blockIdx.x * 16 + 8 * (lane & 1);
-  if (e0 < E) {
-#pragma unroll
-    for (int i = 0; i < NK; ++i)
-      wv[i] = __ldg(reinterpret_cast<const uint4*>(wr + (size_t)(ks + 128 * i) * E + e0));
-  }
+__host__ __device__ constexpr size_t rs_smem_bytes(int H) {
+  return (size_t)kRsMaxT * (H + 8) * 2 + (size_t)2 * H * 16 + (size_t)8 * 16 * 16 * 4;
 }
 
-// Logits of this CTA's 16 experts for all T tokens, from the loaded slices.
-template <int NK>
+__device__ __forceinline__ void cp_async_16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+
+// The CTA's weight columns: ws[a][k][0..7] = Wr[k][16 blockIdx + 8 a + 0..7].
+__device__ __forceinline__ void rs_load_w(const uint16_t* __restrict__ wr, int H, int E,
+                                          uint8_t* smem) {
+  uint16_t* ws = reinterpret_cast<uint16_t*>(smem + (size_t)kRsMaxT * (H + 8) * 2);
+  const int e0 = blockIdx.x * 16;
+  for (int i = threadIdx.x; i < 2 * H; i += blockDim.x) {
+    const int a = i & 1, k = i >> 1;
+    uint16_t* dst = ws + ((size_t)a * H + k) * 8;
+    if (e0 + 8 * a < E)
+      cp_async_16(dst, wr + (size_t)k * E + e0 + 8 * a);
+    else
+      *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Logits of this CTA's 16 experts for all T tokens.
 __device__ __forceinline__ void rs_logits(const uint16_t* __restrict__ x, int T, int H,
-                                          const uint4 (&wv)[NK], const float* __restrict__ bias,
-                                          int E, float* __restrict__ logits, uint8_t* smem) {
-  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                      // [T][H]
-  float* part = reinterpret_cast<float*>(smem + (size_t)kRsMaxT * H * 2);  // [8][16][kRsMaxT]
+                                          const float* __restrict__ bias, int E,
+                                          float* __restrict__ logits, uint8_t* smem) {
+  const int xstr = H + 8;                                           // padded token row
+  uint16_t* xs = reinterpret_cast<uint16_t*>(smem);                 // [16][H + 8]
+  const uint16_t* ws = xs + (size_t)kRsMaxT * xstr;                 // [2][H][8]
+  float* red = reinterpret_cast<float*>(smem + (size_t)kRsMaxT * xstr * 2 + (size_t)2 * H * 16);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int eo = lane & 1, ks = 16 * warp + (lane >> 1);
-  const int e0 = blockIdx.x * 16 + 8 * eo;
-  const bool valid = e0 < E;
-  for (int i = tid; i < T * H / 8; i += blockDim.x)
-    reinterpret_cast<uint4*>(xs)[i] = __ldg(reinterpret_cast<const uint4*>(x) + i);
+  const int vpr = H / 8;                                            // 16-byte pieces per row
+  for (int i = tid; i < T * vpr; i += blockDim.x) {
+    const int t = i / vpr, c = i - t * vpr;
+    cp_async_16(xs + (size_t)t * xstr + 8 * c, x + (size_t)t * H + 8 * c);
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
   __syncthreads();
-  for (int t0 = 0; t0 < T; t0 += 4) {
-    float acc[4][8];
+  float d[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  const int steps = H / 128;                                        // K steps of 16 per warp
+  const uint32_t a_base = smem_u32(xs + (size_t)(lane & 15) * xstr + 8 * (lane >> 4));
+  const uint32_t b_base = smem_u32(ws + ((size_t)(lane >> 4) * H + (lane & 15)) * 8);
+  for (int st = 0; st < steps; ++st) {
+    const int k0 = (warp * steps + st) * 16;
+    uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+    ldsm_x4(a_base + 2 * k0, a0, a1, a2, a3);
+    ldsm_x4_t(b_base + 16 * k0, b0, b1, b2, b3);
+    mma_16816(d[0], a0, a1, a2, a3, b0, b1);
+    mma_16816(d[1], a0, a1, a2, a3, b2, b3);
+  }
+  // red[warp][token][expert]
+  const int g = lane >> 2, c = lane & 3;
 #pragma unroll
-    for (int t = 0; t < 4; ++t)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) acc[t][j] = 0.f;
-    if (valid) {
-#pragma unroll
-      for (int i = 0; i < NK; ++i) {
-        const int k = ks + 128 * i;
-        const uint32_t wq[4] = {wv[i].x, wv[i].y, wv[i].z, wv[i].w};
-        float w[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          w[2 * j] = __uint_as_float(wq[j] << 16);
-          w[2 * j + 1] = __uint_as_float(wq[j] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float xv = (t0 + t < T) ? bf16_to_f32(xs[(t0 + t) * H + k]) : 0.f;
-#pragma unroll
-          for (int j = 0; j < 8; ++j) acc[t][j] = fmaf(xv, w[j], acc[t][j]);
-        }
-      }
-    }
-    // add the 16 slices of this warp that share eo (lanes differing in bits 1..4)
-#pragma unroll
-    for (int t = 0; t < 4; ++t)
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        float v = acc[t][j];
-#pragma unroll
-        for (int off = 2; off < 32; off <<= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-        acc[t][j] = v;
-      }
-    if (lane < 2) {
-#pragma unroll
-      for (int t = 0; t < 4; ++t)
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (t0 + t < T) part[(warp * 16 + 8 * eo + j) * kRsMaxT + t0 + t] = acc[t][j];
-    }
+  for (int nt = 0; nt < 2; ++nt) {
+    float* r = red + (size_t)warp * 256 + nt * 8 + 2 * c;
+    r[g * 16] = d[nt][0];
+    r[g * 16 + 1] = d[nt][1];
+    r[(g + 8) * 16] = d[nt][2];
+    r[(g + 8) * 16 + 1] = d[nt][3];
   }
   __syncthreads();
-  if (tid < 16 * kRsMaxT) {
-    const int el = tid & 15, t = tid >> 4;
-    const int ee = blockIdx.x * 16 + el;
-    if (t < T && ee < E) {
-      float sum = 0.f;
-      for (int w8 = 0; w8 < 8; ++w8) sum += part[(w8 * 16 + el) * kRsMaxT + t];
-      logits[(size_t)t * E + ee] = sum + (bias ? bias[ee] : 0.f);
-    }
+  const int t = tid >> 4, el = tid & 15, ee = blockIdx.x * 16 + el;
+  if (t < T && ee < E) {
+    float sum = 0.f;
+#pragma unroll
+    for (int w8 = 0; w8 < 8; ++w8) sum += red[w8 * 256 + t * 16 + el];
+    logits[(size_t)t * E + ee] = sum + (bias ? bias[ee] : 0.f);
   }
 }
 
-template <int NK>
 __global__ void __launch_bounds__(256) router_logits_small_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, float* __restrict__ logits) {
-  extern __shared__ __align__(16) uint8_t smem[];
-  uint4 wv[NK];
-  rs_load_w<NK>(wr, E, wv);   // weights: written by no launch of this library
+  extern __shared__ __align__(128) uint8_t smem[];
+  rs_load_w(wr, H, E, smem);   // weights: written by no launch of this library
   pdl_begin();
-  rs_logits<NK>(x, T, H, wv, bias, E, logits, smem);
+  rs_logits(x, T, H, bias, E, logits, smem);
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
                                  const float* bias, int E, float* logits, cudaStream_t st) {
   if (!logits) return cudaErrorInvalidValue;
-  if (T <= kRsMaxT && (H == 512 || H == 1024 || H == 2048)) {
-    const size_t smem = (size_t)kRsMaxT * H * 2 + (size_t)8 * 16 * kRsMaxT * 4;
-    auto launch = [&](auto kern) -> cudaError_t {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      if (e != cudaSuccess) return e;
-      return launch_pdl(kern, dim3((E + 15) / 16), dim3(256), smem, st, x, T, H, wr, bias, E, logits);
-    };
-    return H == 512 ? launch(router_logits_small_kernel<4>)
-           : H == 1024 ? launch(router_logits_small_kernel<8>) : launch(router_logits_small_kernel<16>);
+  if (T <= kRsMaxT && H % 128 == 0 && rs_smem_bytes(H) <= 227 * 1024) {
+    const size_t smem = rs_smem_bytes(H);
+    cudaError_t e = cudaFuncSetAttribute(router_logits_small_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(router_logits_small_kernel, dim3((E + 15) / 16), dim3(256), smem, st, x, T,
+                      H, wr, bias, E, logits);
   }
   const size_t smem = (size_t)kLgStages * (kLgXStage + kLgWStage) * 2;
   cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
@@ -528,7 +517,7 @@ cudaError_t launch_route_scatter(const int32_t* topk_idx, const int32_t* blk_off
 // ---------------------------------------------------------------------------
 constexpr int kRsThreads = 256;
 
-template <int NK, int VPL>
+template <int VPL>
 __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, int k, float* __restrict__ logits,
@@ -536,15 +525,14 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
     int32_t* __restrict__ off, int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
     int32_t* __restrict__ num_tiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
     unsigned* __restrict__ arrive) {
-  extern __shared__ __align__(16) uint8_t smem[];
+  extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int idx_s[kRsMaxT * 32];
   __shared__ int cnt_s[512], off_s[512];
   __shared__ int warp_sums[32];
   __shared__ int tot_rows, tot_tiles, is_last;
-  uint4 wv[NK];
-  rs_load_w<NK>(wr, E, wv);   // weights: written by no launch of this library
+  rs_load_w(wr, H, E, smem);   // weights: written by no launch of this library
   pdl_begin();
-  rs_logits<NK>(x, T, H, wv, bias, E, logits, smem);
+  rs_logits(x, T, H, bias, E, logits, smem);
 
   __threadfence();   // this CTA's logits, before its arrival
   __syncthreads();
@@ -616,7 +604,7 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
 }
 
 bool route_small_fits(int T, int H, int E, int k) {
-  return T <= kRsMaxT && (H == 512 || H == 1024 || H == 2048) && E <= 512 && k <= 32;
+  return T <= kRsMaxT && H % 128 == 0 && rs_smem_bytes(H) <= 200 * 1024 && E <= 512 && k <= 32;
 }
 
 cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* wr,
@@ -625,7 +613,7 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
                                int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
                                int32_t* perm, int32_t* inv, unsigned* arrive, cudaStream_t st) {
   if (!route_small_fits(T, H, E, k) || !arrive) return cudaErrorInvalidValue;
-  const size_t smem = (size_t)kRsMaxT * H * 2 + (size_t)8 * 16 * kRsMaxT * 4;
+  const size_t smem = rs_smem_bytes(H);
   auto launch = [&](auto kern) -> cudaError_t {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
@@ -633,11 +621,7 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
                       k, logits, topk_idx, topk_w, cnt, off, tile_off, bmap, num_tiles, perm, inv,
                       arrive);
   };
-  if (E <= 256)
-    return H == 512 ? launch(route_small_kernel<4, 8>)
-           : H == 1024 ? launch(route_small_kernel<8, 8>) : launch(route_small_kernel<16, 8>);
-  return H == 512 ? launch(route_small_kernel<4, 16>)
-         : H == 1024 ? launch(route_small_kernel<8, 16>) : launch(route_small_kernel<16, 16>);
+  return E <= 256 ? launch(route_small_kernel<8>) : launch(route_small_kernel<16>);
 }
 
 // ---------------------------------------------------------------------------
