@@ -64,6 +64,8 @@ struct Params {
   const float* topk_w;
   const int32_t* perm;
   W4Dev w0, w1, sw0, sw1;     // scales and biases (packed words come through the maps)
+  W4Dev next, snext;          // gate/up: down matrices to prefetch into L2 (q null: none)
+  int next_K, next_rows;      // their reduction size, and rows per gate/up unit
   SmallMaps maps;
   DevErr err;
 };
@@ -209,6 +211,16 @@ __global__ void __launch_bounds__(kThreads) w4_grouped_gemm_smallm(const __grid_
           tma_load_2d(slab + ((size_t)m * nb + bx) * ru * 128, map, 32 * bx, grow0, &slab_bar[b]);
         bulk_load(slab + L.s + (size_t)m * sbytes, w.s + (size_t)grow0 * G, sbytes, &slab_bar[b]);
         bulk_load(slab + L.b + (size_t)m * sbytes, w.b + (size_t)grow0 * G, sbytes, &slab_bar[b]);
+      }
+      // gate/up: this unit's share of the expert's down rows goes to L2 now,
+      // so that the down pass finds them there
+      const W4Dev& nw = x.shared ? p.snext : p.next;
+      if (nw.q) {
+        const size_t r0 = (size_t)(x.shared ? 0 : x.e * p.K) + (size_t)p.next_rows * x.ch;
+        const uint32_t rows = (uint32_t)p.next_rows;
+        bulk_prefetch_l2(nw.q + r0 * (p.next_K / 8), rows * (uint32_t)(p.next_K / 2));
+        bulk_prefetch_l2(nw.s + r0 * (p.next_K / 64), rows * (uint32_t)(p.next_K / 32));
+        bulk_prefetch_l2(nw.b + r0 * (p.next_K / 64), rows * (uint32_t)(p.next_K / 32));
       }
     }
   };
@@ -550,6 +562,19 @@ cudaError_t launch_gemm_smallm(int mode, const GemmProblem& g, const SmallMaps& 
   p.w1 = g.w1;
   p.sw0 = g.sw0;
   p.sw1 = g.sw1;
+  // prefetch shares: the down matrices have K (= H) rows per expert, split
+  // evenly over the gate/up units of an expert (16-byte multiples only)
+  p.next = p.snext = W4Dev{nullptr, nullptr, nullptr};
+  p.next_K = g.next_K;
+  p.next_rows = 0;
+  if (mode == 0 && g.next.q && g.K % p.nchunk == 0) {
+    const int rows = g.K / p.nchunk;
+    if ((long long)rows * (g.next_K / 32) % 16 == 0) {
+      p.next = g.next;
+      p.snext = g.has_shared ? g.snext : W4Dev{nullptr, nullptr, nullptr};
+      p.next_rows = rows;
+    }
+  }
   p.maps = maps;
   p.err = err;
   // persistent CTAs (one per SM: the kernel takes the whole register file)

@@ -185,6 +185,12 @@ __device__ __forceinline__ void bulk_load(void* smem_dst, const void* src, uint3
       : "memory");
 }
 
+// Prefetch of a contiguous global range into L2 (16-byte aligned address,
+// size a multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // 2D tiled load global -> shared, completion counted on `bar` (bytes).
 __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, int x, int y,
                                             uint64_t* bar) {

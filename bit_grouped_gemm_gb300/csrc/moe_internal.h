@@ -49,6 +49,19 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
                                int32_t* topk_idx, float* topk_w, int32_t* cnt, int32_t* off,
                                int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
                                int32_t* perm, int32_t* inv, unsigned* arrive, cudaStream_t st);
+// Selection through scatter of a prefill-sized batch in one cooperative
+// launch, from the logits (bit-identical to launch_router_select +
+// launch_route_scan + launch_route_scatter). `arrive` is 0 between launches;
+// `gen` is a generation word the launch advances. route_large_fits tells
+// whether the blocks can all be resident.
+// `cnt8` holds route_large_cnt8_bytes(blocks, E) bytes of scratch.
+bool route_large_fits(int T, int E, int k, int num_sms);
+size_t route_large_cnt8_bytes(int nblk, int E);
+cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                               float* topk_w, uint8_t* cnt8, int32_t* cnt, int32_t* off,
+                               int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
+                               int32_t* perm, int32_t* inv, unsigned* arrive, unsigned* gen,
+                               DevErr err, cudaStream_t st);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
                                int with_shared, uint16_t* xs, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
@@ -83,6 +96,9 @@ struct GemmProblem {
   const int32_t* perm;      // down: position -> slot
   W4Dev w0, w1;             // routed: gate,up (mode 0) or down,down (mode 1)
   W4Dev sw0, sw1;           // shared expert, same roles
+  W4Dev next, snext;        // small-M gate/up only: the down matrices (routed, shared),
+                            // whose rows each unit prefetches into L2 (q null: none)
+  int next_K;               // reduction size of the down matrices (I)
 };
 
 // tcgen05 tensor-core path. `maps` holds the encoded tensor maps the kernel

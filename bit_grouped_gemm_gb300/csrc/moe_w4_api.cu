@@ -25,7 +25,7 @@ struct TimedLaunch {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
-  size_t topk_idx, topk_w, logits, blk_cnt, cnt, off, tile_off, num_tiles, perm, inv, bmap,
+  size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
       err, arrive, xs, act, d, dsh, total;
   int nblk_max, max_tiles, rows_cap;
 };
@@ -46,6 +46,7 @@ Layout make_layout(const moe_plan_desc& d) {
   L.topk_w = take(Tm * k * 4);
   L.logits = take(Tm * E * 4);
   L.blk_cnt = take((size_t)L.nblk_max * E * 4);
+  L.cnt8 = take(route_large_cnt8_bytes(L.nblk_max, (int)E));
   L.cnt = take(E * 4);
   L.off = take((E + 1) * 4);
   L.tile_off = take((E + 1) * 4);
@@ -226,6 +227,21 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
                                 p->at<int32_t>(p->L.inv), p->at<unsigned>(p->L.arrive), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else if (route_large_fits(T, d.num_experts, d.top_k, p->num_sms)) {
+    e = timed(p, 0, st, [&] {
+      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    e = timed(p, 8, st, [&] {
+      unsigned* w = p->at<unsigned>(p->L.arrive);
+      return launch_route_large(logits, T, d.num_experts, d.top_k, p->at<int32_t>(p->L.topk_idx),
+                                p->at<float>(p->L.topk_w), p->at<uint8_t>(p->L.cnt8),
+                                p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
+                                p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
+                                p->at<int32_t>(p->L.num_tiles), p->at<int32_t>(p->L.perm),
+                                p->at<int32_t>(p->L.inv), w, w + 1, p->err(), st);
+    });
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     e = timed(p, 0, st, [&] {
       return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
@@ -321,6 +337,11 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   if (hs) {
     g0.sw0 = dev(shared->gate);
     g0.sw1 = dev(shared->up);
+  }
+  if (path == 2) {   // the small-M gate/up pass prefetches the down rows into L2
+    g0.next = dev(routed->down);
+    if (hs) g0.snext = dev(shared->down);
+    g0.next_K = I;
   }
   // down: B = act [rows][I], out = d [rows][H]
   GemmProblem g1 = g;

@@ -625,6 +625,257 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
 }
 
 // ---------------------------------------------------------------------------
+// Selection, counts, scans, block map and scatter of a prefill-sized batch in
+// one cooperative launch (all CTAs resident at once). CTA b takes tokens
+// [32 b, 32 b + 32): one warp per token selects its top-k (the same
+// topk_warp as router_topk_kernel) and the CTA writes its per-expert counts.
+// A grid barrier follows (the last CTA to arrive sets the arrival counter
+// back to 0 and advances a generation word; the others wait for it, bounded:
+// on a timeout they latch the error and skip the scatter). Then every CTA
+// reads the whole count table (one batch of loads from L2) and derives, in
+// the same order as route_scan_kernel, the expert totals and offsets and its
+// own block's offsets, and scatters its slots; CTA 0 also writes the totals,
+// offsets, tile offsets and block map. Every output is bit-identical to
+// router_topk_kernel + route_scan_kernel + route_scatter_kernel.
+// ---------------------------------------------------------------------------
+constexpr int kRlThreads = 32 * kRouterTB;   // one warp per token
+constexpr int kRlMaxPer = 32;                // blocks per scanning thread (counts held in registers)
+
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Threads per expert in the scans (a power of two), each over a range of blocks.
+__host__ __device__ inline int rl_tpe(int E) {
+  int tpe = 1;
+  while (tpe * 2 * E <= kRlThreads && tpe < 32) tpe *= 2;
+  return tpe;
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(kRlThreads) route_large_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,
+    float* __restrict__ topk_w, uint8_t* cnt8, int np, int32_t* __restrict__ cnt,
+    int32_t* __restrict__ off, int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
+    int32_t* __restrict__ num_tiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+    unsigned* arrive, unsigned* gen, DevErr err) {
+  pdl_begin();
+  __shared__ int idx_s[kRouterTB * 32];
+  __shared__ int cnt_s[512];
+  __shared__ int part_s[1024], pre_s[1024];   // per-(range, expert): block sums, sums before b
+  __shared__ int boff_s[512];                 // this block's first position per expert
+  __shared__ int wrows_s[16], wtiles_s[16];
+  __shared__ int go;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nblk = gridDim.x, b = blockIdx.x;
+  const int t0 = b * kRouterTB;
+  const int nt = min(kRouterTB, T - t0);
+  for (int i = tid; i < E; i += kRlThreads) cnt_s[i] = 0;
+  __syncthreads();
+
+  // ---- top-k and this block's counts
+  if (warp < nt) {
+    const int t = t0 + warp;
+    int idx;
+    float w;
+    topk_warp<VPL>(logits + (size_t)t * E, E, k, idx, w);
+    if (lane < k) {
+      topk_idx[(size_t)t * k + lane] = idx;
+      topk_w[(size_t)t * k + lane] = w;
+      idx_s[warp * k + lane] = idx;
+      atomicAdd(&cnt_s[idx], 1);
+    }
+  }
+  __syncthreads();
+  // counts as bytes, expert-major (at most 32 per block and expert)
+  for (int e = tid; e < E; e += kRlThreads) cnt8[(size_t)e * np + b] = (uint8_t)cnt_s[e];
+
+  // ---- grid barrier (the block's counts are ordered before its arrival by
+  // the CTA barrier and thread 0's fence, which is cumulative)
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned g0 = ld_relaxed_u32(gen);   // moves only after every arrival
+    int ok = 1;
+    if (atomicAdd(arrive, 1u) == (unsigned)nblk - 1) {
+      *arrive = 0u;
+      st_release_u32(gen, g0 + 1u);
+    } else if (ld_relaxed_u32(gen) == g0) {
+      const unsigned long long start = globaltimer_ns();
+      while (ld_relaxed_u32(gen) == g0) {
+        __nanosleep(100);
+        if (globaltimer_ns() - start > err.limit_ns) {
+          report_timeout(err, 30);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");
+    go = ok;
+  }
+  __syncthreads();
+  if (!go) return;
+
+  // ---- totals, offsets and this block's offsets, from the whole count table:
+  // thread (e, q) takes blocks [q per, (q + 1) per) of expert e (per a
+  // multiple of 16), its counts in one batch of 16-byte loads
+  const int tpe = rl_tpe(E);
+  const int e = tid % E, q = tid / E;
+  const bool act = q < tpe;
+  const int per = (nblk + tpe - 1) / tpe + 15 & ~15;
+  const int b0 = min(nblk, q * per), b1 = min(nblk, b0 + per);
+  uint4 cv[kRlMaxPer / 16];
+#pragma unroll
+  for (int i = 0; i < kRlMaxPer / 16; ++i)
+    cv[i] = act && b0 + 16 * i < b1
+                ? __ldcg(reinterpret_cast<const uint4*>(cnt8 + (size_t)e * np + b0) + i)
+                : make_uint4(0u, 0u, 0u, 0u);
+  int sum = 0, pre = 0;
+#pragma unroll
+  for (int i = 0; i < kRlMaxPer; ++i) {
+    const uint4 v = cv[i >> 4];
+    const uint32_t wd = (i & 15) < 4 ? v.x : (i & 15) < 8 ? v.y : (i & 15) < 12 ? v.z : v.w;
+    const int c = b0 + i < b1 ? (int)((wd >> (8 * (i & 3))) & 0xFFu) : 0;
+    sum += c;
+    if (b0 + i < b) pre += c;
+  }
+  if (act) {
+    part_s[q * E + e] = sum;
+    pre_s[q * E + e] = pre;
+  }
+  __syncthreads();
+  // expert totals (threads tid < E) and their exclusive scans over experts:
+  // shuffles inside each warp, then the warps' sums
+  int tot = 0, tiles = 0, before = 0;
+  if (tid < E) {
+#pragma unroll
+    for (int qq = 0; qq < 32; ++qq)
+      if (qq < tpe) {
+        tot += part_s[qq * E + tid];
+        before += pre_s[qq * E + tid];
+      }
+    tiles = (tot + kBM - 1) / kBM;
+  }
+  int ri = tot, ti = tiles;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int rn = __shfl_up_sync(0xffffffffu, ri, o);
+    const int tn = __shfl_up_sync(0xffffffffu, ti, o);
+    if (lane >= o) {
+      ri += rn;
+      ti += tn;
+    }
+  }
+  if (lane == 31 && warp < 16) {
+    wrows_s[warp] = ri;
+    wtiles_s[warp] = ti;
+  }
+  __syncthreads();
+  if (tid < E) {
+    int ro = ri - tot, to = ti - tiles;
+#pragma unroll
+    for (int w2 = 0; w2 < 16; ++w2)
+      if (w2 < warp) {
+        ro += wrows_s[w2];
+        to += wtiles_s[w2];
+      }
+    boff_s[tid] = ro + before;
+    if (b == 0) {
+      cnt[tid] = tot;
+      off[tid] = ro;
+      tile_off[tid] = to;
+      for (int i = 0; i < tiles; ++i) {
+        const int rows = tot - kBM * i;
+        int32_t* m = bmap + 3 * (size_t)(to + i);
+        m[0] = tid;
+        m[1] = ro + kBM * i;
+        m[2] = rows < kBM ? rows : kBM;
+      }
+    }
+  }
+  if (b == 0 && tid == 0) {
+    int rows_all = 0, tiles_all = 0;
+    for (int w2 = 0; w2 < (E + 31) / 32; ++w2) {
+      rows_all += wrows_s[w2];
+      tiles_all += wtiles_s[w2];
+    }
+    off[E] = rows_all;
+    tile_off[E] = tiles_all;
+    num_tiles[0] = tiles_all;
+  }
+  __syncthreads();
+
+  // ---- stable scatter of this block's slots
+  const int nslots = nt * k;
+  for (int i = tid; i < nslots; i += kRlThreads) {
+    const int tl = i / k;
+    const int ex = idx_s[i];
+    int rank = 0;
+    for (int s2 = 0; s2 < tl * k; ++s2) rank += (idx_s[s2] == ex);
+    const int pos = boff_s[ex] + rank;
+    const int slot = t0 * k + i;
+    perm[pos] = slot;
+    inv[slot] = pos;
+  }
+}
+
+// Bytes of the expert-major count array for nblk blocks (with the slack the
+// last block's vector loads may read past the end).
+size_t route_large_cnt8_bytes(int nblk, int E) {
+  const size_t np = (size_t)(nblk + 15) / 16 * 16;
+  return np * E + (size_t)kRlMaxPer * 32;
+}
+
+// Blocks the cooperative launch needs resident at once, and whether they fit.
+bool route_large_fits(int T, int E, int k, int num_sms) {
+  if (E > 512 || k > 32 || T < 1) return false;
+  const int nblk = (T + kRouterTB - 1) / kRouterTB;
+  const int tpe = rl_tpe(E);
+  if (((nblk + tpe - 1) / tpe + 15 & ~15) > kRlMaxPer) return false;
+  int dev = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+    return false;
+  auto occ = [&](auto kern) {
+    return cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRlThreads, 0);
+  };
+  const cudaError_t e = E <= 256 ? occ(route_large_kernel<8>) : occ(route_large_kernel<16>);
+  return e == cudaSuccess && nblk <= per_sm * num_sms;
+}
+
+cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t* topk_idx,
+                               float* topk_w, uint8_t* cnt8, int32_t* cnt, int32_t* off,
+                               int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
+                               int32_t* perm, int32_t* inv, unsigned* arrive, unsigned* gen,
+                               DevErr err, cudaStream_t st) {
+  const int nblk = (T + kRouterTB - 1) / kRouterTB;
+  const int np = (nblk + 15) / 16 * 16;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(nblk);
+  cfg.blockDim = dim3(kRlThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  // cooperative (the blocks wait on the last one), with ordinary stream
+  // order: the launch starts once the previous kernel has completed
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (E <= 256)
+    return cudaLaunchKernelEx(&cfg, route_large_kernel<8>, logits, T, E, k, topk_idx, topk_w, cnt8,
+                              np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err);
+  return cudaLaunchKernelEx(&cfg, route_large_kernel<16>, logits, T, E, k, topk_idx, topk_w, cnt8,
+                            np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err);
+}
+
+// ---------------------------------------------------------------------------
 // Gather: xs[pos] = x[perm[pos] / k] for routed positions, and
 // xs[T*k + t] = x[t] for the shared expert's rows, converted from bf16 to the
 // GEMMs' fp16 operand type (exact inside fp16's range, saturating outside),

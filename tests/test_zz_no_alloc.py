@@ -76,21 +76,25 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert ei.value.status == 4                        # MOE_ERR_CAPACITY
 
 
-# For batches of at most 16 tokens a plan routes in one launch (logits GEMV,
-# then top-k, scans, block map and scatter by the CTA that finishes last);
-# moe_route_noalloc always takes the separate launches. Same arithmetic in
-# the same order: every array, logits and weights included, must agree bit
-# for bit, over each width the fused kernel is specialised on, with and
-# without a bias, on two calls in a row (the arrival counter rearms).
+# A plan routes a batch of at most 16 tokens in one launch (logits GEMV, then
+# top-k, scans, block map and scatter by the CTA that finishes last), and a
+# larger batch in two (the logits GEMM, then one cooperative launch for
+# selection through scatter); moe_route_noalloc always takes the separate
+# launches. Same arithmetic in the same order: every array, logits and
+# weights included, must agree bit for bit, over each width the fused
+# kernels are specialised on, with and without a bias, on two calls in a row
+# (the arrival counter and the generation word rearm).
 FUSED_CASES = [
     # T, hidden, experts, top_k, routing
     (1, 2048, 256, 8, "zipf"), (5, 2048, 256, 8, "uniform"), (16, 2048, 256, 8, "zipf"),
     (3, 1024, 512, 8, "uniform"), (16, 512, 8, 2, "zipf"), (9, 1024, 64, 32, "uniform"),
+    (17, 2048, 256, 8, "zipf"), (300, 1024, 512, 8, "zipf"), (2048, 2048, 256, 8, "uniform"),
+    (4096, 2048, 256, 8, "zipf"), (999, 512, 8, 2, "uniform"), (77, 512, 64, 32, "zipf"),
 ]
 
 
 @pytest.mark.parametrize("T,H,E,k,routing", FUSED_CASES)
-def test_fused_decode_routing_matches_separate_launches(T, H, E, k, routing):
+def test_fused_routing_matches_separate_launches(T, H, E, k, routing):
     sh = synth.MoEShape(hidden=H, inter=256, num_experts=E, top_k=k)
     w = synth.Workload(f"fused{T}", T, 2, routing, seed=500 + T + E, shape=sh)
     plan = bg.moe_plan_create(bg.plan_desc(hidden=H, inter=256, num_experts=E, top_k=k,
