@@ -25,7 +25,7 @@ struct TimedLaunch {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
-  size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
+  size_t topk_idx, topk_w, logits, wt, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
       err, arrive, xs, act, d, dsh, total;
   int nblk_max, max_tiles, rows_cap;
 };
@@ -45,6 +45,7 @@ Layout make_layout(const moe_plan_desc& d) {
   L.topk_idx = take(Tm * k * 4);
   L.topk_w = take(Tm * k * 4);
   L.logits = take(Tm * E * 4);
+  L.wt = take(E * d.hidden * 2);   // router weight, transposed (tensor-core logits)
   L.blk_cnt = take((size_t)L.nblk_max * E * 4);
   L.cnt8 = take(route_large_cnt8_bytes(L.nblk_max, (int)E));
   L.cnt = take(E * 4);
@@ -87,41 +88,6 @@ moe_status check_desc(const moe_plan_desc* d) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn get_encode() {
-  static EncodeTiledFn fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                         &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(p);
-  });
-  return fn;
-}
-
-// 2D row-major tensor map: `rows` x `cols` elements, box `box_cols` x `box_rows`,
-// 128-byte swizzle (box_cols * elem == 128).
-bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
-               uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
-  EncodeTiledFn enc = get_encode();
-  if (!enc) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
-  cuuint32_t box[2] = {box_cols, box_rows};
-  cuuint32_t es[2] = {1, 1};
-  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
 
 }  // namespace
 
@@ -229,7 +195,8 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else if (route_large_fits(T, d.num_experts, d.top_k, p->num_sms)) {
     e = timed(p, 0, st, [&] {
-      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
+      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits,
+                                  p->at<uint16_t>(p->L.wt), p->err(), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = timed(p, 8, st, [&] {
@@ -244,7 +211,8 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     e = timed(p, 0, st, [&] {
-      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits, st);
+      return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits,
+                                  p->at<uint16_t>(p->L.wt), p->err(), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = timed(p, 8, st, [&] {

@@ -10,9 +10,50 @@
 // token order, and no result depends on atomic ordering.
 #include <cuda_pipeline.h>
 
+#include <mutex>
+
 #include "moe_common.cuh"
 
 namespace moe {
+
+// ------------------------------------------------------------ tensor maps ---
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+// 2D row-major tensor map: `rows` x `cols` elements, box `box_cols` x `box_rows`,
+// 128-byte swizzle (box_cols * elem == 128).
+bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const void* base,
+               uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * (uint64_t)elem_bytes};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 // ---------------------------------------------------------------------------
 // Router logits: logits[t][e] = sum_h x[t][h] * Wr[h][e] + bias[e], bf16
@@ -333,9 +374,211 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
   rs_logits(x, T, H, bias, E, logits, smem);
 }
 
+// ---------------------------------------------------------------------------
+// Router logits for prefill-sized batches on the tensor cores (tcgen05).
+// logits = x Wr + bias is a plain GEMM whose K (the hidden size) is long next
+// to both T and E, so it belongs on tcgen05 rather than mma.sync, whose rate
+// it otherwise runs at. The B operand must be K-major, so the router weight
+// [H][E] is first transposed into scratch (router_wt_kernel; it reads the
+// weight before waiting for the previous launch and writes after). A CTA
+// computes a 128-token x 64-expert tile: TMA brings 64-wide K chunks of both
+// operands (128-byte swizzle, 6 stages), one thread issues M=128 N=64 K=16
+// MMAs (bf16 in, FP32 accumulation in tensor memory), and four warps add the
+// bias and store the rows. Every wait is bounded: on timeout the error is
+// latched and the CTA stops issuing and exits once its own work is done.
+// ---------------------------------------------------------------------------
+constexpr int kRtM = 128, kRtN = 64, kRtStages = 6;
+constexpr int kRtABytes = kRtM * 128, kRtBBytes = kRtN * 128;   // 64 bf16 of K per row
+constexpr size_t kRtSmem = (size_t)kRtStages * (kRtABytes + kRtBBytes) + 1024;
+
+struct RtParams {
+  CUtensorMap ma;        // x, bf16 [T][H], box 64 x 128 rows
+  CUtensorMap mb;        // transposed weight, bf16 [E][H], box 64 x 64 rows
+  int T, H, E;
+  const float* bias;
+  float* logits;
+  DevErr err;
+};
+
+// wt[e][h] = wr[h][e], 32 x 32 tiles through shared memory.
+__global__ void __launch_bounds__(256) router_wt_kernel(const uint16_t* __restrict__ wr, int H,
+                                                        int E, uint16_t* __restrict__ wt) {
+  __shared__ uint16_t tile[32][34];
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
+  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
+  uint16_t v[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = wr[(size_t)(h0 + ty + 8 * i) * E + e0 + tx];   // weights
+  pdl_begin();   // the scratch may still be read by an earlier launch until now
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tile[ty + 8 * i][tx] = v[i];
+  __syncthreads();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) wt[(size_t)(e0 + ty + 8 * i) * H + h0 + tx] = tile[tx][ty + 8 * i];
+}
+
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+  return (1u << 4)                                 // D format: f32
+         | (1u << 7)                               // A format: bf16
+         | (1u << 10)                              // B format: bf16
+         | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16.
+__device__ __forceinline__ void mma_f16_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__global__ void __launch_bounds__(128) router_logits_tc_kernel(const __grid_constant__ RtParams p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  uint8_t* sa = smem;
+  uint8_t* sb = smem + kRtStages * kRtABytes;
+  __shared__ __align__(8) uint64_t full[kRtStages], empty[kRtStages], acc_full;
+  __shared__ uint32_t tmem_slot;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    tmem_alloc(&tmem_slot, 64);
+    tmem_relinquish();
+  }
+  if (threadIdx.x == 32) {
+    for (int i = 0; i < kRtStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&acc_full, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&p.ma);
+    tma_prefetch_desc(&p.mb);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  pdl_begin();   // x comes from the previous launch
+
+  const int m0 = blockIdx.x * kRtM, n0 = blockIdx.y * kRtN;
+  const int nk = p.H / 64;
+  const unsigned long long lim = p.err.limit_ns;
+  if (warp == 0) {
+    // TMA producer
+    for (int c = 0; c < nk; ++c) {
+      const int s = c % kRtStages;
+      if (c >= kRtStages && !mbar_wait_drain(&empty[s], ((c / kRtStages) & 1) ^ 1, lim)) {
+        if (lane == 0) report_timeout(p.err, 40);
+        break;
+      }
+      if (elect_one_sync()) {
+        mbar_arrive_expect_tx(&full[s], kRtABytes + kRtBBytes);
+        tma_load_2d(sa + s * kRtABytes, &p.ma, 64 * c, m0, &full[s]);
+        tma_load_2d(sb + s * kRtBBytes, &p.mb, 64 * c, n0, &full[s]);
+      }
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // MMA issuer
+    const uint32_t idesc = idesc_bf16_f32(kRtM, kRtN);
+    bool ok = true;
+    for (int c = 0; c < nk; ++c) {
+      const int s = c % kRtStages;
+      if (!mbar_wait_drain(&full[s], (c / kRtStages) & 1, lim)) {
+        if (lane == 0) report_timeout(p.err, 41);
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (elect_one_sync()) {
+        const uint32_t abase = smem_u32(sa + s * kRtABytes), bbase = smem_u32(sb + s * kRtBBytes);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          mma_f16_ss(tmem, smem_desc_sw128(abase + 32 * kk), smem_desc_sw128(bbase + 32 * kk),
+                     idesc, (c | kk) != 0);
+        mma_commit(&empty[s]);
+      }
+      __syncwarp();
+    }
+    if (ok && elect_one_sync()) mma_commit(&acc_full);
+    __syncwarp();
+  }
+  // epilogue: thread = token row of the tile, 64 experts
+  const bool have = mbar_wait_drain(&acc_full, 0, lim);
+  if (!have && lane == 0) report_timeout(p.err, 42);
+  tc_fence_after();
+  uint32_t v0[32], v1[32];
+  const uint32_t taddr = tmem + ((uint32_t)(32 * warp) << 16);
+  tmem_ld_32x32b_x32(taddr, v0);
+  tmem_ld_32x32b_x32(taddr + 32, v1);
+  tmem_wait_ld();
+  const int t = m0 + 32 * warp + lane;
+  if (have && t < p.T) {
+    float4* o = reinterpret_cast<float4*>(p.logits + (size_t)t * p.E + n0);
+    const float4* bb = reinterpret_cast<const float4*>(p.bias + n0);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const uint32_t* v = j < 8 ? v0 : v1;
+      const int q = 4 * (j & 7);
+      float4 r = make_float4(__uint_as_float(v[q]), __uint_as_float(v[q + 1]),
+                             __uint_as_float(v[q + 2]), __uint_as_float(v[q + 3]));
+      if (p.bias) {
+        const float4 b4 = __ldg(bb + j);
+        r.x += b4.x;
+        r.y += b4.y;
+        r.z += b4.z;
+        r.w += b4.w;
+      }
+      o[j] = r;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 64);
+  }
+}
+
+bool router_tc_fits(int T, int H, int E) {
+  return T > kRsMaxT && H % 64 == 0 && H <= 16384 && E % 64 == 0 && E <= 1024;
+}
+
+// Transpose into `wt` and the tcgen05 GEMM.
+cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, const uint16_t* wr,
+                                    const float* bias, int E, float* logits, uint16_t* wt,
+                                    DevErr err, cudaStream_t st) {
+  RtParams p;
+  if (!encode_2d(&p.ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, T, H, 64, kRtM) ||
+      !encode_2d(&p.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wt, E, H, 64, kRtN))
+    return cudaErrorInvalidValue;
+  p.T = T;
+  p.H = H;
+  p.E = E;
+  p.bias = bias;
+  p.logits = logits;
+  p.err = err;
+  cudaError_t e = launch_pdl(router_wt_kernel, dim3(H / 32, E / 32), dim3(256), 0, st, wr, H, E, wt);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)kRtSmem);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(router_logits_tc_kernel, dim3((T + kRtM - 1) / kRtM, E / kRtN), dim3(128),
+                    kRtSmem, st, p);
+}
+
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
-                                 const float* bias, int E, float* logits, cudaStream_t st) {
+                                 const float* bias, int E, float* logits, uint16_t* wt,
+                                 DevErr err, cudaStream_t st) {
   if (!logits) return cudaErrorInvalidValue;
+  // (the tensor-core epilogue moves logits and bias in 16-byte pieces)
+  const bool al16 = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(bias)) & 15u) == 0;
+  if (wt && al16 && router_tc_fits(T, H, E))
+    return launch_router_logits_tc(x, T, H, wr, bias, E, logits, wt, err, st);
   if (T <= kRsMaxT && H % 128 == 0 && rs_smem_bytes(H) <= 227 * 1024) {
     const size_t smem = rs_smem_bytes(H);
     cudaError_t e = cudaFuncSetAttribute(router_logits_small_kernel,
@@ -364,9 +607,9 @@ cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32
 
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
-                               float* topk_w, float* logits, int32_t* blk_cnt,
-                               cudaStream_t st) {
-  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, st);
+                               float* topk_w, float* logits, int32_t* blk_cnt, uint16_t* wt,
+                               DevErr err, cudaStream_t st) {
+  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, wt, err, st);
   if (e != cudaSuccess) return e;
   return launch_router_select(logits, T, E, k, topk_idx, topk_w, blk_cnt, st);
 }

@@ -27,22 +27,38 @@ constexpr int kMaxDevices = 64;
 // the GPU (different streams, no ordering) race on it.
 static __device__ __align__(256) int32_t g_blk_cnt[kMaxBlocks * kMaxExperts];
 
-std::mutex g_mu;
-int32_t* g_blk_cnt_addr[kMaxDevices] = {};
+// The router weight transposed for the tensor-core logits (experts x hidden
+// up to kMaxWt elements; larger shapes take the mma.sync logits), and the
+// error word of its bounded waits (latched, never cleared: a timeout there
+// means the GPU has stopped making progress).
+constexpr size_t kMaxWt = (size_t)2 << 20;
+static __device__ __align__(256) uint16_t g_wt[kMaxWt];
+static __device__ int g_err[2];
 
-// Device address of g_blk_cnt on the current device. In host code the name
-// g_blk_cnt is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and reused.
-moe_status scratch_address(int32_t** out) {
+std::mutex g_mu;
+struct Scratch {
+  int32_t* blk;
+  uint16_t* wt;
+  int* err;
+};
+Scratch g_addr[kMaxDevices] = {};
+
+// Device addresses of the arrays above on the current device. In host code
+// their names are only host-side stand-ins, so the addresses are looked up
+// once per device, with that device current, and reused.
+moe_status scratch_address(Scratch* out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_blk_cnt_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_blk_cnt) != cudaSuccess || !p) return MOE_ERR_CUDA;
-    g_blk_cnt_addr[dev] = static_cast<int32_t*>(p);
+  if (!g_addr[dev].blk) {
+    void *b = nullptr, *w = nullptr, *e = nullptr;
+    if (cudaGetSymbolAddress(&b, g_blk_cnt) != cudaSuccess || !b ||
+        cudaGetSymbolAddress(&w, g_wt) != cudaSuccess || !w ||
+        cudaGetSymbolAddress(&e, g_err) != cudaSuccess || !e)
+      return MOE_ERR_CUDA;
+    g_addr[dev] = Scratch{static_cast<int32_t*>(b), static_cast<uint16_t*>(w), static_cast<int*>(e)};
   }
-  *out = g_blk_cnt_addr[dev];
+  *out = g_addr[dev];
   return MOE_OK;
 }
 
@@ -67,13 +83,17 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
   for (const void* q : need)
     if (!q || !al(q, 8)) return MOE_ERR_INVALID_ARG;
 
-  int32_t* blk = nullptr;
-  moe_status s = scratch_address(&blk);
+  Scratch sc;
+  moe_status s = scratch_address(&sc);
   if (s != MOE_OK) return s;
+  int32_t* blk = sc.blk;
+  uint16_t* wt = (size_t)num_experts * hidden <= kMaxWt ? sc.wt : nullptr;
+  const moe::DevErr err{sc.err, sc.err + 1, 1000000000ull};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int nblk = (T + moe::kRouterTB - 1) / moe::kRouterTB;
   if (moe::launch_router_topk(x, T, hidden, router_w, router_bias, num_experts, top_k,
-                              out->topk_idx, out->topk_w, out->logits, blk, st) != cudaSuccess)
+                              out->topk_idx, out->topk_w, out->logits, blk, wt, err,
+                              st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_route_scan(blk, nblk, T, top_k, num_experts, out->counts, out->offsets,
                              out->tile_offsets, out->block_map, out->num_tiles,
