@@ -33,18 +33,18 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const voi
                uint64_t rows, uint64_t cols, uint32_t box_cols, uint32_t box_rows);
 
 // -------------------------------------------------------------- routing ---
-// Router logits. With `wt` (E*H bf16 of scratch) and router_tc_fits, the
-// tcgen05 path (weight transposed into wt first); else mma.sync paths.
+// Router logits: the tcgen05 path when router_tc_fits (and logits and bias
+// are 16-byte aligned), else the mma.sync paths.
 bool router_tc_fits(int T, int H, int E);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
-                                 const float* bias, int E, float* logits, uint16_t* wt,
-                                 DevErr err, cudaStream_t st);
+                                 const float* bias, int E, float* logits, DevErr err,
+                                 cudaStream_t st);
 cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32_t* topk_idx,
                                  float* topk_w, int32_t* blk_cnt, cudaStream_t st);
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
-                               float* topk_w, float* logits, int32_t* blk_cnt, uint16_t* wt,
-                               DevErr err, cudaStream_t st);
+                               float* topk_w, float* logits, int32_t* blk_cnt, DevErr err,
+                               cudaStream_t st);
 cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E,
                               int32_t* cnt, int32_t* off, int32_t* tile_off, int32_t* bmap,
                               int32_t* num_tiles, cudaStream_t st);

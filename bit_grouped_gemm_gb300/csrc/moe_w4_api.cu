@@ -25,7 +25,7 @@ struct TimedLaunch {
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
-  size_t topk_idx, topk_w, logits, wt, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
+  size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
       err, arrive, xs, act, d, dsh, total;
   int nblk_max, max_tiles, rows_cap;
 };
@@ -45,7 +45,6 @@ Layout make_layout(const moe_plan_desc& d) {
   L.topk_idx = take(Tm * k * 4);
   L.topk_w = take(Tm * k * 4);
   L.logits = take(Tm * E * 4);
-  L.wt = take(E * d.hidden * 2);   // router weight, transposed (tensor-core logits)
   L.blk_cnt = take((size_t)L.nblk_max * E * 4);
   L.cnt8 = take(route_large_cnt8_bytes(L.nblk_max, (int)E));
   L.cnt = take(E * 4);
@@ -196,7 +195,7 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   } else if (route_large_fits(T, d.num_experts, d.top_k, p->num_sms)) {
     e = timed(p, 0, st, [&] {
       return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits,
-                                  p->at<uint16_t>(p->L.wt), p->err(), st);
+                                  p->err(), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = timed(p, 8, st, [&] {
@@ -212,7 +211,7 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   } else {
     e = timed(p, 0, st, [&] {
       return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits,
-                                  p->at<uint16_t>(p->L.wt), p->err(), st);
+                                  p->err(), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     e = timed(p, 8, st, [&] {

@@ -378,11 +378,10 @@ __global__ void __launch_bounds__(256) router_logits_small_kernel(
 // Router logits for prefill-sized batches on the tensor cores (tcgen05).
 // logits = x Wr + bias is a plain GEMM whose K (the hidden size) is long next
 // to both T and E, so it belongs on tcgen05 rather than mma.sync, whose rate
-// it otherwise runs at. The B operand must be K-major, so the router weight
-// [H][E] is first transposed into scratch (router_wt_kernel; it reads the
-// weight before waiting for the previous launch and writes after). A CTA
-// computes a 128-token x 64-expert tile: TMA brings 64-wide K chunks of both
-// operands (128-byte swizzle, 6 stages), one thread issues M=128 N=64 K=16
+// it otherwise runs at. A CTA computes a 128-token x 64-expert tile: TMA
+// brings 64-wide K chunks of x (K-major) and of the router weight in its own
+// [H][E] layout (64 hidden rows x 64 experts, read by the MMA as an N-major
+// operand), 128-byte swizzle, 6 stages; one thread issues M=128 N=64 K=16
 // MMAs (bf16 in, FP32 accumulation in tensor memory), and four warps add the
 // bias and store the rows. Every wait is bounded: on timeout the error is
 // latched and the CTA stops issuing and exits once its own work is done.
@@ -393,36 +392,35 @@ constexpr size_t kRtSmem = (size_t)kRtStages * (kRtABytes + kRtBBytes) + 1024;
 
 struct RtParams {
   CUtensorMap ma;        // x, bf16 [T][H], box 64 x 128 rows
-  CUtensorMap mb;        // transposed weight, bf16 [E][H], box 64 x 64 rows
+  CUtensorMap mb;        // router weight, bf16 [H][E], box 64 experts x 64 rows
   int T, H, E;
   const float* bias;
   float* logits;
   DevErr err;
 };
 
-// wt[e][h] = wr[h][e], 32 x 32 tiles through shared memory.
-__global__ void __launch_bounds__(256) router_wt_kernel(const uint16_t* __restrict__ wr, int H,
-                                                        int E, uint16_t* __restrict__ wt) {
-  __shared__ uint16_t tile[32][34];
-  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
-  const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;
-  uint16_t v[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = wr[(size_t)(h0 + ty + 8 * i) * E + e0 + tx];   // weights
-  pdl_begin();   // the scratch may still be read by an earlier launch until now
-#pragma unroll
-  for (int i = 0; i < 4; ++i) tile[ty + 8 * i][tx] = v[i];
-  __syncthreads();
-#pragma unroll
-  for (int i = 0; i < 4; ++i) wt[(size_t)(e0 + ty + 8 * i) * H + h0 + tx] = tile[tx][ty + 8 * i];
-}
-
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// kind::f16 instruction descriptor: D fp32, A and B bf16, A K-major, B
+// N-major (bit 16): B is read from the router weight's own [H][E] layout.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32_bn(int M, int N) {
   return (1u << 4)                                 // D format: f32
          | (1u << 7)                               // A format: bf16
          | (1u << 10)                              // B format: bf16
+         | (1u << 16)                              // B N-major
          | (static_cast<uint32_t>(N >> 3) << 17)   // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);  // M / 16
+}
+
+// Shared-memory descriptor of an N-major tile with 128-byte swizzle: rows are
+// K (64 N elements = 128 bytes each), 8-row groups 1024 bytes apart; one
+// 64-wide N block per tile.
+__device__ __forceinline__ uint64_t smem_desc_sw128_mn(uint32_t smem_addr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((smem_addr >> 4) & 0x3FFFu);        // start address
+  d |= static_cast<uint64_t>(8192u >> 4) << 16;                   // LBO: next N block (none)
+  d |= static_cast<uint64_t>(1024u >> 4) << 32;                   // SBO: 8 K-rows * 128 B
+  d |= static_cast<uint64_t>(1u) << 46;                           // descriptor version
+  d |= static_cast<uint64_t>(2u) << 61;                           // 128-byte swizzle
+  return d;
 }
 
 // D[tmem] (+)= A[smem desc] * B[smem desc]; kind::f16.
@@ -478,13 +476,13 @@ __global__ void __launch_bounds__(128) router_logits_tc_kernel(const __grid_cons
       if (elect_one_sync()) {
         mbar_arrive_expect_tx(&full[s], kRtABytes + kRtBBytes);
         tma_load_2d(sa + s * kRtABytes, &p.ma, 64 * c, m0, &full[s]);
-        tma_load_2d(sb + s * kRtBBytes, &p.mb, 64 * c, n0, &full[s]);
+        tma_load_2d(sb + s * kRtBBytes, &p.mb, n0, 64 * c, &full[s]);
       }
       __syncwarp();
     }
   } else if (warp == 1) {
     // MMA issuer
-    const uint32_t idesc = idesc_bf16_f32(kRtM, kRtN);
+    const uint32_t idesc = idesc_bf16_f32_bn(kRtM, kRtN);
     bool ok = true;
     for (int c = 0; c < nk; ++c) {
       const int s = c % kRtStages;
@@ -498,7 +496,7 @@ __global__ void __launch_bounds__(128) router_logits_tc_kernel(const __grid_cons
         const uint32_t abase = smem_u32(sa + s * kRtABytes), bbase = smem_u32(sb + s * kRtBBytes);
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          mma_f16_ss(tmem, smem_desc_sw128(abase + 32 * kk), smem_desc_sw128(bbase + 32 * kk),
+          mma_f16_ss(tmem, smem_desc_sw128(abase + 32 * kk), smem_desc_sw128_mn(bbase + 2048 * kk),
                      idesc, (c | kk) != 0);
         mma_commit(&empty[s]);
       }
@@ -548,13 +546,12 @@ bool router_tc_fits(int T, int H, int E) {
   return T > kRsMaxT && H % 64 == 0 && H <= 16384 && E % 64 == 0 && E <= 1024;
 }
 
-// Transpose into `wt` and the tcgen05 GEMM.
 cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, const uint16_t* wr,
-                                    const float* bias, int E, float* logits, uint16_t* wt,
-                                    DevErr err, cudaStream_t st) {
+                                    const float* bias, int E, float* logits, DevErr err,
+                                    cudaStream_t st) {
   RtParams p;
   if (!encode_2d(&p.ma, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, x, T, H, 64, kRtM) ||
-      !encode_2d(&p.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wt, E, H, 64, kRtN))
+      !encode_2d(&p.mb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, wr, H, E, 64, 64))
     return cudaErrorInvalidValue;
   p.T = T;
   p.H = H;
@@ -562,23 +559,21 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, const uint1
   p.bias = bias;
   p.logits = logits;
   p.err = err;
-  cudaError_t e = launch_pdl(router_wt_kernel, dim3(H / 32, E / 32), dim3(256), 0, st, wr, H, E, wt);
-  if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(router_logits_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)kRtSmem);
+  cudaError_t e = cudaFuncSetAttribute(router_logits_tc_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kRtSmem);
   if (e != cudaSuccess) return e;
   return launch_pdl(router_logits_tc_kernel, dim3((T + kRtM - 1) / kRtM, E / kRtN), dim3(128),
                     kRtSmem, st, p);
 }
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
-                                 const float* bias, int E, float* logits, uint16_t* wt,
-                                 DevErr err, cudaStream_t st) {
+                                 const float* bias, int E, float* logits, DevErr err,
+                                 cudaStream_t st) {
   if (!logits) return cudaErrorInvalidValue;
   // (the tensor-core epilogue moves logits and bias in 16-byte pieces)
   const bool al16 = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(bias)) & 15u) == 0;
-  if (wt && al16 && router_tc_fits(T, H, E))
-    return launch_router_logits_tc(x, T, H, wr, bias, E, logits, wt, err, st);
+  if (al16 && router_tc_fits(T, H, E))
+    return launch_router_logits_tc(x, T, H, wr, bias, E, logits, err, st);
   if (T <= kRsMaxT && H % 128 == 0 && rs_smem_bytes(H) <= 227 * 1024) {
     const size_t smem = rs_smem_bytes(H);
     cudaError_t e = cudaFuncSetAttribute(router_logits_small_kernel,
@@ -607,9 +602,9 @@ cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32
 
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
-                               float* topk_w, float* logits, int32_t* blk_cnt, uint16_t* wt,
-                               DevErr err, cudaStream_t st) {
-  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, wt, err, st);
+                               float* topk_w, float* logits, int32_t* blk_cnt, DevErr err,
+                               cudaStream_t st) {
+  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, err, st);
   if (e != cudaSuccess) return e;
   return launch_router_select(logits, T, E, k, topk_idx, topk_w, blk_cnt, st);
 }

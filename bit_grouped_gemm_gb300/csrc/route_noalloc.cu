@@ -27,18 +27,13 @@ constexpr int kMaxDevices = 64;
 // the GPU (different streams, no ordering) race on it.
 static __device__ __align__(256) int32_t g_blk_cnt[kMaxBlocks * kMaxExperts];
 
-// The router weight transposed for the tensor-core logits (experts x hidden
-// up to kMaxWt elements; larger shapes take the mma.sync logits), and the
-// error word of its bounded waits (latched, never cleared: a timeout there
-// means the GPU has stopped making progress).
-constexpr size_t kMaxWt = (size_t)2 << 20;
-static __device__ __align__(256) uint16_t g_wt[kMaxWt];
+// The error word of the tensor-core logits' bounded waits (latched, never
+// cleared: a timeout there means the GPU has stopped making progress).
 static __device__ int g_err[2];
 
 std::mutex g_mu;
 struct Scratch {
   int32_t* blk;
-  uint16_t* wt;
   int* err;
 };
 Scratch g_addr[kMaxDevices] = {};
@@ -51,12 +46,11 @@ moe_status scratch_address(Scratch* out) {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
   if (!g_addr[dev].blk) {
-    void *b = nullptr, *w = nullptr, *e = nullptr;
+    void *b = nullptr, *e = nullptr;
     if (cudaGetSymbolAddress(&b, g_blk_cnt) != cudaSuccess || !b ||
-        cudaGetSymbolAddress(&w, g_wt) != cudaSuccess || !w ||
         cudaGetSymbolAddress(&e, g_err) != cudaSuccess || !e)
       return MOE_ERR_CUDA;
-    g_addr[dev] = Scratch{static_cast<int32_t*>(b), static_cast<uint16_t*>(w), static_cast<int*>(e)};
+    g_addr[dev] = Scratch{static_cast<int32_t*>(b), static_cast<int*>(e)};
   }
   *out = g_addr[dev];
   return MOE_OK;
@@ -87,12 +81,11 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
   moe_status s = scratch_address(&sc);
   if (s != MOE_OK) return s;
   int32_t* blk = sc.blk;
-  uint16_t* wt = (size_t)num_experts * hidden <= kMaxWt ? sc.wt : nullptr;
   const moe::DevErr err{sc.err, sc.err + 1, 1000000000ull};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int nblk = (T + moe::kRouterTB - 1) / moe::kRouterTB;
   if (moe::launch_router_topk(x, T, hidden, router_w, router_bias, num_experts, top_k,
-                              out->topk_idx, out->topk_w, out->logits, blk, wt, err,
+                              out->topk_idx, out->topk_w, out->logits, blk, err,
                               st) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_route_scan(blk, nblk, T, top_k, num_experts, out->counts, out->offsets,
