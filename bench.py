@@ -22,6 +22,10 @@ pool of 64 pre-generated device batches and replays the 40-layer step from
 a CUDA graph; the roofline is HBM bandwidth over the packed bytes of the
 experts each layer's routing selects (counted from the routing itself).
 
+--tokens N --chunk C: a prompt of N tokens through the stack in chunks of at
+most C tokens (the plan's capacity; moe_forward_stack runs each chunk through
+all layers), e.g. the long-prompt sweep of the chunked-prefill summary.
+
 --impl reference times the oracle (the CPU reference of this build) on the
 same workload, a bounded sample per step.
 Multi-GPU: independent replicas (the block does not shard), one per rank.
@@ -57,6 +61,11 @@ def parse_args(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--workload", default="prefill_t4096_l40_zipf")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the prompt length of a prefill workload")
+    ap.add_argument("--chunk", type=int, default=0,
+                    help="chunked prefill: plan capacity (tokens per chunk); default: the "
+                         "whole prompt in one chunk")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args(argv)
@@ -212,6 +221,9 @@ def workload(args):
     w = synth.standard_workloads()[args.workload]
     if args.layers:
         w = dataclasses.replace(w, layers=args.layers)
+    if args.tokens and w.tokens > 16:
+        w = dataclasses.replace(w, tokens=args.tokens,
+                                name=w.name.replace(f"t{w.tokens}_", f"t{args.tokens}_"))
     return w
 
 
@@ -245,17 +257,20 @@ def main(argv=None):
     layers = stack.make_layers(w, "cuda")
     weight_bytes = sum(L.nbytes() for L in layers)
     alpha = stack.residual_alpha(w.layers)
+    chunk = min(T, args.chunk) if args.chunk > 0 else T
     plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
-                                           sh.group_size, int(sh.has_shared), T), local)
+                                           sh.group_size, int(sh.has_shared), chunk), local)
     stream = torch.cuda.current_stream()
     x0 = synth.tokens_x(w, "cuda")
     x = x0.clone()
-    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
-    xn = torch.empty_like(x)
+    xn = torch.empty((chunk, sh.hidden), dtype=x.dtype, device="cuda")
+    layer_arr = bg.moe_layers(layers)
 
+    # one step: the whole stack through the native driver (chunks of `chunk`
+    # tokens, each through all layers)
     def step():
         x.copy_(x0)
-        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        bg.moe_forward_stack(plan, x, xn, T, layer_arr, alpha)
 
     for _ in range(max(args.warmup, 0)):
         step()
@@ -301,7 +316,7 @@ def main(argv=None):
 
         def e2e_step():
             x.copy_(xh, non_blocking=True)
-            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            bg.moe_forward_stack(plan, x, xn, T, layer_arr, alpha)
             out_h.copy_(x, non_blocking=True)
         for _ in range(2):
             e2e_step()
@@ -322,8 +337,9 @@ def main(argv=None):
     # --- roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU)
     peaks, peak_src = load_peaks()
     n_pairs = T * (sh.top_k + int(sh.has_shared))
-    flops_gateup = 4.0 * sh.hidden * sh.inter * n_pairs        # per launch (one layer)
     gu_ms, gu_n = kt["gate_up_gemm"]
+    # per launch: one layer of one chunk (the average over the step's launches)
+    flops_gateup = 4.0 * sh.hidden * sh.inter * n_pairs * w.layers * args.steps / max(gu_n, 1)
     achieved = flops_gateup / (gu_ms / gu_n / 1e3) / 1e12 if gu_n else None
     peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
@@ -357,6 +373,7 @@ def main(argv=None):
                    "inter": sh.inter, "experts": sh.num_experts, "top_k": sh.top_k,
                    "shared_experts": int(sh.has_shared), "group_size": sh.group_size,
                    "routing": w.routing + (f"(s={w.zipf_s})" if w.routing == "zipf" else ""),
+                   "chunk": chunk,
                    "weights_gb": round(weight_bytes / 1e9, 2),
                    "l2": "inputs larger than L2: every step streams the packed weights "
                          f"({weight_bytes / 1e9:.1f} GB) from HBM",

@@ -47,6 +47,11 @@ class MoeExperts(ctypes.Structure):
     _fields_ = [("gate", MoeW4), ("up", MoeW4), ("down", MoeW4)]
 
 
+class MoeLayer(ctypes.Structure):
+    _fields_ = [("router_w", ctypes.c_void_p), ("router_bias", ctypes.c_void_p),
+                ("routed", MoeExperts), ("shared", MoeExperts)]
+
+
 class MoeRouting(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("topk_idx", "topk_w", "counts", "offsets", "tile_offsets", "perm", "inv",
@@ -84,6 +89,7 @@ def load_library(path: Optional[str] = None):
         "moe_forward_layer_residual": (S, [P, P, I, P, P, ctypes.POINTER(MoeExperts),
                                            ctypes.POINTER(MoeExperts), ctypes.c_float, P, P, P]),
         "moe_residual_add": (S, [P, P, P, I, ctypes.c_float, P, P, P]),
+        "moe_forward_stack": (S, [P, P, P, I, ctypes.POINTER(MoeLayer), I, ctypes.c_float, P]),
         "moe_get_error": (S, [P]),
         "moe_debug_wait_timeout": (S, [P, I, P]),
         "moe_enable_timing": (S, [P, I]),
@@ -186,6 +192,25 @@ def moe_forward_layer_residual(plan: int, xn, T: int, router_w, router_bias, rou
         plan, _ptr(xn), T, _ptr(router_w), _ptr(router_bias), ctypes.byref(routed),
         ctypes.byref(shared) if shared is not None else None, float(alpha), _ptr(x),
         _ptr(xn_out), _stream(stream)), "moe_forward_layer_residual")
+
+
+def moe_layers(layers) -> ctypes.Array:
+    """A ctypes array of MoeLayer from objects with router_w, router_bias,
+    routed_c and shared_c (the tensors must outlive its use)."""
+    arr = (MoeLayer * len(layers))()
+    for i, L in enumerate(layers):
+        arr[i].router_w = _ptr(L.router_w)
+        arr[i].router_bias = _ptr(L.router_bias)
+        arr[i].routed = L.routed_c
+        if L.shared_c is not None:
+            arr[i].shared = L.shared_c
+    return arr
+
+
+def moe_forward_stack(plan: int, x, xn, T: int, layers: ctypes.Array, alpha: float,
+                      stream=None) -> None:
+    _check(load_library().moe_forward_stack(plan, _ptr(x), _ptr(xn), T, layers, len(layers),
+                                            float(alpha), _stream(stream)), "moe_forward_stack")
 
 
 def moe_route_noalloc(x, T: int, hidden: int, router_w, router_bias, num_experts: int,

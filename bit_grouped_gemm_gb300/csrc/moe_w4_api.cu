@@ -554,6 +554,38 @@ moe_status moe_forward_layer_residual(moe_plan_t p, const uint16_t* xn, int T,
   return ffn_impl(p, xn, T, &r, routed, shared, nullptr, &res, st);
 }
 
+moe_status moe_forward_stack(moe_plan_t p, uint16_t* x, uint16_t* xn, int T,
+                             const moe_layer* layers, int num_layers, float alpha,
+                             moe_stream_t stream) {
+  if (!p || !x || !xn || !layers || num_layers < 1 || T < 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(xn) || x == xn) return MOE_ERR_INVALID_ARG;
+  const int H = p->d.hidden, chunk = p->d.max_tokens;
+  // the stream and xn must not overlap (xn holds one chunk)
+  const uint8_t *xb = reinterpret_cast<const uint8_t*>(x), *nb = reinterpret_cast<const uint8_t*>(xn);
+  const size_t xbytes = (size_t)T * H * 2, nbytes = (size_t)(T < chunk ? T : chunk) * H * 2;
+  if (xb < nb + nbytes && nb < xb + xbytes) return MOE_ERR_INVALID_ARG;
+  moe_status s;
+  for (int l = 0; l < num_layers; ++l) {
+    const moe_layer& L = layers[l];
+    if (!L.router_w || !aligned16(L.router_w)) return MOE_ERR_INVALID_ARG;
+    if (L.router_bias && (reinterpret_cast<uintptr_t>(L.router_bias) & 3u)) return MOE_ERR_INVALID_ARG;
+    if ((s = check_experts(&L.routed)) != MOE_OK) return s;
+    if (p->d.has_shared && (s = check_experts(&L.shared)) != MOE_OK) return s;
+  }
+  for (int c0 = 0; c0 < T; c0 += chunk) {
+    const int Tc = T - c0 < chunk ? T - c0 : chunk;
+    uint16_t* xc = x + (size_t)c0 * H;
+    if ((s = moe_residual_add(p, xc, nullptr, Tc, 0.f, xc, xn, stream)) != MOE_OK) return s;
+    for (int l = 0; l < num_layers; ++l) {
+      const moe_layer& L = layers[l];
+      s = moe_forward_layer_residual(p, xn, Tc, L.router_w, L.router_bias, &L.routed,
+                                     p->d.has_shared ? &L.shared : nullptr, alpha, xc, xn, stream);
+      if (s != MOE_OK) return s;
+    }
+  }
+  return MOE_OK;
+}
+
 moe_status moe_residual_add(moe_plan_t p, const uint16_t* x, const float* y, int T,
                             float alpha, uint16_t* x_out, uint16_t* xn_out, moe_stream_t stream) {
   if (!p || !x) return MOE_ERR_INVALID_ARG;

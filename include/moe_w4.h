@@ -173,6 +173,32 @@ moe_status moe_forward_layer_residual(moe_plan_t plan, const uint16_t* xn, int T
                                       float alpha, uint16_t* x, uint16_t* xn_out,
                                       moe_stream_t stream);
 
+/* One layer of a stack for moe_forward_stack: its router and experts.
+ * shared is ignored (may be NULL) when the plan has no shared expert. */
+typedef struct {
+  const uint16_t* router_w;     /* bf16 [H][E] */
+  const float* router_bias;     /* f32 [E] or NULL */
+  moe_experts routed;
+  moe_experts shared;
+} moe_layer;
+
+/* A stack of MoE layers on a prompt of any length (chunked prefill; the
+ * pages' engine prefills long prompts in chunks, "Las optimizaciones en el
+ * prefill"). x is the residual stream, bf16 [T][H], updated in place:
+ *   xn = bf16(rmsnorm(x));
+ *   for each layer: x = bf16(x + alpha * moe_layer(xn)); xn = bf16(rmsnorm(x))
+ * T may exceed the plan's max_tokens: the tokens go through all layers in
+ * chunks of at most max_tokens rows, one chunk after the other (the block
+ * treats every token on its own, so each chunk's result is the one of the
+ * whole prompt). xn is caller scratch, bf16 [min(T, max_tokens)][H], and holds
+ * the last chunk's normalised stream on return. Every layer of a chunk is one
+ * moe_forward_layer_residual; stream-ordered, no host sync. Errors: as for
+ * the per-layer calls (checked for every layer before any launch);
+ * MOE_ERR_INVALID_ARG for num_layers < 1 or a NULL layers array. */
+moe_status moe_forward_stack(moe_plan_t plan, uint16_t* x, uint16_t* xn, int T,
+                             const moe_layer* layers, int num_layers, float alpha,
+                             moe_stream_t stream);
+
 /* Update between stacked layers (not part of the expert block itself):
  *   x_out[t] = bf16(x[t] + alpha * y[t])                 (skipped if y == NULL)
  *   xn_out[t] = bf16(x_out[t] / sqrt(mean_h x_out[t][h]^2 + 1e-6))

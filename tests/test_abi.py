@@ -44,6 +44,7 @@ def test_struct_layouts_match_header():
     assert ctypes.sizeof(bg.MoeW4) == 3 * 8
     assert ctypes.sizeof(bg.MoeExperts) == 9 * 8
     assert ctypes.sizeof(bg.MoeRouting) == 10 * 8
+    assert ctypes.sizeof(bg.MoeLayer) == 2 * 8 + 2 * 9 * 8
 
 
 def test_version_and_strings(lib):
@@ -82,4 +83,5 @@ def test_null_arguments_rejected(lib):
     assert lib.moe_forward_layer(None, None, 1, None, None, None, None, None, None) == 1
     assert lib.moe_forward_layer_residual(None, None, 1, None, None, None, None, 0.0, None, None,
                                           None) == 1
+    assert lib.moe_forward_stack(None, None, None, 1, None, 1, 0.0, None) == 1
     assert lib.moe_get_error(None) == 1

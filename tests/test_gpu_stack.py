@@ -164,3 +164,65 @@ def test_fused_layer_update_bit_identical(T):
             assert ei.value.status == 1
     finally:
         bg.moe_plan_destroy(plan)
+
+
+def _stack_bits(plan, w, layers, T, driver, x0):
+    x, xn = x0.clone(), torch.empty_like(x0)
+    alpha = stack.residual_alpha(40)
+    if driver:
+        arr = bg.moe_layers(layers)
+        bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
+    else:
+        y = torch.empty(x0.shape, dtype=torch.float32, device="cuda")
+        stack.run_stack(plan, x, xn, layers, T, y, alpha, fused=True)
+    torch.cuda.synchronize()
+    assert bg.moe_get_error(plan) == 0
+    return x.view(torch.int16).cpu().numpy()
+
+
+def test_stack_driver_matches_layer_calls():
+    """moe_forward_stack (the native layer loop) gives the bits of the
+    per-layer calls, here for one chunk (T <= max_tokens), 3 layers."""
+    T = 512
+    w = dataclasses.replace(synth.standard_workloads()["prefill_t4096_l40_zipf"], tokens=T, layers=3)
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
+    try:
+        x0 = synth.tokens_x(w, "cuda")
+        a = _stack_bits(plan, w, layers, T, True, x0)
+        b = _stack_bits(plan, w, layers, T, False, x0)
+        assert np.array_equal(a, b)
+        # argument errors: no layers, xn overlapping x (status 1)
+        x, xn = x0.clone(), torch.empty_like(x0)
+        arr = bg.moe_layers(layers)
+        assert bg.load_library().moe_forward_stack(plan, x.data_ptr(), xn.data_ptr(), T, arr, 0,
+                                                   0.1, None) == 1
+        assert bg.load_library().moe_forward_stack(plan, x.data_ptr(), x[1:].data_ptr(), T, arr,
+                                                   3, 0.1, None) == 1
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("chunk", [256, 224])
+def test_chunked_prefill_matches_one_pass(chunk):
+    """A 600-token prompt through 3 layers in chunks of `chunk` rows (the
+    plan's capacity; ragged last chunk) gives the bits of one 600-token pass:
+    the block treats every token on its own, and every chunk here takes the
+    tensor-core path like the whole prompt."""
+    T = 600
+    w = dataclasses.replace(synth.standard_workloads()["prefill_t4096_l40_zipf"], tokens=T, layers=3)
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    mk = lambda m: bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                                   sh.group_size, int(sh.has_shared), m), 0)
+    whole, chunked = mk(T), mk(chunk)
+    try:
+        x0 = synth.tokens_x(w, "cuda")
+        a = _stack_bits(whole, w, layers, T, True, x0)
+        b = _stack_bits(chunked, w, layers, T, True, x0)
+        assert np.array_equal(a, b)
+    finally:
+        bg.moe_plan_destroy(whole)
+        bg.moe_plan_destroy(chunked)
