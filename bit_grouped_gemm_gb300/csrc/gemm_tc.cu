@@ -26,8 +26,9 @@
 //     gathered, and fp16's 11-bit significand keeps the rounding of the
 //     dequantised weights and SwiGLU activations 8x below bf16's;
 //   * one thread issues tcgen05.mma (M=128, K=16, fp16 in, fp32 in TMEM) for
-//     both weight blocks; 4 epilogue warps read the accumulators back with
-//     tcgen05.ld and apply SwiGLU (gate/up) or the top-k weight (down);
+//     both weight blocks; 8 epilogue warps, two per TMEM lane quarter taking
+//     alternate 32-token groups, read the accumulators back with tcgen05.ld
+//     and apply SwiGLU (gate/up) or the top-k weight (down);
 //   * persistent CTAs (one per SM, 512 TMEM columns each) walk the units;
 //     the number of units is read from device memory, never from the host.
 // Every wait is bounded: on timeout the CTA latches an error, drains its own
@@ -37,7 +38,7 @@
 namespace moe {
 namespace tc {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;             // 20 warps
 constexpr int kBStages = 6;               // activation chunks (64 K) in flight
 constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
 constexpr int kAStages = 4;               // TMEM weight stages (64 K)
@@ -46,9 +47,9 @@ constexpr int kQTileBytes = 128 * 128;    // 128 weight rows x 32 words
 constexpr int kQStageBytes = 2 * kQTileBytes;
 constexpr int kOffB = 0;
 constexpr int kOffQ = kOffB + kBStages * kBTileBytes;
-constexpr int kOffW = kOffQ + kQStages * kQStageBytes;   // epilogue row weights [4][128]
-constexpr int kOffX = kOffW + 4 * 128 * 4;               // epilogue transpose [4][32 x 32 fp16]
-constexpr int kOffBar = kOffX + 4 * 2048;
+constexpr int kOffW = kOffQ + kQStages * kQStageBytes;   // epilogue row weights [8][128]
+constexpr int kOffX = kOffW + 8 * 128 * 4;               // epilogue transpose [8][32 x 32 fp16]
+constexpr int kOffBar = kOffX + 8 * 2048;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // barriers + alignment slack
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kAccCol0 = 0, kAccCol1 = 128, kAStageCol = 256;
@@ -179,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       mbar_init(&a_full[i], 9);   // 8 dequant warps + the activation forwarder
     }
     mbar_init(acc_full, 1);
-    mbar_init(acc_empty, 4);
+    mbar_init(acc_empty, 8);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -454,10 +455,13 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     }
   } else if (warp >= 12) {
     // ------------------------------------------------------ epilogue warps
-    const int quarter = warp & 3;
+    // Two warps per TMEM lane quarter take alternate 32-token groups, so the
+    // accumulators are read out (and released to the next unit) twice as
+    // fast as with one.
+    const int quarter = warp & 3, part = (warp - 12) >> 2;
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
-    float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * quarter;   // this warp's copy
-    uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + kOffX) + 1024 * quarter;  // 32 x 32 fp16
+    float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * (warp - 12);   // this warp's copy
+    uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + kOffX) + 1024 * (warp - 12);  // 32 x 32 fp16
     uint32_t it = 0;
     bool ok = true;
     UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
@@ -475,13 +479,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       }
       if (!(ok = warp_wait(acc_full, it & 1, abort_flag, p.err, 8, 32 * p.mode))) break;
       tc_fence_after();
-      for (int c0 = 0; c0 < U.rows; c0 += 32) {
+      if (32 * part >= U.rows) {
+        // no group for this warp in this unit
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_relaxed(acc_empty);
+      }
+      for (int c0 = 32 * part; c0 < U.rows; c0 += 64) {
         uint32_t v0[32], v1[32];
         tmem_ld_32x32b_x32(tmem + lane_base + kAccCol0 + c0, v0);
         tmem_ld_32x32b_x32(tmem + lane_base + kAccCol1 + c0, v1);
         tmem_wait_ld();
-        if (c0 + 32 >= U.rows) {
-          // accumulators fully read: let the next unit's MMAs start now
+        if (c0 + 64 >= U.rows) {
+          // this warp's accumulators fully read: let the next unit's MMAs start
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive_relaxed(acc_empty);
