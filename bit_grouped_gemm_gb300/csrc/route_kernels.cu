@@ -713,22 +713,27 @@ cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E, i
 // ---------------------------------------------------------------------------
 // Stable scatter: slot s = t*k + j of block b goes to
 //   pos = blk_off[b][e] + #{t' < t in block b : token t' selected e}
+// A token's k experts are distinct, so the count is the popcount of the
+// block's per-expert token mask below bit t (blocks hold at most 32 tokens).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) route_scatter_kernel(
     const int32_t* __restrict__ topk_idx, const int32_t* __restrict__ blk_off, int T, int k,
     int E, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
   pdl_begin();
   __shared__ int idx_s[kRouterTB * 32];
+  __shared__ unsigned mask_s[1024];
   const int t0 = blockIdx.x * kRouterTB;
   const int nt = min(kRouterTB, T - t0);
   const int nslots = nt * k;
+  for (int i = threadIdx.x; i < E; i += blockDim.x) mask_s[i] = 0u;
   for (int i = threadIdx.x; i < nslots; i += blockDim.x) idx_s[i] = topk_idx[(size_t)t0 * k + i];
+  __syncthreads();
+  for (int i = threadIdx.x; i < nslots; i += blockDim.x) atomicOr(&mask_s[idx_s[i]], 1u << (i / k));
   __syncthreads();
   for (int i = threadIdx.x; i < nslots; i += blockDim.x) {
     const int tl = i / k;
     const int e = idx_s[i];
-    int rank = 0;
-    for (int s = 0; s < tl * k; ++s) rank += (idx_s[s] == e);
+    const int rank = __popc(mask_s[e] & ((1u << tl) - 1u));
     const int pos = blk_off[(size_t)blockIdx.x * E + e] + rank;
     const int slot = t0 * k + i;
     perm[pos] = slot;
@@ -766,6 +771,7 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ int idx_s[kRsMaxT * 32];
   __shared__ int cnt_s[512], off_s[512];
+  __shared__ unsigned mask_s[512];   // per expert: the tokens that selected it
   __shared__ int warp_sums[32];
   __shared__ int tot_rows, tot_tiles, is_last;
   rs_load_w(wr, H, E, smem);   // weights: written by no launch of this library
@@ -780,7 +786,10 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
   __threadfence();   // the other CTAs' logits, after their arrivals
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) *arrive = 0u;
-  for (int e = tid; e < E; e += kRsThreads) cnt_s[e] = 0;
+  for (int e = tid; e < E; e += kRsThreads) {
+    cnt_s[e] = 0;
+    mask_s[e] = 0u;
+  }
   __syncthreads();
 
   // top-k, one warp per token
@@ -793,6 +802,7 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
       topk_w[t * k + lane] = w;
       idx_s[t * k + lane] = idx;
       atomicAdd(&cnt_s[idx], 1);
+      atomicOr(&mask_s[idx], 1u << t);
     }
   }
   __syncthreads();
@@ -829,12 +839,12 @@ __global__ void __launch_bounds__(kRsThreads) route_small_kernel(
   }
   __syncthreads();
 
-  // stable scatter: rank = earlier tokens that selected the same expert
+  // stable scatter: rank = earlier tokens that selected the same expert (a
+  // token's k experts are distinct, so the token mask's popcount below t)
   for (int i = tid; i < T * k; i += kRsThreads) {
     const int e = idx_s[i];
     const int tl = i / k;
-    int rank = 0;
-    for (int s = 0; s < tl * k; ++s) rank += (idx_s[s] == e);
+    const int rank = __popc(mask_s[e] & ((1u << tl) - 1u));
     const int pos = off_s[e] + rank;
     perm[pos] = i;
     inv[i] = pos;
@@ -907,13 +917,17 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
   __shared__ int cnt_s[512];
   __shared__ int part_s[1024], pre_s[1024];   // per-(range, expert): block sums, sums before b
   __shared__ int boff_s[512];                 // this block's first position per expert
+  __shared__ unsigned mask_s[512];            // per expert: the block's tokens that selected it
   __shared__ int wrows_s[16], wtiles_s[16];
   __shared__ int go;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nblk = gridDim.x, b = blockIdx.x;
   const int t0 = b * kRouterTB;
   const int nt = min(kRouterTB, T - t0);
-  for (int i = tid; i < E; i += kRlThreads) cnt_s[i] = 0;
+  for (int i = tid; i < E; i += kRlThreads) {
+    cnt_s[i] = 0;
+    mask_s[i] = 0u;
+  }
   __syncthreads();
 
   // ---- top-k and this block's counts
@@ -927,6 +941,7 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
       topk_w[(size_t)t * k + lane] = w;
       idx_s[warp * k + lane] = idx;
       atomicAdd(&cnt_s[idx], 1);
+      atomicOr(&mask_s[idx], 1u << warp);
     }
   }
   __syncthreads();
@@ -1049,13 +1064,13 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
   }
   __syncthreads();
 
-  // ---- stable scatter of this block's slots
+  // ---- stable scatter of this block's slots (rank: earlier tokens of the
+  // block that selected the expert; a token's experts are distinct)
   const int nslots = nt * k;
   for (int i = tid; i < nslots; i += kRlThreads) {
     const int tl = i / k;
     const int ex = idx_s[i];
-    int rank = 0;
-    for (int s2 = 0; s2 < tl * k; ++s2) rank += (idx_s[s2] == ex);
+    const int rank = __popc(mask_s[ex] & ((1u << tl) - 1u));
     const int pos = boff_s[ex] + rank;
     const int slot = t0 * k + i;
     perm[pos] = slot;
