@@ -64,14 +64,16 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
 // launch_route_scan + launch_route_scatter). `arrive` is 0 between launches;
 // `gen` is a generation word the launch advances. route_large_fits tells
 // whether the blocks can all be resident.
-// `cnt8` holds route_large_cnt8_bytes(blocks, E) bytes of scratch.
+// `cnt8` holds route_large_cnt8_bytes(blocks, E) bytes of scratch. When `xs`
+// is set, the launch also does launch_gather_rows' work (x: bf16 [T][H]).
 bool route_large_fits(int T, int E, int k, int num_sms);
 size_t route_large_cnt8_bytes(int nblk, int E);
 cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t* topk_idx,
                                float* topk_w, uint8_t* cnt8, int32_t* cnt, int32_t* off,
                                int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
                                int32_t* perm, int32_t* inv, unsigned* arrive, unsigned* gen,
-                               DevErr err, cudaStream_t st);
+                               DevErr err, const uint16_t* x, uint16_t* xs, int H,
+                               int with_shared, cudaStream_t st);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
                                int with_shared, uint16_t* xs, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,

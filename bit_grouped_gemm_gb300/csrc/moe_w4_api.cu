@@ -175,10 +175,21 @@ moe_status check_experts(const moe_experts* x) {
 
 W4Dev dev(const moe_w4& m) { return W4Dev{m.qweight, m.scales, m.biases}; }
 
+// GEMM path the feed-forward part of a T-token call takes.
+int ffn_path(const moe_plan* p, int T) {
+  const moe_plan_desc& d = p->d;
+  const int small_max = d.small_m_max_tokens > 0 ? d.small_m_max_tokens : 16;
+  return d.gemm_path != 0 ? d.gemm_path : (T <= small_max && smallm_fits(d.hidden, d.inter) ? 2 : 1);
+}
+
+// Routing. With `fuse_gather`, a routing launch that can also does the
+// gather of the tensor-core path (x rows into the plan's xs) and sets
+// *gathered; otherwise *gathered is false.
 moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* router_w,
                       const float* router_bias, moe_routing* out, bool want_logits,
-                      cudaStream_t st) {
+                      cudaStream_t st, bool fuse_gather = false, bool* gathered = nullptr) {
   const moe_plan_desc& d = p->d;
+  if (gathered) *gathered = false;
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   float* logits = p->at<float>(p->L.logits);   // the top-k kernel reads them back
   cudaError_t e;
@@ -205,9 +216,12 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
                                 p->at<int32_t>(p->L.cnt), p->at<int32_t>(p->L.off),
                                 p->at<int32_t>(p->L.tile_off), p->at<int32_t>(p->L.bmap),
                                 p->at<int32_t>(p->L.num_tiles), p->at<int32_t>(p->L.perm),
-                                p->at<int32_t>(p->L.inv), w, w + 1, p->err(), st);
+                                p->at<int32_t>(p->L.inv), w, w + 1, p->err(), x,
+                                fuse_gather ? p->at<uint16_t>(p->L.xs) : nullptr, d.hidden,
+                                d.has_shared, st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (gathered) *gathered = fuse_gather;
   } else {
     e = timed(p, 0, st, [&] {
       return launch_router_logits(x, T, d.hidden, router_w, router_bias, d.num_experts, logits,
@@ -256,21 +270,20 @@ struct ResidualUpdate {
 };
 
 // Exactly one of y (the block output) and res (the fused stack update) is set.
+// `pre_gathered`: the routing launch already wrote the gathered rows.
 moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
                     const moe_experts* routed, const moe_experts* shared, float* y,
-                    const ResidualUpdate* res, cudaStream_t st) {
+                    const ResidualUpdate* res, cudaStream_t st, bool pre_gathered = false) {
   const moe_plan_desc& d = p->d;
   const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
   const int hs = d.has_shared;
-  const int small_max = d.small_m_max_tokens > 0 ? d.small_m_max_tokens : 16;
-  const int path =
-      d.gemm_path != 0 ? d.gemm_path : (T <= small_max && smallm_fits(H, I) ? 2 : 1);
+  const int path = ffn_path(p, T);
   p->last_path = path;
 
   // the tensor-core path reads gathered rows with TMA; the small-M path reads
   // the token rows itself
   cudaError_t e = cudaSuccess;
-  if (path == 1) {
+  if (path == 1 && !pre_gathered) {
     e = timed(p, 3, st, [&] {
       return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), st);
     });
@@ -525,9 +538,10 @@ moe_status moe_forward_layer(moe_plan_t p, const uint16_t* x, int T, const uint1
   if (s != MOE_OK) return s;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   moe_routing r;
-  s = route_impl(p, x, T, router_w, router_bias, &r, false, st);
+  bool gathered = false;
+  s = route_impl(p, x, T, router_w, router_bias, &r, false, st, ffn_path(p, T) == 1, &gathered);
   if (s != MOE_OK) return s;
-  return ffn_impl(p, x, T, &r, routed, shared, y, nullptr, st);
+  return ffn_impl(p, x, T, &r, routed, shared, y, nullptr, st, gathered);
 }
 
 moe_status moe_forward_layer_residual(moe_plan_t p, const uint16_t* xn, int T,
@@ -548,10 +562,11 @@ moe_status moe_forward_layer_residual(moe_plan_t p, const uint16_t* xn, int T,
   }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   moe_routing r;
-  s = route_impl(p, xn, T, router_w, router_bias, &r, false, st);
+  bool gathered = false;
+  s = route_impl(p, xn, T, router_w, router_bias, &r, false, st, ffn_path(p, T) == 1, &gathered);
   if (s != MOE_OK) return s;
   const ResidualUpdate res{alpha, x, xn_out};
-  return ffn_impl(p, xn, T, &r, routed, shared, nullptr, &res, st);
+  return ffn_impl(p, xn, T, &r, routed, shared, nullptr, &res, st, gathered);
 }
 
 moe_status moe_forward_stack(moe_plan_t p, uint16_t* x, uint16_t* xn, int T,

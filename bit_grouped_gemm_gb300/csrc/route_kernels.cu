@@ -911,9 +911,11 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
     float* __restrict__ topk_w, uint8_t* cnt8, int np, int32_t* __restrict__ cnt,
     int32_t* __restrict__ off, int32_t* __restrict__ tile_off, int32_t* __restrict__ bmap,
     int32_t* __restrict__ num_tiles, int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-    unsigned* arrive, unsigned* gen, DevErr err) {
+    unsigned* arrive, unsigned* gen, DevErr err, const uint16_t* __restrict__ x,
+    uint16_t* __restrict__ xs, int H, int with_shared) {
   pdl_begin();
   __shared__ int idx_s[kRouterTB * 32];
+  __shared__ int pos_s[kRouterTB * 32];       // position of each of the block's slots
   __shared__ int cnt_s[512];
   __shared__ int part_s[1024], pre_s[1024];   // per-(range, expert): block sums, sums before b
   __shared__ int boff_s[512];                 // this block's first position per expert
@@ -1075,6 +1077,25 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
     const int slot = t0 * k + i;
     perm[pos] = slot;
     inv[slot] = pos;
+    pos_s[i] = pos;
+  }
+  if (!xs) return;
+
+  // ---- gather (the work of gather_rows_kernel, fused): one warp per token
+  // of the block reads its row once and writes it, as fp16 in perm8 order, to
+  // its k routed positions and its shared-expert row.
+  __syncthreads();
+  if (warp < nt) {
+    const int t = t0 + warp;
+    const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    for (int v = lane; v < H / 8; v += 32) {
+      const uint4 a = __ldg(src + v);
+      const uint4 o = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(a.x), bf16x2_to_f16x2_sat(a.y),
+                                                bf16x2_to_f16x2_sat(a.z), bf16x2_to_f16x2_sat(a.w)));
+      for (int j = 0; j < k; ++j)
+        reinterpret_cast<uint4*>(xs + (size_t)pos_s[warp * k + j] * H)[v] = o;
+      if (with_shared) reinterpret_cast<uint4*>(xs + ((size_t)T * k + t) * H)[v] = o;
+    }
   }
 }
 
@@ -1106,7 +1127,8 @@ cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t
                                float* topk_w, uint8_t* cnt8, int32_t* cnt, int32_t* off,
                                int32_t* tile_off, int32_t* bmap, int32_t* num_tiles,
                                int32_t* perm, int32_t* inv, unsigned* arrive, unsigned* gen,
-                               DevErr err, cudaStream_t st) {
+                               DevErr err, const uint16_t* x, uint16_t* xs, int H,
+                               int with_shared, cudaStream_t st) {
   const int nblk = (T + kRouterTB - 1) / kRouterTB;
   const int np = (nblk + 15) / 16 * 16;
   cudaLaunchConfig_t cfg = {};
@@ -1123,9 +1145,11 @@ cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t
   cfg.numAttrs = 1;
   if (E <= 256)
     return cudaLaunchKernelEx(&cfg, route_large_kernel<8>, logits, T, E, k, topk_idx, topk_w, cnt8,
-                              np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err);
+                              np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err,
+                              x, xs, H, with_shared);
   return cudaLaunchKernelEx(&cfg, route_large_kernel<16>, logits, T, E, k, topk_idx, topk_w, cnt8,
-                            np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err);
+                            np, cnt, off, tile_off, bmap, num_tiles, perm, inv, arrive, gen, err,
+                            x, xs, H, with_shared);
 }
 
 // ---------------------------------------------------------------------------

@@ -201,6 +201,25 @@ def test_ffn_on_caller_routing():
         bg.moe_plan_destroy(plan)
 
 
+@pytest.mark.parametrize("name", ["t512_zipf", "t2048_uniform"])
+def test_routing_fused_gather_matches_gather_launch(name):
+    # moe_forward_layer lets the cooperative routing launch write the gathered
+    # rows; moe_route + moe_grouped_w4_ffn runs the separate gather kernel.
+    w = WL[name]
+    c = Case(w, gap=False)
+    plan = make_plan(w)
+    try:
+        y1 = run_layer(c, plan).cpu().numpy()
+        r = bg.moe_route(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias)
+        y2 = torch.empty(c.x.shape, dtype=torch.float32, device="cuda")
+        bg.moe_grouped_w4_ffn(plan, c.x, w.tokens, r, c.L.routed_c, c.L.shared_c, y2)
+        torch.cuda.synchronize()
+        assert bg.moe_get_error(plan) == 0
+        assert np.array_equal(y1, y2.cpu().numpy())
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("path", [1, 2])
 def test_deterministic(path):
     w = WL["t512_zipf"]
