@@ -884,7 +884,10 @@ cudaError_t launch_route_small(const uint16_t* x, int T, int H, const uint16_t* 
 // the same order as route_scan_kernel, the expert totals and offsets and its
 // own block's offsets, and scatters its slots; CTA 0 also writes the totals,
 // offsets, tile offsets and block map. Every output is bit-identical to
-// router_topk_kernel + route_scan_kernel + route_scatter_kernel.
+// router_topk_kernel + route_scan_kernel + route_scatter_kernel. Given `xs`,
+// the CTA then also gathers its tokens' rows (gather_rows_kernel's output,
+// bit-identical): each token row is read once and written to its k
+// positions and its shared-expert row.
 // ---------------------------------------------------------------------------
 constexpr int kRlThreads = 32 * kRouterTB;   // one warp per token
 constexpr int kRlMaxPer = 32;                // blocks per scanning thread (counts held in registers)
