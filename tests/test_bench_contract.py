@@ -1,6 +1,7 @@
 """The JSON line of bench.py's reference arm (the fp64 oracle on the host
 cores), run on a small workload: every key of the line and their relations.
-This arm needs no GPU; the GPU arm's line is written by the same helpers."""
+This arm needs no GPU; it shares the argument parsing, the workload table and
+the oracle sampling (its cpu_baseline) with the GPU arm."""
 import json
 import os
 import subprocess
