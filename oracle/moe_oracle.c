@@ -125,12 +125,25 @@ void oracle_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
     }
 }
 
+/* The value a logit ranks by. The pages say nothing about a NaN score; the
+ * reading taken is that a NaN logit counts as -infinity: it ranks below every
+ * number (ties among such experts go to the lower index like any other tie)
+ * and gets softmax weight zero. -0 and +0 compare equal, so they tie. */
+static double rank_value(double l) {
+#if ORACLE_PLANT == 13
+  return isnan(l) ? INFINITY : l;                /* planted: NaN ranks first */
+#else
+  return isnan(l) ? -INFINITY : l;
+#endif
+}
+
 /* is expert a ranked before expert b (higher logit, lower index on ties) */
 static int ranks_before(const double* l, int a, int b) {
+  double la = rank_value(l[a]), lb = rank_value(l[b]);
 #if ORACLE_PLANT == 5
-  return l[a] > l[b] || (l[a] == l[b] && a > b);   /* planted: ties upward */
+  return la > lb || (la == lb && a > b);         /* planted: ties upward */
 #else
-  return l[a] > l[b] || (l[a] == l[b] && a < b);
+  return la > lb || (la == lb && a < b);
 #endif
 }
 
@@ -156,11 +169,11 @@ void oracle_topk(const double* logits, int T, int E, int k, int32_t* idx,
     for (int e = 0; e < E; ++e)
       if (!taken[e] && (next < 0 || ranks_before(l, e, next))) next = e;
     int last = idx[(size_t)t * k + k - 1];
-    gap[t] = next < 0 ? INFINITY : l[last] - l[next];
-    /* softmax over all experts */
-    double mx = l[idx[(size_t)t * k]];
+    gap[t] = next < 0 ? INFINITY : rank_value(l[last]) - rank_value(l[next]);
+    /* softmax over all experts (a NaN logit as -infinity: weight zero) */
+    double mx = rank_value(l[idx[(size_t)t * k]]);
     double z = 0.0;
-    for (int e = 0; e < E; ++e) { p[e] = exp(l[e] - mx); z += p[e]; }
+    for (int e = 0; e < E; ++e) { p[e] = exp(rank_value(l[e]) - mx); z += p[e]; }
     for (int e = 0; e < E; ++e) p[e] /= z;
     /* renormalise over the selected experts */
     double zs = 0.0;

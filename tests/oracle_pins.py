@@ -152,6 +152,28 @@ def pin_topk_ties(orc):
     assert gap[0] == 0.0
 
 
+def pin_topk_nan_and_signed_zero(orc):
+    # A NaN logit ranks as -inf (below every number, lower index first among
+    # equals) and gets weight zero; -0 and +0 tie; all-NaN rows keep valid,
+    # distinct indices (their weights are 0/0).
+    nan = float("nan")
+    L = np.array([[nan, 1.0, 2.0, nan]])
+    idx, w, gap = orc.topk(L, 2)
+    assert idx[0].tolist() == [2, 1]
+    e = np.exp(1.0)
+    assert np.allclose(w[0], [e / (e + 1), 1 / (e + 1)], rtol=1e-15, atol=0)
+    assert gap[0] == np.inf                      # runner-up is a NaN (-inf)
+    idx, w, _ = orc.topk(L, 3)
+    assert idx[0].tolist() == [2, 1, 0] and w[0, 2] == 0.0
+    idx, w, _ = orc.topk(L, 4)
+    assert idx[0].tolist() == [2, 1, 0, 3] and w[0, 3] == 0.0
+    L = np.array([[-0.0, 0.0, -0.0, -1.0]])
+    idx, w, gap = orc.topk(L, 2)
+    assert idx[0].tolist() == [0, 1] and np.array_equal(w[0], [0.5, 0.5]) and gap[0] == 0.0
+    idx, w, _ = orc.topk(np.full((1, 5), nan), 3)
+    assert idx[0].tolist() == [0, 1, 2] and np.isnan(w).all()
+
+
 def pin_topk_weights(orc):
     rng = np.random.default_rng(6)
     E = 16
@@ -326,6 +348,7 @@ def pin_rmsnorm(orc):
 
 
 ALL_PINS = [pin_bf16, pin_dequant_integer, pin_dequant_bias_only, pin_dequant_one_hot,
-            pin_router_library, pin_topk_bruteforce, pin_topk_ties, pin_topk_weights,
+            pin_router_library, pin_topk_bruteforce, pin_topk_ties,
+            pin_topk_nan_and_signed_zero, pin_topk_weights,
             pin_route_maps, pin_ffn_odd_identity, pin_ffn_zero_gate, pin_layer_k1,
             pin_layer_shared_weight_one, pin_residual, pin_rmsnorm]

@@ -18,6 +18,7 @@ PLANTS = {
     10: "down matrix transposed",
     11: "shared expert dropped",
     12: "rms norm without square root",
+    13: "NaN logit ranked above every number",
 }
 
 
