@@ -14,7 +14,11 @@ weights, 18 GB, are far larger than L2, so every step streams them from HBM).
 e2e: the same through the C ABI with x copied in from pinned host memory and
 the result copied back, inside the timed region.
 roofline: the dominant kernel (grouped gate/up GEMM) against the measured
-dense bf16 peak. cpu_baseline: the fp64 oracle on a bounded sample.
+dense bf16 peak (burst, or the sustained figure when the clock record of the
+timed region shows the power cap); the down GEMM's figures beside it.
+cpu_baseline: the fp64 oracle on a bounded sample.
+decode: the same stack on decode-sized batches T = 1, 4, 8 (1000 graph-replayed
+steps each by default), HBM roofline as for --workload decode_t*_l40.
 
 --workload decode_t{1,4,8}_l40: the same 40-layer stack on a decode batch of
 T tokens through the small-M path. Every step copies a fresh batch from a
@@ -68,6 +72,10 @@ def parse_args(argv=None):
                          "whole prompt in one chunk")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true",
+                    help="skip the decode-sized batches (T = 1, 4, 8) of the default line")
+    ap.add_argument("--decode-steps", type=int, default=1000,
+                    help="graph-replayed steps per decode batch size")
     return ap.parse_args(argv)
 
 
@@ -77,6 +85,42 @@ def parse_args(argv=None):
 def dist_info():
     return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
             int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def cpu_model():
+    """Host CPU model name (x86 /proc/cpuinfo 'model name', else lscpu's
+    'Model name' as on Arm), or None."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    return None
+
+
+def tensor_peak(peaks, src, clocks):
+    """The dense bf16 peak a tensor-bound kernel of this run is measured
+    against: the burst figure, unless the clock record of the timed region
+    shows the power cap or SM clocks below 90% of their maximum, in which
+    case the sustained (power-capped) figure."""
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    capped = False
+    if clocks and clocks.get("sm_mhz") and clocks.get("sm_max_mhz"):
+        capped = ("sw_power_cap" in clocks.get("reasons", [])
+                  or clocks["sm_mhz"] < 0.9 * clocks["sm_max_mhz"])
+    if capped:
+        return sustained, f"{src} bf16_tflops_sustained (of {src}): power cap or low SM clock seen"
+    return burst, f"{src} bf16_tflops, burst (of {src}): SM clock at maximum, no power cap seen"
 
 
 def load_peaks():
@@ -336,18 +380,25 @@ def main(argv=None):
 
     # --- roofline of the dominant kernel (grouped gate/up GEMM + SwiGLU)
     peaks, peak_src = load_peaks()
+    clocks = clk.summary()
     n_pairs = T * (sh.top_k + int(sh.has_shared))
     gu_ms, gu_n = kt["gate_up_gemm"]
+    dn_ms, dn_n = kt["down_gemm"]
     # per launch: one layer of one chunk (the average over the step's launches)
     flops_gateup = 4.0 * sh.hidden * sh.inter * n_pairs * w.layers * args.steps / max(gu_n, 1)
+    flops_down = 2.0 * sh.hidden * sh.inter * n_pairs * w.layers * args.steps / max(dn_n, 1)
     achieved = flops_gateup / (gu_ms / gu_n / 1e3) / 1e12 if gu_n else None
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    achieved_dn = flops_down / (dn_ms / dn_n / 1e3) / 1e12 if dn_n else None
+    peak, peak_note = tensor_peak(peaks, peak_src, clocks)
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                 "frac": (achieved / peak) if achieved else None,
                 "traffic": profiled_traffic(PROFILE_GATEUP, GEMM_SRC),
                 "kernel": "w4_grouped_gemm_tc, gate/up + SwiGLU (one launch per layer)",
-                "peak_source": f"{peak_src} bf16_tflops_sustained (of {peak_src})",
-                "algorithmic_flops_per_launch": flops_gateup}
+                "peak_source": peak_note,
+                "algorithmic_flops_per_launch": flops_gateup,
+                "down_gemm": {"achieved": achieved_dn,
+                              "frac": (achieved_dn / peak) if achieved_dn else None,
+                              "algorithmic_flops_per_launch": flops_down}}
     step_flops = w.layers * (n_pairs * 6.0 * sh.hidden * sh.inter +
                              T * 2.0 * sh.hidden * sh.num_experts)
     kernels = {k: {"ms_per_step": v[0] / args.steps, "launches_per_step": v[1] / args.steps}
@@ -360,14 +411,29 @@ def main(argv=None):
         st, sl = (min(T, 16 * threads), min(w.layers, 3))
         rate, el = oracle_sample_rate(w, layers, threads, st, sl)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "cpu_model": cpu_model(),
                "sample": f"{st} tokens x layers 0-{sl - 1} of the {T}-token {w.layers}-layer "
                          f"stack, fp64 oracle on {threads} threads, {el:.1f} s, "
                          f"scaled by {sl}/{w.layers}"}
 
+    # --- decode-sized batches through the same 40-layer stack (same weights)
+    decode = None
+    if not args.no_decode and w.layers > 1:
+        decode = {}
+        for td in (1, 4, 8):
+            wd = synth.standard_workloads()[f"decode_t{td}_l40"]
+            if wd.layers != w.layers or wd.seed != w.seed:
+                wd = dataclasses.replace(wd, layers=w.layers, seed=w.seed)
+            r = measure_decode(wd, layers, local, pg, ws, steps=args.decode_steps,
+                               warmup=max(args.warmup, 10))
+            decode[f"t{td}"] = r
+
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "precision": "bf16 inputs; fp16 MMA operands (activations converted, weights rebuilt "
+                     "as fp16(q*scale+bias)); fp32 accumulation",
         "data": "synthetic",
         "config": {"workload": w.name, "tokens": T, "layers": w.layers, "hidden": sh.hidden,
                    "inter": sh.inter, "experts": sh.num_experts, "top_k": sh.top_k,
@@ -385,13 +451,79 @@ def main(argv=None):
         "gpu_launches": gpu_launches,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "clocks": clk.summary(),
+        "clocks": clocks,
+        "decode": decode,
     }
     if rank == 0:
         print(json.dumps(out), flush=True)
     bg.moe_plan_destroy(plan)
     if pg:
         pg.destroy_process_group()
+
+
+def measure_decode(w, layers, local, pg, ws, steps, warmup):
+    """Decode-sized batch through the stack: the whole step captured in one
+    CUDA graph, replayed `steps` times with a fresh batch copied in from a
+    device pool before each replay; HBM roofline over the packed bytes of the
+    experts each layer's routing selects. Returns the summary dict."""
+    import torch
+    from bit_grouped_gemm_gb300 import binding as bg, stack, synth
+    sh = w.shape
+    T = w.tokens
+    alpha = stack.residual_alpha(w.layers)
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), local)
+    try:
+        pool = synth.decode_pool(w, 64, "cuda")
+        x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
+        xn = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+        for i in range(3):
+            x.copy_(pool[i])
+            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        torch.cuda.synchronize()
+        assert bg.moe_get_error(plan) == 0
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        for i in range(warmup):
+            x.copy_(pool[i % pool.shape[0]], non_blocking=True)
+            graph.replay()
+        torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with ClockSampler(local) as clk:
+            ev0.record(stream)
+            for i in range(steps):
+                x.copy_(pool[i % pool.shape[0]], non_blocking=True)
+                graph.replay()
+            ev1.record(stream)
+            torch.cuda.synchronize()
+        if pg:
+            pg.barrier()
+        ms = max_over_ranks(ev0.elapsed_time(ev1), pg)
+        assert bg.moe_get_error(plan) == 0
+        step_bytes, experts_per_layer = decode_step_bytes(w, layers, plan, pool)
+        peaks, peak_src = load_peaks()
+        peak = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+        ms_per_step = ms / steps
+        achieved = step_bytes / (ms_per_step / 1e3) / 1e9
+        del graph
+        return {"tokens": T, "layers": w.layers, "steps": steps, "warmup": warmup,
+                "ms_per_step": ms_per_step,
+                "value": replica_value(ws, T, steps, ms), "unit": "tokens/s",
+                "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                             "frac": achieved / peak,
+                             "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
+                             "algorithmic_bytes_per_step": step_bytes,
+                             "distinct_routed_experts_per_layer": experts_per_layer},
+                "graph": "whole step replayed from one CUDA graph; fresh batch per step",
+                "clocks": clk.summary()}
+    finally:
+        bg.moe_plan_destroy(plan)
 
 
 def decode_step_bytes(w, layers, plan, pool, samples=8):
@@ -513,6 +645,7 @@ def run_decode(args, w, ws, rank, local, pg):
         "metric": METRIC_DECODE, "value": replica_value(ws, T, args.steps, ms), "unit": "tokens/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "precision": "bf16 inputs; fp16 MMA operands; fp32 accumulation",
         "data": "synthetic",
         "config": {"workload": w.name, "tokens": T, "layers": w.layers, "hidden": sh.hidden,
                    "inter": sh.inter, "experts": sh.num_experts, "top_k": sh.top_k,
@@ -563,6 +696,7 @@ def run_reference(args, ws, rank):
         secs += el
     value = tok / secs / w.layers
     cpu = {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "cpu_model": cpu_model(),
            "sample": f"{sample} tokens of layer 0 per step, fp64 oracle on {threads} "
                      f"threads, scaled by 1/{w.layers}"}
     print(json.dumps({

@@ -18,7 +18,8 @@ LIB_PATH = os.path.join(HERE, "libmoe_w4.so")
 
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
-                3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY", 5: "MOE_ERR_DEVICE_TIMEOUT"}
+                3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY", 5: "MOE_ERR_DEVICE_TIMEOUT",
+                6: "MOE_ERR_OPERAND_RANGE"}
 KERNEL_KINDS = ("router", "scan", "scatter", "gather", "gate_up_gemm", "down_gemm",
                 "combine", "residual", "topk")
 
@@ -97,6 +98,8 @@ def load_library(path: Optional[str] = None):
         "moe_last_gemm_path": (I, [P]),
         "moe_debug_buffer": (P, [P, I]),
         "moe_route_noalloc": (S, [P, I, I, P, P, I, I, ctypes.POINTER(MoeRouting), P]),
+        "moe_route_noalloc_get_error": (S, []),
+        "moe_route_noalloc_debug_wait_timeout": (S, [I, P]),
         "moe_status_string": (ctypes.c_char_p, [S]),
         "moe_version": (I, []),
     }
@@ -220,6 +223,17 @@ def moe_route_noalloc(x, T: int, hidden: int, router_w, router_bias, num_experts
                                             _ptr(router_bias), num_experts, top_k,
                                             ctypes.byref(out), _stream(stream)),
            "moe_route_noalloc")
+
+
+def moe_route_noalloc_get_error() -> int:
+    """Status of moe_route_noalloc's device error word on the current device
+    (read and cleared; synchronises the device)."""
+    return load_library().moe_route_noalloc_get_error()
+
+
+def moe_route_noalloc_debug_wait_timeout(limit_us: int, stream=None) -> None:
+    _check(load_library().moe_route_noalloc_debug_wait_timeout(int(limit_us), _stream(stream)),
+           "moe_route_noalloc_debug_wait_timeout")
 
 
 def moe_residual_add(plan: int, x, y, T: int, alpha: float, x_out=None, xn_out=None,

@@ -293,6 +293,7 @@ __global__ void __launch_bounds__(kThreads) w4_grouped_gemm_smallm(const __grid_
       }
       __syncthreads();
       const uint16_t* rows_in = p.gather_x ? p.gather_x : p.act_in;
+      uint32_t over = 0u;   // bf16 token values that saturate in fp16
       for (int base = 0; base < 8 * NT * G; base += 2 * kThreads) {
         uint4 v[2][8];
         int sr[2];
@@ -319,9 +320,12 @@ __global__ void __launch_bounds__(kThreads) w4_grouped_gemm_smallm(const __grid_
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
               uint4 x8 = v[q][j];
-              if (p.gather_x)   // bf16 token values -> the fp16 perm8 operand of a gathered row
+              if (p.gather_x) {   // bf16 token values -> the fp16 perm8 operand of a gathered row
+                over |= bf16x2_f16_overflow(x8.x) | bf16x2_f16_overflow(x8.y) |
+                        bf16x2_f16_overflow(x8.z) | bf16x2_f16_overflow(x8.w);
                 x8 = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(x8.x), bf16x2_to_f16x2_sat(x8.y),
                                                bf16x2_to_f16x2_sat(x8.z), bf16x2_to_f16x2_sat(x8.w)));
+              }
               dst[4 * j + 0] = x8.x;   // (x0, x4)
               dst[4 * j + 1] = x8.y;   // (x1, x5)
               dst[4 * j + 2] = x8.z;   // (x2, x6)
@@ -336,6 +340,7 @@ __global__ void __launch_bounds__(kThreads) w4_grouped_gemm_smallm(const __grid_
           xg[tr * G + grp] = sum;
         }
       }
+      report_range_warp(p.err, over != 0u);
       if (pass0 == 0) {
         // bounded wait for the slab; on a timeout the error is latched and
         // the CTA stops (outputs of the unit left unwritten)

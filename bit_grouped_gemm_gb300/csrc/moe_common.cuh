@@ -54,7 +54,11 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // ---------------------------------------------------------------- errors ---
 // Device error word bits (latched with atomicOr, read by moe_get_error).
-enum : int { DEVERR_TIMEOUT = 1 };
+//   DEVERR_TIMEOUT: a bounded wait ran out;
+//   DEVERR_RANGE:   an operand left the range in which its conversion to the
+//                   MMAs' fp16 is faithful (see bf16x2_f16_overflow and
+//                   w4_range_flags).
+enum : int { DEVERR_TIMEOUT = DEVERR_TIMEOUT_BIT, DEVERR_RANGE = DEVERR_RANGE_BIT };
 
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -65,6 +69,20 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 __device__ __forceinline__ void report_timeout(const DevErr& e, int site) {
   atomicOr(e.word, DEVERR_TIMEOUT);
   atomicCAS(e.where, 0, site);
+}
+
+// Latches DEVERR_RANGE once per warp that saw a flag (call with the whole
+// warp converged).
+__device__ __forceinline__ void report_range_warp(const DevErr& e, bool bad) {
+  if (__any_sync(0xffffffffu, bad) && (threadIdx.x & 31) == 0) atomicOr(e.word, DEVERR_RANGE);
+}
+
+// Nonzero when either bf16 of the pair has magnitude >= 2^16 (or is inf or
+// NaN): its fp16 conversion saturates. The magnitudes m < 0x8000 of both
+// halves get 0x8000 - 0x4780 added in one 32-bit add (no carry between the
+// halves), which sets bit 15 of a half exactly when m >= 0x4780 (2^16).
+__device__ __forceinline__ uint32_t bf16x2_f16_overflow(uint32_t v) {
+  return ((v & 0x7FFF7FFFu) + 0x38803880u) & 0x80008000u;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

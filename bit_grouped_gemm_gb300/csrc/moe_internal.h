@@ -13,6 +13,10 @@ constexpr int kBM = 128;          // rows per block-map tile
 constexpr int kRouterTB = 32;     // tokens per router / scatter block
 constexpr int kGroup = 64;        // quantisation group
 
+// Bits of the device error word.
+constexpr int DEVERR_TIMEOUT_BIT = 1;   // a bounded wait ran out
+constexpr int DEVERR_RANGE_BIT = 2;     // an operand outside the fp16 range
+
 // Device error state: plain pointers, usable on host and device.
 struct DevErr {
   int* word;                      // error bits (DEVERR_*)
@@ -34,17 +38,20 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const voi
 
 // -------------------------------------------------------------- routing ---
 // Router logits: the tcgen05 path when router_tc_fits (and logits and bias
-// are 16-byte aligned), else the mma.sync paths.
+// are 16-byte aligned), else the mma.sync paths. weights_early: the small-T
+// kernel may copy the router weight before waiting for the previous launch
+// (true inside the library's own launch sequences, where no launch writes
+// weights).
 bool router_tc_fits(int T, int H, int E);
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
                                  const float* bias, int E, float* logits, DevErr err,
-                                 cudaStream_t st);
+                                 cudaStream_t st, bool weights_early = true);
 cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32_t* topk_idx,
                                  float* topk_w, int32_t* blk_cnt, cudaStream_t st);
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
                                float* topk_w, float* logits, int32_t* blk_cnt, DevErr err,
-                               cudaStream_t st);
+                               cudaStream_t st, bool weights_early = true);
 cudaError_t launch_route_scan(int32_t* blk_cnt, int nblk, int T, int k, int E,
                               int32_t* cnt, int32_t* off, int32_t* tile_off, int32_t* bmap,
                               int32_t* num_tiles, cudaStream_t st);
@@ -75,7 +82,11 @@ cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t
                                DevErr err, const uint16_t* x, uint16_t* xs, int H,
                                int with_shared, cudaStream_t st);
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
-                               int with_shared, uint16_t* xs, cudaStream_t st);
+                               int with_shared, uint16_t* xs, DevErr err, cudaStream_t st);
+// Checks the fp16 operand range of n scales and biases (bf16) of a 4-bit
+// weight set; latches DEVERR_RANGE in err when one is out of range.
+cudaError_t launch_w4_range_check(const uint16_t* s, const uint16_t* b, size_t n, DevErr err,
+                                  int num_sms, cudaStream_t st);
 cudaError_t launch_combine(const uint16_t* d, const float* d_sh, const int32_t* inv, int T,
                            int k, int H, float* y, cudaStream_t st);
 // combine, then x = bf16(x + alpha * y) in place and xn = bf16(rmsnorm(x)),

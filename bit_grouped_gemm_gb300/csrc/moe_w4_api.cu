@@ -6,6 +6,7 @@
 #include <cstring>
 #include <map>
 #include <mutex>
+#include <set>
 #include <tuple>
 #include <vector>
 
@@ -104,6 +105,8 @@ struct moe_plan {
   // encoded uint32 [rows][cols] maps of packed weights, by (base, rows, cols,
   // box rows): a layer's maps are encoded on its first call only
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t>, CUtensorMap> qmaps;
+  // weight sets (scales, biases, count) whose fp16 operand range was checked
+  std::set<std::tuple<const void*, const void*, size_t>> range_checked;
 
   bool qmap(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     const auto key = std::make_tuple(base, rows, cols, box_rows);
@@ -280,12 +283,32 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   const int path = ffn_path(p, T);
   p->last_path = path;
 
+  // The scales and biases of a weight set are checked against the fp16
+  // operand range once, on the first call that sees the set (by address), in
+  // a kernel on the stream; a value out of range latches DEVERR_RANGE.
+  cudaError_t e = cudaSuccess;
+  auto range_check = [&](const moe_w4& m, size_t n) {
+    if (p->range_checked.size() >= 4096) p->range_checked.clear();
+    if (!p->range_checked.insert(std::make_tuple((const void*)m.scales, (const void*)m.biases, n)).second)
+      return cudaSuccess;
+    return launch_w4_range_check(m.scales, m.biases, n, p->err(), p->num_sms, st);
+  };
+  const size_t n_gu = (size_t)I * (H / kGroup), n_dn = (size_t)H * (I / kGroup);
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+    const moe_w4& m = i == 0 ? routed->gate : i == 1 ? routed->up : routed->down;
+    e = range_check(m, (i < 2 ? n_gu : n_dn) * E);
+    if (e == cudaSuccess && hs) {
+      const moe_w4& ms = i == 0 ? shared->gate : i == 1 ? shared->up : shared->down;
+      e = range_check(ms, i < 2 ? n_gu : n_dn);
+    }
+  }
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+
   // the tensor-core path reads gathered rows with TMA; the small-M path reads
   // the token rows itself
-  cudaError_t e = cudaSuccess;
   if (path == 1 && !pre_gathered) {
     e = timed(p, 3, st, [&] {
-      return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), st);
+      return launch_gather_rows(x, r->perm, T, k, H, hs, p->at<uint16_t>(p->L.xs), p->err(), st);
     });
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
@@ -629,7 +652,8 @@ moe_status moe_get_error(moe_plan_t p) {
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaSetDevice(prev);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (h[0] & 1) return MOE_ERR_DEVICE_TIMEOUT;
+  if (h[0] & DEVERR_TIMEOUT_BIT) return MOE_ERR_DEVICE_TIMEOUT;
+  if (h[0] & DEVERR_RANGE_BIT) return MOE_ERR_OPERAND_RANGE;
   return MOE_OK;
 }
 
@@ -685,10 +709,11 @@ const char* moe_status_string(moe_status s) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_CAPACITY: return "T above plan capacity";
     case MOE_ERR_DEVICE_TIMEOUT: return "device bounded wait timed out";
+    case MOE_ERR_OPERAND_RANGE: return "operand outside the fp16 range of the MMAs";
   }
   return "unknown status";
 }
 
-int moe_version(void) { return 100; }
+int moe_version(void) { return 200; }
 
 }  // extern "C"

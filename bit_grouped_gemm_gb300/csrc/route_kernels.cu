@@ -365,12 +365,17 @@ __device__ __forceinline__ void rs_logits(const uint16_t* __restrict__ x, int T,
   }
 }
 
+// kEarlyW: copy the weight columns before waiting for the previous launch
+// (the library's own launch sequences, where no launch writes the weights);
+// otherwise after it (a caller's kernel just before may write them).
+template <bool kEarlyW>
 __global__ void __launch_bounds__(256) router_logits_small_kernel(
     const uint16_t* __restrict__ x, int T, int H, const uint16_t* __restrict__ wr,
     const float* __restrict__ bias, int E, float* __restrict__ logits) {
   extern __shared__ __align__(128) uint8_t smem[];
-  rs_load_w(wr, H, E, smem);   // weights: written by no launch of this library
+  if (kEarlyW) rs_load_w(wr, H, E, smem);
   pdl_begin();
+  if (!kEarlyW) rs_load_w(wr, H, E, smem);
   rs_logits(x, T, H, bias, E, logits, smem);
 }
 
@@ -568,7 +573,7 @@ cudaError_t launch_router_logits_tc(const uint16_t* x, int T, int H, const uint1
 
 cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t* wr,
                                  const float* bias, int E, float* logits, DevErr err,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, bool weights_early) {
   if (!logits) return cudaErrorInvalidValue;
   // (the tensor-core epilogue moves logits and bias in 16-byte pieces)
   const bool al16 = ((reinterpret_cast<uintptr_t>(logits) | reinterpret_cast<uintptr_t>(bias)) & 15u) == 0;
@@ -576,11 +581,13 @@ cudaError_t launch_router_logits(const uint16_t* x, int T, int H, const uint16_t
     return launch_router_logits_tc(x, T, H, wr, bias, E, logits, err, st);
   if (T <= kRsMaxT && H % 128 == 0 && rs_smem_bytes(H) <= 227 * 1024) {
     const size_t smem = rs_smem_bytes(H);
-    cudaError_t e = cudaFuncSetAttribute(router_logits_small_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    return launch_pdl(router_logits_small_kernel, dim3((E + 15) / 16), dim3(256), smem, st, x, T,
-                      H, wr, bias, E, logits);
+    auto launch = [&](auto kern) -> cudaError_t {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
+      return launch_pdl(kern, dim3((E + 15) / 16), dim3(256), smem, st, x, T, H, wr, bias, E, logits);
+    };
+    return weights_early ? launch(router_logits_small_kernel<true>)
+                         : launch(router_logits_small_kernel<false>);
   }
   const size_t smem = (size_t)kLgStages * (kLgXStage + kLgWStage) * 2;
   cudaError_t e = cudaFuncSetAttribute(router_logits_kernel,
@@ -603,8 +610,8 @@ cudaError_t launch_router_select(const float* logits, int T, int E, int k, int32
 cudaError_t launch_router_topk(const uint16_t* x, int T, int H, const uint16_t* wr,
                                const float* bias, int E, int k, int32_t* topk_idx,
                                float* topk_w, float* logits, int32_t* blk_cnt, DevErr err,
-                               cudaStream_t st) {
-  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, err, st);
+                               cudaStream_t st, bool weights_early) {
+  cudaError_t e = launch_router_logits(x, T, H, wr, bias, E, logits, err, st, weights_early);
   if (e != cudaSuccess) return e;
   return launch_router_select(logits, T, E, k, topk_idx, topk_w, blk_cnt, st);
 }
@@ -1091,14 +1098,18 @@ __global__ void __launch_bounds__(kRlThreads) route_large_kernel(
   if (warp < nt) {
     const int t = t0 + warp;
     const uint4* src = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    uint32_t over = 0u;
     for (int v = lane; v < H / 8; v += 32) {
       const uint4 a = __ldg(src + v);
+      over |= bf16x2_f16_overflow(a.x) | bf16x2_f16_overflow(a.y) | bf16x2_f16_overflow(a.z) |
+              bf16x2_f16_overflow(a.w);
       const uint4 o = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(a.x), bf16x2_to_f16x2_sat(a.y),
                                                 bf16x2_to_f16x2_sat(a.z), bf16x2_to_f16x2_sat(a.w)));
       for (int j = 0; j < k; ++j)
         reinterpret_cast<uint4*>(xs + (size_t)pos_s[warp * k + j] * H)[v] = o;
       if (with_shared) reinterpret_cast<uint4*>(xs + ((size_t)T * k + t) * H)[v] = o;
     }
+    report_range_warp(err, over != 0u);
   }
 }
 
@@ -1160,35 +1171,88 @@ cudaError_t launch_route_large(const float* logits, int T, int E, int k, int32_t
 // xs[T*k + t] = x[t] for the shared expert's rows, converted from bf16 to the
 // GEMMs' fp16 operand type (exact inside fp16's range, saturating outside),
 // each block of 8 stored in perm8 order (the K order of the dequantised
-// weights). One warp per row.
+// weights). One warp per row. A value of magnitude 2^16 or more (or inf, or
+// NaN) saturates and latches DEVERR_RANGE.
 // ---------------------------------------------------------------------------
 __global__ void gather_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ perm,
                                    int T, int k, int H, int with_shared,
-                                   uint16_t* __restrict__ xs) {
+                                   uint16_t* __restrict__ xs, DevErr err) {
   pdl_begin();
   const int rows = T * k + (with_shared ? T : 0);
   const int lane = threadIdx.x & 31;
   const int wid = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int nw = (gridDim.x * blockDim.x) >> 5;
   const int vec = H / 8;   // 16-byte vectors per row
+  uint32_t over = 0u;
   for (int r = wid; r < rows; r += nw) {
     const int src = r < T * k ? perm[r] / k : r - T * k;
     const uint4* s = reinterpret_cast<const uint4*>(x + (size_t)src * H);
     uint4* d = reinterpret_cast<uint4*>(xs + (size_t)r * H);
     for (int i = lane; i < vec; i += 32) {
       const uint4 v = __ldg(s + i);
+      over |= bf16x2_f16_overflow(v.x) | bf16x2_f16_overflow(v.y) | bf16x2_f16_overflow(v.z) |
+              bf16x2_f16_overflow(v.w);
       d[i] = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(v.x), bf16x2_to_f16x2_sat(v.y),
                                        bf16x2_to_f16x2_sat(v.z), bf16x2_to_f16x2_sat(v.w)));
     }
   }
+  report_range_warp(err, over != 0u);
 }
 
 cudaError_t launch_gather_rows(const uint16_t* x, const int32_t* perm, int T, int k, int H,
-                               int with_shared, uint16_t* xs, cudaStream_t st) {
+                               int with_shared, uint16_t* xs, DevErr err, cudaStream_t st) {
   const int rows = T * k + (with_shared ? T : 0);
   int blocks = (rows + 7) / 8;
   if (blocks > 4096) blocks = 4096;
-  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, x, perm, T, k, H, with_shared, xs);
+  return launch_pdl(gather_rows_kernel, dim3(blocks), dim3(256), 0, st, x, perm, T, k, H, with_shared,
+                    xs, err);
+}
+
+// ---------------------------------------------------------------------------
+// Operand range of a 4-bit weight set for the tensor-core path, which
+// rebuilds each weight as fp16(q * scale + bias) from fp16 copies of the bf16
+// scale and bias. Faithful when every scale is 0 or has magnitude in
+// [2^-14, 2^12) (a normal fp16, and 15 * scale stays below 2^16) and every
+// bias has magnitude below 2^11 (so |q * scale + bias| < 65504). Anything
+// else (a subnormal or huge scale, a huge bias, inf, NaN) latches
+// DEVERR_RANGE. Flags are computed on pairs of bf16 magnitudes m < 0x8000 by
+// 32-bit adds that set bit 15 of a half when m reaches a bound (no carry
+// crosses between the halves).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t w4_range_flags(uint32_t s2, uint32_t b2) {
+  const uint32_t ms = s2 & 0x7FFF7FFFu, mb = b2 & 0x7FFF7FFFu;
+  const uint32_t s_high = ms + 0x3A803A80u;    // m >= 0x4580 (2^12)
+  const uint32_t s_nz = ms + 0x7FFF7FFFu;      // m >= 1
+  const uint32_t s_norm = ms + 0x47804780u;    // m >= 0x3880 (2^-14)
+  const uint32_t b_high = mb + 0x3B003B00u;    // m >= 0x4500 (2^11)
+  return (s_high | (s_nz & ~s_norm) | b_high) & 0x80008000u;
+}
+
+__global__ void __launch_bounds__(256) w4_range_kernel(const uint16_t* __restrict__ s,
+                                                       const uint16_t* __restrict__ b, size_t n,
+                                                       DevErr err) {
+  pdl_begin();
+  uint32_t bad = 0u;
+  const size_t stride = (size_t)gridDim.x * blockDim.x;
+  const size_t i0 = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const uint4* s4 = reinterpret_cast<const uint4*>(s);
+  const uint4* b4 = reinterpret_cast<const uint4*>(b);
+  for (size_t i = i0; i < n / 8; i += stride) {
+    const uint4 sv = __ldg(s4 + i), bv = __ldg(b4 + i);
+    bad |= w4_range_flags(sv.x, bv.x) | w4_range_flags(sv.y, bv.y) | w4_range_flags(sv.z, bv.z) |
+           w4_range_flags(sv.w, bv.w);
+  }
+  for (size_t i = n / 8 * 8 + i0; i < n; i += stride)   // tail (n not a multiple of 8)
+    bad |= w4_range_flags(s[i], b[i]) & 0x8000u;
+  report_range_warp(err, bad != 0u);
+}
+
+cudaError_t launch_w4_range_check(const uint16_t* s, const uint16_t* b, size_t n, DevErr err,
+                                  int num_sms, cudaStream_t st) {
+  size_t blocks = (n / 8 + 255) / 256;
+  if (blocks > (size_t)4 * num_sms) blocks = (size_t)4 * num_sms;
+  if (blocks < 1) blocks = 1;
+  return launch_pdl(w4_range_kernel, dim3((unsigned)blocks), dim3(256), 0, st, s, b, n, err);
 }
 
 // ---------------------------------------------------------------------------

@@ -1,14 +1,14 @@
 // route_noalloc.cu -- routing for callers that cannot allocate device memory.
 //
 // moe_route needs a plan, and a plan allocates its scratch with cudaMalloc.
-// Some callers cannot do that: code running inside another framework's
-// memory pool or graph-capture region (where a cudaMalloc would break the
-// capture or force a device-wide synchronisation), allocator-less embedded
-// runtimes, and callbacks that must not block. moe_route_noalloc serves
-// them: the caller passes inputs and every output buffer, and the only
-// scratch the routing kernels need (the per-token-block expert counts) lives
-// in a fixed array in this file, sized for at most kMaxTokens tokens and
-// kMaxExperts experts.
+// Some callers cannot do that: a host framework that hands out all device
+// memory from its own pool (a cudaMalloc behind its back can fail or
+// fragment the memory it budgets), runtimes with no device allocator at
+// all, and latency-bound callbacks that must not block (cudaMalloc can
+// synchronise the device). moe_route_noalloc serves them: the caller passes
+// inputs and every output buffer, and the only scratch the routing kernels
+// need (the per-token-block expert counts) lives in a fixed array in this
+// file, sized for at most kMaxTokens tokens and kMaxExperts experts.
 #include <mutex>
 
 #include "moe_internal.h"
@@ -27,8 +27,9 @@ constexpr int kMaxDevices = 64;
 // the GPU (different streams, no ordering) race on it.
 static __device__ __align__(256) int32_t g_blk_cnt[kMaxBlocks * kMaxExperts];
 
-// The error word of the tensor-core logits' bounded waits (latched, never
-// cleared: a timeout there means the GPU has stopped making progress).
+// The error word of the tensor-core logits' bounded waits: bits as in the
+// plan's error word, then the first failing site. Read and cleared by
+// moe_route_noalloc_get_error.
 static __device__ int g_err[2];
 
 std::mutex g_mu;
@@ -58,6 +59,8 @@ moe_status scratch_address(Scratch* out) {
 
 bool al(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+
 }  // namespace
 
 extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
@@ -68,7 +71,8 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
   if (T < 1 || hidden <= 0 || hidden % 64 || num_experts < 8 || num_experts % 8 ||
       top_k < 1 || top_k > num_experts)
     return MOE_ERR_INVALID_ARG;
-  if (T > kMaxTokens || num_experts > kMaxExperts || top_k > 32) return MOE_ERR_CAPACITY;
+  if (top_k > 32) return MOE_ERR_UNSUPPORTED;
+  if (T > kMaxTokens || num_experts > kMaxExperts) return MOE_ERR_CAPACITY;
   if (!al(x, 16) || !al(router_w, 16) || (router_bias && !al(router_bias, 4)))
     return MOE_ERR_INVALID_ARG;
   const void* need[] = {out->topk_idx, out->topk_w, out->counts,    out->offsets,
@@ -81,12 +85,15 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
   moe_status s = scratch_address(&sc);
   if (s != MOE_OK) return s;
   int32_t* blk = sc.blk;
-  const moe::DevErr err{sc.err, sc.err + 1, 1000000000ull};
+  const moe::DevErr err{sc.err, sc.err + 1, kWaitLimitNs};
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   const int nblk = (T + moe::kRouterTB - 1) / moe::kRouterTB;
+  // every input is read after the previous launch on the stream has
+  // completed (weights_early = false): the caller's own kernel just before
+  // may have written the router weight
   if (moe::launch_router_topk(x, T, hidden, router_w, router_bias, num_experts, top_k,
                               out->topk_idx, out->topk_w, out->logits, blk, err,
-                              st) != cudaSuccess)
+                              st, /*weights_early=*/false) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (moe::launch_route_scan(blk, nblk, T, top_k, num_experts, out->counts, out->offsets,
                              out->tile_offsets, out->block_map, out->num_tiles,
@@ -96,4 +103,28 @@ extern "C" moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden,
                                 st) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+extern "C" moe_status moe_route_noalloc_get_error(void) {
+  Scratch sc;
+  moe_status s = scratch_address(&sc);
+  if (s != MOE_OK) return s;
+  int h[2] = {0, 0};
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e == cudaSuccess) e = cudaMemcpy(h, sc.err, sizeof h, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemset(sc.err, 0, sizeof h);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return (h[0] & moe::DEVERR_TIMEOUT_BIT) ? MOE_ERR_DEVICE_TIMEOUT : MOE_OK;
+}
+
+extern "C" moe_status moe_route_noalloc_debug_wait_timeout(int limit_us, moe_stream_t stream) {
+  if (limit_us <= 0 || limit_us > 10000000) return MOE_ERR_INVALID_ARG;
+  Scratch sc;
+  moe_status s = scratch_address(&sc);
+  if (s != MOE_OK) return s;
+  const moe::DevErr err{sc.err, sc.err + 1, (unsigned long long)limit_us * 1000ull};
+  return moe::launch_debug_wait(err, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
 }

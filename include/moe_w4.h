@@ -30,6 +30,27 @@
  *   - A plan is not thread-safe: calls on one plan must come from one host
  *     thread at a time, and calls that share a plan's scratch must be ordered
  *     on the device (same stream, or explicit events).
+ *   - Operand precision. The pages fix only FP32 accumulation and the bf16
+ *     scale and bias. The expert GEMMs multiply fp16 operands: token values
+ *     are converted from bf16 to fp16 (exact for magnitudes up to 65504;
+ *     below 2^-14 they become fp16 subnormals, an absolute error under
+ *     2^-25, negligible against a unit-scale row), the tensor-core path
+ *     rebuilds each weight as fp16(q * scale + bias) from fp16 copies of the
+ *     scale and bias, and the SwiGLU activations are stored as fp16. The
+ *     contract, checked on the device:
+ *       |x| < 65536 for every token value (a larger one, an inf or a NaN is
+ *         clamped to +-65504 and flagged), checked on every call;
+ *       every scale is 0 or has magnitude in [2^-14, 2^12) and every bias
+ *         has magnitude below 2^11 (then |q * scale + bias| < 65504 and no
+ *         scale is an fp16 subnormal), checked once per weight set, by a
+ *         kernel on the stream the first time a plan sees the set (by its
+ *         scale and bias addresses; new values written in place at the
+ *         same addresses are not checked again).
+ *     A value outside the contract sets a bit in the plan's device error
+ *     word that moe_get_error reports as MOE_ERR_OPERAND_RANGE; the call
+ *     itself still completes with clamped values. The activations the
+ *     block produces itself (RMS-normalised stack input, SwiGLU outputs of
+ *     in-contract weights) stay far inside these bounds.
  */
 #ifndef MOE_W4_H
 #define MOE_W4_H
@@ -50,7 +71,8 @@ typedef enum {
   MOE_ERR_UNSUPPORTED = 2,    /* valid request this build has no kernel for */
   MOE_ERR_CUDA = 3,           /* a CUDA runtime/driver call failed */
   MOE_ERR_CAPACITY = 4,       /* T above the plan's max_tokens */
-  MOE_ERR_DEVICE_TIMEOUT = 5  /* a device-side bounded wait ran out */
+  MOE_ERR_DEVICE_TIMEOUT = 5, /* a device-side bounded wait ran out */
+  MOE_ERR_OPERAND_RANGE = 6   /* an input outside the fp16 operand range (below) */
 } moe_status;
 
 /* Plan description. Sizes are in elements. */
@@ -214,31 +236,53 @@ moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, 
 
 /* Routing without a plan and without any device allocation. The pages have
  * no counterpart: this entry point exists for callers that cannot call
- * cudaMalloc -- code running inside another framework's memory pool or
- * stream-capture region (where an allocation would break the capture or
- * synchronise the device), allocator-less embedded runtimes, callbacks that
- * must not block. It computes exactly what moe_route computes, with the
- * same kernels.
+ * cudaMalloc -- a host framework that hands out all device memory from its
+ * own pool (an allocation behind its back can fail or fragment the memory
+ * it budgets), runtimes with no device allocator at all, and latency-bound
+ * callbacks that must not block (cudaMalloc can synchronise the device).
+ * It computes exactly what moe_route computes, with the same kernels.
  * The caller passes x, router_w, router_bias (may be NULL) as for moe_route
  * and every output buffer in `out` (layouts as in moe_routing; block_map
  * must hold ceil(T*k/128) + E triples; logits is required, every buffer
- * 8-byte aligned; hidden a multiple of 64, num_experts a multiple of 8,
- * otherwise MOE_ERR_INVALID_ARG). The library's
- * only scratch for this call is a fixed device array of 128 x 512 int32
- * (256 KB) in the library image, present on every GPU that loads the
- * library until the process exits; hence T <= 4096 and num_experts <= 512,
- * and larger requests return MOE_ERR_CAPACITY. Nothing in that array needs
- * clearing between calls. The first call on a device looks up the array's
- * device address (with that device current); make that first call before
- * any stream capture. All calls share the array: calls that can overlap on
- * the GPU (different streams without ordering) race and must not be made. */
+ * 8-byte aligned; hidden a multiple of 64, num_experts a multiple of 8 and
+ * at least 8, 1 <= top_k <= num_experts, otherwise MOE_ERR_INVALID_ARG;
+ * top_k above 32 returns MOE_ERR_UNSUPPORTED as for a plan). Every input is
+ * read only after the previous work on the stream has completed, so the
+ * caller's own kernel just before may write x or the router weight.
+ * The library's only scratch for this call is a fixed device array of
+ * 128 x 512 int32 (256 KB) in the library image, present on every GPU that
+ * loads the library until the process exits; hence T <= 4096 and
+ * num_experts <= 512, and larger requests return MOE_ERR_CAPACITY. Nothing
+ * in that array needs clearing between calls. The first call on a device
+ * looks up the array's device address (with that device current); make
+ * that first call before any stream capture. All calls share the array:
+ * calls that can overlap on the GPU (different streams without ordering)
+ * race and must not be made.
+ * A bounded wait of the routing kernels that runs out (1 s) leaves the
+ * outputs unspecified and is reported by moe_route_noalloc_get_error. */
 moe_status moe_route_noalloc(const uint16_t* x, int T, int hidden, const uint16_t* router_w,
                              const float* router_bias, int num_experts, int top_k,
                              const moe_routing* out, moe_stream_t stream);
 
+/* Reads and clears the device error word of moe_route_noalloc on the
+ * current device (shared by every call on that device). Synchronises the
+ * device: call it between steps, never inside one. Returns MOE_OK,
+ * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA if the context has failed. Not
+ * part of the pages' method: the error path of the call above. */
+moe_status moe_route_noalloc_get_error(void);
+
+/* Launches, on `stream`, a kernel whose bounded wait can never be satisfied,
+ * with the given limit (1 us .. 10 s) and the error word of
+ * moe_route_noalloc: it gives up, latches MOE_ERR_DEVICE_TIMEOUT there and
+ * exits, so a test can check moe_route_noalloc_get_error without faulting
+ * or hanging the GPU. */
+moe_status moe_route_noalloc_debug_wait_timeout(int limit_us, moe_stream_t stream);
+
 /* Reads and clears the plan's device error word. Synchronises the device:
  * call it between layers or steps, never inside one. Returns MOE_OK,
- * MOE_ERR_DEVICE_TIMEOUT, or MOE_ERR_CUDA if the context has failed. */
+ * MOE_ERR_DEVICE_TIMEOUT (a bounded wait ran out; reported first),
+ * MOE_ERR_OPERAND_RANGE (an input outside the fp16 operand contract above),
+ * or MOE_ERR_CUDA if the context has failed. */
 moe_status moe_get_error(moe_plan_t plan);
 
 /* Launch a kernel whose bounded wait can never be satisfied, with the given

@@ -31,6 +31,20 @@ def host_set(dev_set: dict) -> dict:
     return {m: (words(q), bits(s), bits(b)) for m, (q, s, b) in dev_set.items()}
 
 
+def router_logits_mt(orc, x_bits: np.ndarray, wr_bits: np.ndarray, rb) -> np.ndarray:
+    """The oracle's router logits of many rows, the rows split over host
+    threads (each thread one call of the oracle on a contiguous slice)."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+    T = x_bits.shape[0]
+    n = max(1, min(os.cpu_count() or 1, (T + 63) // 64))
+    cuts = np.linspace(0, T, n + 1).astype(int)
+    with ThreadPoolExecutor(n) as ex:
+        parts = list(ex.map(lambda i: orc.router_logits(x_bits[cuts[i]:cuts[i + 1]], wr_bits, rb),
+                            range(n)))
+    return np.concatenate(parts, axis=0)
+
+
 def enforce_gap(w: synth.Workload, x: torch.Tensor, router_w: torch.Tensor,
                 router_bias, k: int, max_attempts: int = 20) -> np.ndarray:
     """Redraw rows of x (in place) until every token's 8th/9th logit gap in
@@ -38,13 +52,14 @@ def enforce_gap(w: synth.Workload, x: torch.Tensor, router_w: torch.Tensor,
     orc = oracle.get()
     wr = bits(router_w)
     rb = None if router_bias is None else router_bias.cpu().numpy()
+    _, _, gap = orc.topk(router_logits_mt(orc, bits(x), wr, rb), k)
     for attempt in range(1, max_attempts + 1):
-        logits = orc.router_logits(bits(x), wr, rb)
-        _, _, gap = orc.topk(logits, k)
         bad = np.nonzero(gap < GAP_MIN)[0]
         if bad.size == 0:
             return gap
         synth.redraw_rows(w, x, bad.tolist(), attempt)
+        _, _, gap[bad] = orc.topk(orc.router_logits(bits(x[torch.from_numpy(bad).to(x.device)]),
+                                                    wr, rb), k)
     raise AssertionError("could not meet the logit-gap precondition")
 
 
@@ -58,7 +73,7 @@ class _DevArray:
 
 def device_view(ptr: int, n: int, dtype) -> torch.Tensor:
     """Zero-copy torch view of n elements at a device address."""
-    typestr = {torch.int32: "<i4", torch.float32: "<f4"}[dtype]
+    typestr = {torch.int32: "<i4", torch.float32: "<f4", torch.int16: "<i2"}[dtype]
     return torch.as_tensor(_DevArray(ptr, n, typestr), device="cuda")
 
 
@@ -93,3 +108,43 @@ def check_y(y_gpu: np.ndarray, y_orc: np.ndarray, tol: float = Y_TOL):
     ratio = err / rms
     assert ratio <= tol, f"max|dy| = {err:.3e}, rms(y) = {rms:.3e}, ratio {ratio:.3e} > {tol}"
     return ratio
+
+
+def caller_routing_buffers(T: int, k: int, E: int):
+    """Zeroed device buffers for every routing output (layouts of
+    moe_routing) and the MoeRouting struct pointing at them."""
+    from bit_grouped_gemm_gb300 import binding as bg
+    max_tiles = (T * k + 127) // 128 + E
+    z = lambda n, dt=torch.int32: torch.zeros(n, dtype=dt, device="cuda")
+    bufs = dict(topk_idx=z(T * k), topk_w=z(T * k, torch.float32), counts=z(E),
+                offsets=z(E + 1), tile_offsets=z(E + 1), perm=z(T * k), inv=z(T * k),
+                block_map=z(max_tiles * 3), num_tiles=z(4), logits=z(T * E, torch.float32))
+    r = bg.MoeRouting(**{n: t.data_ptr() for n, t in bufs.items()})
+    return bufs, r
+
+
+def bf16_ulp(v: np.ndarray) -> np.ndarray:
+    """Spacing of bf16 values at |v| (8 significant bits; normal range)."""
+    a = np.maximum(np.abs(v), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(a)) - 7)
+
+
+def layer_output_from_scratch(plan: int, inv: np.ndarray, rows: np.ndarray, T: int, k: int,
+                              H: int, has_shared: bool) -> np.ndarray:
+    """The block output y of the plan's last layer call for the given token
+    rows, rebuilt from the plan's scratch exactly as the combine adds it: the
+    shared expert's FP32 row, then the k weighted bf16 routed rows in slot
+    order, each addition rounded to FP32 (the fused combine never stores y)."""
+    from bit_grouped_gemm_gb300 import binding as bg
+    d = device_view(bg.moe_debug_buffer(plan, 2), T * k * H, torch.int16).view(T * k, H)
+    pos = torch.from_numpy(inv.reshape(T, k)[rows].astype(np.int64)).cuda()
+    dr = d[pos.reshape(-1)].cpu().numpy().reshape(len(rows), k, H)
+    dr = (dr.view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+    if has_shared:
+        dsh = device_view(bg.moe_debug_buffer(plan, 3), T * H, torch.float32).view(T, H)
+        acc = dsh[torch.from_numpy(np.asarray(rows, np.int64)).cuda()].cpu().numpy().copy()
+    else:
+        acc = np.zeros((len(rows), H), np.float32)
+    for j in range(k):
+        acc = (acc + dr[:, j]).astype(np.float32)
+    return acc

@@ -85,3 +85,18 @@ def test_null_arguments_rejected(lib):
                                           None) == 1
     assert lib.moe_forward_stack(None, None, None, 1, None, 1, 0.0, None) == 1
     assert lib.moe_get_error(None) == 1
+
+
+def test_noalloc_host_checks(lib):
+    """moe_route_noalloc's size limits are checked on the host before any
+    CUDA call: top_k above 32 is unsupported (as for a plan), T above 4096 or
+    more than 512 experts exceed its fixed scratch."""
+    fake = 1 << 20                                   # aligned, never dereferenced
+    r = bg.MoeRouting(*([fake] * 10))
+    call = lambda T, E, k: lib.moe_route_noalloc(fake, T, 2048, fake, None, E, k,
+                                                 ctypes.byref(r), None)
+    assert call(16, 64, 33) == 2                     # MOE_ERR_UNSUPPORTED
+    assert call(4097, 256, 8) == 4                   # MOE_ERR_CAPACITY
+    assert call(16, 520, 8) == 4
+    assert call(0, 256, 8) == 1                      # MOE_ERR_INVALID_ARG
+    assert call(16, 256, 0) == 1

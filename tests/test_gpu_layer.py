@@ -60,6 +60,7 @@ class Case:
 
 
 def make_plan(w: synth.Workload, gemm_path=0, max_tokens=None):
+    """A plan for the workload's shape (capacity: its T, or max_tokens)."""
     sh = w.shape
     d = bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k, sh.group_size,
                      int(sh.has_shared), max_tokens or w.tokens, 128, gemm_path)
@@ -71,7 +72,7 @@ SMALL = synth.MoEShape(hidden=256, inter=256, num_experts=16, top_k=4)
 
 
 @pytest.mark.parametrize("name", ["t128_uniform", "t512_zipf", "t2048_uniform", "t2048_zipf",
-                                  "decode_t1_l40", "decode_t8_l40"])
+                                  "prefill_t4096_l40_zipf", "decode_t1_l40", "decode_t8_l40"])
 def test_route_bit_exact(name):
     """Routing against the oracle; the decode sizes exercise the router's
     GEMV path for batches of at most 16 tokens."""
@@ -127,17 +128,165 @@ def test_layer_parity_full(name, path):
         bg.moe_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("name", ["t2048_uniform", "t2048_zipf"])
-def test_layer_parity_sampled(name):
+@pytest.mark.parametrize("name", ["t2048_uniform", "t2048_zipf", "prefill_t4096_l40_zipf"])
+def test_layer_parity_all_rows(name):
+    """Every output row of a full-size layer against the oracle (layer 0 of
+    the 40-layer stack for the 4096-token workload), so every tile of every
+    expert -- full, partial and the hot experts' many -- is compared."""
     w = WL[name]
     c = Case(w)
     plan = make_plan(w)
     try:
         y = run_layer(c, plan)
-        rng = np.random.default_rng(0)
-        rows = np.sort(rng.choice(w.tokens, size=96, replace=False)).astype(np.int32)
-        orc = c.oracle_layer(rows)
-        parity.check_y(y.double().cpu().numpy()[rows], orc["y"])
+        orc = c.oracle_layer()
+        r = bg.moe_route(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias)
+        g = parity.routing_to_numpy(r, w.tokens, w.shape.top_k, w.shape.num_experts)
+        assert np.array_equal(g["topk_idx"], orc["topk_idx"])
+        parity.check_y(y.double().cpu().numpy(), orc["y"])
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+def _tie_bias(kind: str, E: int) -> np.ndarray:
+    """Router biases that make every token's logits exactly these values
+    (the router weight is zero): ties, signed zeros and NaNs."""
+    nan = np.float32("nan")
+    b = np.full(E, -1.0, np.float32)
+    if kind == "ties":          # ten experts tied at 0.5; the top 8 are the lowest indices
+        b[[3, 9, 17, 40, 41, 100, 130, 200, 201, E - 1]] = 0.5
+        b[[5, 6]] = 0.25
+    elif kind == "signed_zero":  # +0 and -0 tie at the top
+        b[:] = -2.0
+        b[[2, 4, 8, 16, 32, 64, 128, E - 3, E - 2, E - 1]] = [0.0, -0.0] * 5
+    elif kind == "nan":          # four finite experts, the rest NaN: four picks of weight 0
+        b[:] = nan
+        b[[7, 11, 13, 250]] = 1.0
+    elif kind == "all_nan":
+        b[:] = nan
+    return b
+
+
+@pytest.mark.parametrize("T", [5, 100])
+@pytest.mark.parametrize("kind", ["ties", "signed_zero", "nan", "all_nan"])
+def test_routing_ties_nan_signed_zero(T, kind):
+    """Routing edge cases on the GPU against the oracle's top-k: exact ties
+    (the lower expert index wins, in selection and slot order), -0 tying
+    with +0, and NaN logits ranking as -infinity with weight zero. The router
+    weight is zero, so each logit is exactly its bias; the chosen weights are
+    exact binary fractions (or 0, or NaN), so they compare bit for bit. T = 5
+    takes the one-launch decode routing, T = 100 the cooperative one; the
+    allocation-free entry point (separate launches) is checked too. The
+    weights are compared bit for bit after rounding the oracle's fp64
+    weights to the FP32 the GPU stores (the fp64 renormalisation itself can
+    round in the last place: a sum of eight equal terms)."""
+    sh = synth.MoEShape()
+    E, k = sh.num_experts, sh.top_k
+    w = synth.Workload(f"ties{T}", T, 1, "uniform", seed=901 + T, shape=sh)
+    x = synth.tokens_x(w, "cuda")
+    wr = torch.zeros((sh.hidden, E), dtype=torch.bfloat16, device="cuda")
+    bias = _tie_bias(kind, E)
+    rb = torch.from_numpy(bias).cuda()
+    orc = oracle.get()
+    logits = orc.router_logits(parity.bits(x), parity.bits(wr), bias)
+    idx, wts, _ = orc.topk(logits, k)
+    plan = make_plan(w, max_tokens=T)
+    try:
+        outs = [parity.routing_to_numpy(bg.moe_route(plan, x, T, wr, rb), T, k, E)]
+        bufs, r = parity.caller_routing_buffers(T, k, E)
+        bg.moe_route_noalloc(x, T, sh.hidden, wr, rb, E, k, r)
+        outs.append(parity.routing_to_numpy(r, T, k, E))
+        assert bg.moe_route_noalloc_get_error() == 0
+        assert bg.moe_get_error(plan) == 0
+        for g in outs:
+            assert np.array_equal(g["topk_idx"], idx)
+            gw = g["topk_w"]
+            w32 = wts.astype(np.float32)
+            assert np.array_equal(np.isnan(gw), np.isnan(w32))
+            fin = ~np.isnan(w32)
+            assert np.array_equal(gw[fin].view(np.uint32), w32[fin].view(np.uint32))
+            maps = orc.route_maps(g["topk_idx"], E, 128)
+            for key in ("counts", "offsets", "tile_offsets", "perm", "inv", "block_map"):
+                assert np.array_equal(g[key], maps[key]), key
+        if kind == "ties":
+            assert idx[0].tolist() == [3, 9, 17, 40, 41, 100, 130, 200]
+            assert np.all(np.abs(wts - 0.125) <= 1e-15)
+        elif kind == "nan":
+            assert idx[0].tolist() == [7, 11, 13, 250, 0, 1, 2, 3]
+            assert np.all(np.abs(wts[:, :4] - 0.25) <= 1e-15) and np.all(wts[:, 4:] == 0.0)
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T,path", [(128, 1), (4, 2), (4, 1)])
+def test_operand_range_is_flagged(T, path):
+    """Inputs outside the fp16 operand contract of the expert GEMMs latch an
+    error that moe_get_error reports as MOE_ERR_OPERAND_RANGE (6): a token
+    value above 65504 (checked on every call), and a weight set with a scale
+    below 2^-14 (checked the first time a plan sees the set). In-contract
+    inputs report 0, as in every other test of this suite."""
+    w = dataclasses.replace(WL["t128_uniform"], tokens=T)
+    c = Case(w, gap=False)
+    plan = make_plan(w, path)
+    try:
+        run_layer(c, plan)                                  # in contract: status 0
+        x_big = c.x.clone()
+        x_big[T // 2, 17] = 70000.0                         # bf16 70144: saturates in fp16
+        y = torch.empty(c.x.shape, dtype=torch.float32, device="cuda")
+        bg.moe_forward_layer(plan, x_big, T, c.L.router_w, c.L.router_bias, c.L.routed_c,
+                             c.L.shared_c, y)
+        assert bg.moe_get_error(plan) == 6
+        run_layer(c, plan)                                  # cleared; x back in range
+        # a subnormal-in-fp16 scale in a fresh copy of the up matrix's scales
+        up_s = c.L.routed["up"][1].clone()
+        up_s[3, 5, 2] = 1e-6
+        routed = bg.experts(c.L.routed["gate"], (c.L.routed["up"][0], up_s, c.L.routed["up"][2]),
+                            c.L.routed["down"])
+        bg.moe_forward_layer(plan, c.x, T, c.L.router_w, c.L.router_bias, routed, c.L.shared_c, y)
+        torch.cuda.synchronize()
+        assert bg.moe_get_error(plan) == 6
+        # a bias of magnitude 2^11 in the shared expert's down matrix
+        sd_b = c.L.shared["down"][2].clone()
+        sd_b[0, 100, 3] = 2048.0
+        shared = bg.experts(c.L.shared["gate"], c.L.shared["up"],
+                            (c.L.shared["down"][0], c.L.shared["down"][1], sd_b))
+        bg.moe_forward_layer(plan, c.x, T, c.L.router_w, c.L.router_bias, c.L.routed_c, shared, y)
+        assert bg.moe_get_error(plan) == 6
+        assert bg.moe_get_error(plan) == 0
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T", [4, 512])
+def test_no_host_sync_inside_a_layer(T):
+    """A layer call returns while the device is still busy: the stream is
+    held by a kernel that spins for about a second (torch.cuda._sleep), the
+    layer is enqueued behind it, and the stream must still report work
+    pending when the call has returned (a host sync inside the call would
+    have waited for the sleep). Warm calls first, so that one-time work
+    (module loading, tensor maps, the weight range check) is done."""
+    w = dataclasses.replace(WL["t512_zipf"], tokens=T)
+    c = Case(w, gap=False)
+    plan = make_plan(w)
+    try:
+        y = torch.empty(c.x.shape, dtype=torch.float32, device="cuda")
+        xs, xn = c.x.clone(), torch.empty_like(c.x)
+        layers = bg.moe_layers([c.L])
+        for _ in range(2):
+            bg.moe_forward_layer(plan, c.x, T, c.L.router_w, c.L.router_bias, c.L.routed_c,
+                                 c.L.shared_c, y)
+            bg.moe_forward_stack(plan, xs, xn, T, layers, 0.1)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream()
+        for call in ("layer", "stack"):
+            torch.cuda._sleep(2_000_000_000)              # ~1 s of device time
+            if call == "layer":
+                bg.moe_forward_layer(plan, c.x, T, c.L.router_w, c.L.router_bias, c.L.routed_c,
+                                     c.L.shared_c, y)
+            else:
+                bg.moe_forward_stack(plan, xs, xn, T, layers, 0.1)
+            assert not stream.query(), f"{call}: the call waited for the device"
+            torch.cuda.synchronize()
+        assert bg.moe_get_error(plan) == 0
     finally:
         bg.moe_plan_destroy(plan)
 

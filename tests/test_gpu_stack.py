@@ -1,21 +1,32 @@
 """GPU parity of the stacked layers:
-    xn = rmsnorm(x); y = moe(xn); x <- bf16(x + y/sqrt(L))
+    xn = rmsnorm(x); y = moe(xn); x <- bf16(x + y/sqrt(L)); xn <- rmsnorm(x)
 
-The full-size prefill stack (T=4096, 40 layers, Zipf routing, ~18 GB of packed
-weights) runs on the GPU in the launch configuration the benchmark times. The
-oracle follows a sample of tokens through all 40 layers on its own, in fp64,
-from the generator's inputs; no oracle input ever comes from the GPU. At each
-layer the GPU also runs the layer on a copy of its own batch in which the
-sampled rows are replaced by the oracle's normalised inputs (same T, same
-grid, the rest of the batch keeps the GPU's routing context). On those rows:
+The GPU chain runs through exactly the calls the benchmark times (for
+prefill moe_forward_layer_residual per layer, the combine fused with the
+stack update, as moe_forward_stack issues it; for decode the same calls the
+replayed CUDA graph holds). The oracle follows a set of token rows through
+all layers on its own, in fp64, from the generator's inputs; no oracle input
+ever comes from the GPU. At each layer the GPU also runs the layer, with the
+same call, on a copy of its batch in which the followed rows are replaced by
+the oracle's rows (same T, same grid; the rest of the batch keeps the GPU's
+routing context). On those rows:
   * routing indices must equal the oracle's wherever the oracle's 8th/9th
     logit gap is >= 1e-3;
-  * outputs must satisfy max|y_gpu - y_oracle| <= 2e-2 * rms(y_oracle) over
-    the compared rows of the layer.
+  * the layer output y (rebuilt from the plan's scratch exactly as the fused
+    combine adds it) must satisfy max|y_gpu - y_oracle| <= 2e-2 *
+    rms(y_oracle) over the compared rows of the layer;
+  * the updated residual row must be y's update, bf16(x + y/sqrt(L)), to
+    within half a bf16 unit in the last place (plus the FP32 rounding before
+    it), and the next layer's input its RMS norm to within one unit.
 The GPU's own chain is checked at every layer for the invariants any correct
 routing map has.
 
-The decode stack (T = 8, 40 layers) is checked the same way on all 8 rows.
+Rows followed at T = 4096: for layer 0 (whose routing the oracle computes on
+all rows beforehand), the last token of every active expert (so every
+expert's last, partial tile holds a compared row) and the first token of
+every tile of the most loaded expert; every 16th token (so every tile of a
+hot expert holds several, at every layer); and the last 32 tokens. Decode
+batches (T = 1, 4, 8) follow every row.
 """
 import dataclasses
 import os
@@ -55,10 +66,10 @@ def oracle_layer_for_rows(L: stack.DeviceLayer, xn_bits: np.ndarray, sh: synth.M
         qh = np.zeros(tuple(q.shape), np.uint32)
         shh = np.zeros(tuple(s.shape), np.uint16)
         bh = np.zeros(tuple(b.shape), np.uint16)
-        for e in need:
-            qh[e] = parity.words(q[e])
-            shh[e] = parity.bits(s[e])
-            bh[e] = parity.bits(b[e])
+        sel = torch.tensor(need, dtype=torch.int64, device=q.device)
+        qh[need] = parity.words(q[sel])
+        shh[need] = parity.bits(s[sel])
+        bh[need] = parity.bits(b[sel])
         routed[m] = (qh, shh, bh)
     shared = parity.host_set(L.shared) if L.shared is not None else None
     return orc.moe_rows(xn_bits, wr, rb, routed, shared, sh.top_k, sh.group_size,
@@ -69,10 +80,61 @@ def to_dev_bits(b: np.ndarray) -> torch.Tensor:
     return torch.from_numpy(b.view(np.int16).copy()).cuda().view(torch.bfloat16)
 
 
-def run_chain_check(w: synth.Workload, rows: np.ndarray):
+def bits_f64(b: np.ndarray) -> np.ndarray:
+    return parity.bf16_f64(b)
+
+
+def tile_coverage(g: dict, rows_ok: np.ndarray, k: int):
+    """From a routing result: (last tiles of active experts holding a compared
+    row, active experts, tiles of the most loaded expert holding a compared
+    row, its tiles)."""
+    bmap, inv, cnt = g["block_map"], g["inv"], g["counts"]
+    pos = inv.reshape(-1, k)[rows_ok].reshape(-1)
+    starts = bmap[:, 1]
+    tile_of = np.searchsorted(starts, pos, side="right") - 1
+    covered = np.zeros(len(bmap), bool)
+    covered[tile_of] = True
+    last = {}
+    for t, (e, _, _) in enumerate(bmap):
+        last[int(e)] = t
+    n_last = sum(covered[t] for t in last.values())
+    hot = int(np.argmax(cnt))
+    hot_tiles = [t for t, (e, _, _) in enumerate(bmap) if e == hot]
+    return int(n_last), len(last), int(covered[hot_tiles].sum()), len(hot_tiles)
+
+
+def prefill_rows(w: synth.Workload, L0: stack.DeviceLayer) -> np.ndarray:
+    """The token rows the 40-layer prefill chain follows (module docstring)."""
+    orc = oracle.get()
     sh = w.shape
-    T = w.tokens
-    layers = stack.make_layers(w, "cuda")
+    T, k = w.tokens, sh.top_k
+    xn0 = orc.rmsnorm(parity.bits(synth.tokens_x(w, "cpu")))
+    rb = None if L0.router_bias is None else L0.router_bias.cpu().numpy()
+    idx, _, gap = orc.topk(parity.router_logits_mt(orc, xn0, parity.bits(L0.router_w), rb), k)
+    maps = orc.route_maps(idx, sh.num_experts, 128)
+    off, perm, cnt = maps["offsets"], maps["perm"], maps["counts"]
+    rows = set(range(0, T, 16)) | set(range(T - 32, T))
+    for e in np.nonzero(cnt)[0]:
+        # the last token of the expert's last tile whose gap allows comparison
+        first_last_tile = off[e] + 128 * ((cnt[e] - 1) // 128)
+        for p in range(off[e + 1] - 1, first_last_tile - 1, -1):
+            t = perm[p] // k
+            if gap[t] >= parity.GAP_MIN:
+                rows.add(int(t))
+                break
+    hot = int(np.argmax(cnt))
+    for p in range(off[hot], off[hot + 1], 128):
+        rows.add(int(perm[p] // k))
+    return np.array(sorted(rows), np.int32)
+
+
+def run_chain_check(w: synth.Workload, rows: np.ndarray, layers=None):
+    """The chain check of the module docstring; returns per-layer stats
+    (layer, compared rows, y ratio, last tiles covered, active experts, hot
+    tiles covered, hot tiles)."""
+    sh = w.shape
+    T, k, H = w.tokens, sh.top_k, sh.hidden
+    layers = layers if layers is not None else stack.make_layers(w, "cuda")
     plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
                                            sh.group_size, int(sh.has_shared), T), 0)
     alpha = stack.residual_alpha(w.layers)
@@ -81,34 +143,46 @@ def run_chain_check(w: synth.Workload, rows: np.ndarray):
     try:
         x = synth.tokens_x(w, "cuda")
         xn = torch.empty_like(x)
-        y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
-        y_chk = torch.empty_like(y)
-        xo = parity.bits(x)[rows]                    # oracle's own chain
+        xo = parity.bits(x)[rows]                    # the oracle's own chain
         bg.moe_residual_add(plan, x, None, T, 0.0, x, xn)
         rows_t = torch.from_numpy(rows.astype(np.int64)).cuda()
         for li, L in enumerate(layers):
-            # the GPU chain
+            # the GPU chain's routing invariants
             r = bg.moe_route(plan, xn, T, L.router_w, L.router_bias)
-            g = parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)
+            g = parity.routing_to_numpy(r, T, k, sh.num_experts)
             check_route_invariants(g, g["topk_idx"], sh.num_experts, 128)
-            bg.moe_forward_layer(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
-                                 L.shared_c, y)
-            # the same layer on the oracle's inputs for the sampled rows
+            # the layer on the oracle's rows, through the timed call
             xon = orc.rmsnorm(xo)
             xin = xn.clone()
             xin[rows_t] = to_dev_bits(xon)
-            rc = bg.moe_route(plan, xin, T, L.router_w, L.router_bias)
-            gidx = parity.routing_to_numpy(rc, T, sh.top_k, sh.num_experts)["topk_idx"][rows]
-            bg.moe_forward_layer(plan, xin, T, L.router_w, L.router_bias, L.routed_c,
-                                 L.shared_c, y_chk)
+            x_chk = x.clone()
+            x_chk[rows_t] = to_dev_bits(xo)
+            xn_chk = torch.empty_like(x)
+            rc = bg.moe_route(plan, xin, T, L.router_w, L.router_bias)   # the routing pointers
+            bg.moe_forward_layer_residual(plan, xin, T, L.router_w, L.router_bias, L.routed_c,
+                                          L.shared_c, alpha, x_chk, xn_chk)
+            gc = parity.routing_to_numpy(rc, T, k, sh.num_experts)
+            y_gpu = parity.layer_output_from_scratch(plan, gc["inv"], rows, T, k, H,
+                                                     sh.has_shared)
             o = oracle_layer_for_rows(L, xon, sh)
             ok = o["gap"] >= parity.GAP_MIN
-            assert np.array_equal(gidx[ok], o["topk_idx"][ok]), li
-            yg = y_chk.double().cpu().numpy()[rows]
-            ratio = parity.check_y(yg[ok], o["y"][ok])
-            stats.append((li, int(ok.sum()), ratio))
-            # advance both chains
-            bg.moe_residual_add(plan, x, y, T, alpha, x, xn)
+            assert np.array_equal(gc["topk_idx"][rows][ok], o["topk_idx"][ok]), li
+            # (a layer where no followed row has the gap compares no output;
+            # the chains still advance, each with its own routing)
+            ratio = parity.check_y(y_gpu[ok].astype(np.float64), o["y"][ok]) if ok.any() else 0.0
+            # the fused stack update on the same rows
+            xc = bits_f64(parity.bits(x_chk)[rows])
+            want = bits_f64(xo) + np.float64(np.float32(alpha)) * y_gpu.astype(np.float64)
+            slack = 0.5 * parity.bf16_ulp(np.maximum(np.abs(xc), np.abs(want))) * (1 + 2.0 ** -15)
+            assert np.all(np.abs(xc - want) <= slack + 1e-30), li
+            xn_want = bits_f64(orc.rmsnorm(parity.bits(x_chk)[rows]))
+            xn_got = bits_f64(parity.bits(xn_chk)[rows])
+            assert np.all(np.abs(xn_got - xn_want) <= parity.bf16_ulp(xn_want) + 1e-30), li
+            cov = tile_coverage(gc, rows[ok], k) if ok.any() else (0, 0, 0, 0)
+            stats.append((li, int(ok.sum()), ratio) + cov)
+            # advance both chains: the GPU by the timed call, the oracle by its own update
+            bg.moe_forward_layer_residual(plan, xn, T, L.router_w, L.router_bias, L.routed_c,
+                                          L.shared_c, alpha, x, xn)
             xo = orc.residual(xo, o["y"], alpha)
         assert bg.moe_get_error(plan) == 0
         assert np.isfinite(x.float().cpu().numpy()).all()
@@ -117,17 +191,110 @@ def run_chain_check(w: synth.Workload, rows: np.ndarray):
         bg.moe_plan_destroy(plan)
 
 
-def test_prefill_stack_t4096_l40_sampled():
+def test_prefill_stack_t4096_l40_chain():
     w = synth.standard_workloads()["prefill_t4096_l40_zipf"]
-    rows = np.array([0, 1, 777, 2048, 3333, 4095], np.int32)
-    stats = run_chain_check(w, rows)
-    assert sum(n for _, n, _ in stats) >= 0.9 * len(rows) * w.layers, stats
+    layers = stack.make_layers(w, "cuda")
+    rows = prefill_rows(w, layers[0])
+    assert len(rows) >= 256
+    stats = run_chain_check(w, rows, layers)
+    print("layer, compared rows, y ratio, last tiles covered/active, hot tiles covered/all")
+    for st in stats:
+        print(f"  {st[0]:2d} {st[1]:4d} {st[2]:.2e} {st[3]}/{st[4]} {st[5]}/{st[6]}")
+    assert sum(st[1] for st in stats) >= 0.9 * len(rows) * w.layers, stats
+    # layer 0: every active expert's last tile holds a compared row
+    assert stats[0][3] >= stats[0][4] - 2, stats[0]
+    # every layer: every tile of the most loaded expert holds a compared row
+    assert all(st[5] == st[6] for st in stats), stats
 
 
-def test_decode_stack_t8_l40():
-    w = synth.standard_workloads()["decode_t8_l40"]
-    stats = run_chain_check(w, np.arange(8, dtype=np.int32))
-    assert sum(n for _, n, _ in stats) >= 0.9 * 8 * w.layers, stats
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_decode_stack_l40_chain(T):
+    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    stats = run_chain_check(w, np.arange(T, dtype=np.int32))
+    assert sum(st[1] for st in stats) >= 0.9 * T * w.layers, stats
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_decode_graph_replay_matches_eager(T):
+    """The decode benchmark replays the whole 40-layer step from one CUDA
+    graph; the replay gives the bits of the same calls issued eagerly (which
+    the chain test above compares with the oracle)."""
+    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
+    try:
+        pool = synth.decode_pool(w, 4, "cuda")
+        alpha = stack.residual_alpha(w.layers)
+        x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
+        xn = torch.empty_like(x)
+        y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+        x.copy_(pool[0])
+        stack.run_stack(plan, x, xn, layers, T, y, alpha)       # warm (one-time work)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, capture_error_mode="thread_local"):
+            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        for i in (1, 2, 3):
+            x.copy_(pool[i])
+            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            torch.cuda.synchronize()
+            eager = x.view(torch.int16).cpu().numpy().copy()
+            x.copy_(pool[i])
+            graph.replay()
+            torch.cuda.synchronize()
+            assert np.array_equal(x.view(torch.int16).cpu().numpy(), eager), i
+        assert bg.moe_get_error(plan) == 0
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("chunk", [256])
+def test_chunked_prefill_parity(chunk):
+    """moe_forward_stack on a prompt longer than the plan's capacity (600
+    tokens in chunks of 256, 256 and a ragged 88) against the oracle, layer by
+    layer over 3 layers: at each layer the GPU runs moe_forward_stack for that
+    one layer on its batch with the followed rows replaced by the oracle's
+    residual rows (rows in every chunk, and every row of the last one), and
+    the updated rows must satisfy |x_gpu - x_oracle| <= sqrt(1/L) * 2e-2 *
+    rms(y_oracle) + one bf16 unit (both sides round x + y/sqrt(L) once to
+    bf16 after outputs within the layer tolerance)."""
+    T = 600
+    w = dataclasses.replace(synth.standard_workloads()["prefill_t4096_l40_zipf"], tokens=T,
+                            layers=3)
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    alpha = stack.residual_alpha(40)
+    rows = np.array(sorted({0, 1, 100, 255, 256, 300, 511} | set(range(512, T))), np.int32)
+    rows_t = torch.from_numpy(rows.astype(np.int64)).cuda()
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), chunk), 0)
+    orc = oracle.get()
+    try:
+        x = synth.tokens_x(w, "cuda")
+        xn = torch.empty((chunk, sh.hidden), dtype=x.dtype, device="cuda")
+        xo = parity.bits(x)[rows]
+        for li, L in enumerate(layers):
+            one = bg.moe_layers([L])
+            x_chk = x.clone()
+            x_chk[rows_t] = to_dev_bits(xo)
+            bg.moe_forward_stack(plan, x_chk, xn, T, one, alpha)
+            o = oracle_layer_for_rows(L, orc.rmsnorm(xo), sh)
+            xo_next = orc.residual(xo, o["y"], alpha)
+            ok = o["gap"] >= parity.GAP_MIN
+            got = bits_f64(parity.bits(x_chk)[rows])[ok]
+            want = bits_f64(xo_next)[ok]
+            rms = float(np.sqrt(np.mean(o["y"][ok] ** 2)))
+            bound = alpha * parity.Y_TOL * rms + parity.bf16_ulp(np.maximum(np.abs(got),
+                                                                            np.abs(want)))
+            assert np.all(np.abs(got - want) <= bound), li
+            assert ok.sum() >= 0.9 * len(rows)
+            bg.moe_forward_stack(plan, x, xn, T, one, alpha)        # the GPU's own chain
+            xo = xo_next
+        assert bg.moe_get_error(plan) == 0
+    finally:
+        bg.moe_plan_destroy(plan)
 
 
 @pytest.mark.gpu

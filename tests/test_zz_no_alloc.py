@@ -9,8 +9,6 @@ not), runs two calls in a row with different inputs, and requires the same
 routing as the plan-based entry point: integer arrays exactly, top-k weights
 within the 1e-5 tolerance of the other routing tests.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -30,13 +28,7 @@ def built():
 
 
 def caller_buffers(T, k, E):
-    max_tiles = (T * k + 127) // 128 + E
-    z = lambda n, dt=torch.int32: torch.zeros(n, dtype=dt, device="cuda")
-    bufs = dict(topk_idx=z(T * k), topk_w=z(T * k, torch.float32), counts=z(E),
-                offsets=z(E + 1), tile_offsets=z(E + 1), perm=z(T * k), inv=z(T * k),
-                block_map=z(max_tiles * 3), num_tiles=z(4), logits=z(T * E, torch.float32))
-    r = bg.MoeRouting(**{n: t.data_ptr() for n, t in bufs.items()})
-    return bufs, r
+    return parity.caller_routing_buffers(T, k, E)
 
 
 @pytest.mark.parametrize("name", ["t512_zipf", "t128_uniform"])
@@ -114,3 +106,25 @@ def test_fused_routing_matches_separate_launches(T, H, E, k, routing):
             assert got["num_tiles"] == ref["num_tiles"]
     finally:
         bg.moe_plan_destroy(plan)
+
+
+def test_noalloc_device_timeout_is_reported_and_cleared():
+    """The allocation-free routing has its own device error word (it has no
+    plan): a bounded wait that runs out is reported by
+    moe_route_noalloc_get_error, which also clears it, and routing still
+    works afterwards. The wait is made to run out by a kernel whose barrier
+    nothing signals (20 ms limit): no fault, no hang."""
+    assert bg.moe_route_noalloc_get_error() == 0
+    bg.moe_route_noalloc_debug_wait_timeout(20000)
+    assert bg.moe_route_noalloc_get_error() == 5           # MOE_ERR_DEVICE_TIMEOUT
+    assert bg.moe_route_noalloc_get_error() == 0           # cleared
+    w = synth.standard_workloads()["t128_uniform"]
+    sh = w.shape
+    L = stack.make_layer(w, 0, "cuda")
+    x = synth.tokens_x(w, "cuda")
+    _, r = caller_buffers(w.tokens, sh.top_k, sh.num_experts)
+    bg.moe_route_noalloc(x, w.tokens, sh.hidden, L.router_w, L.router_bias, sh.num_experts,
+                         sh.top_k, r)
+    got = parity.routing_to_numpy(r, w.tokens, sh.top_k, sh.num_experts)
+    assert got["offsets"][-1] == w.tokens * sh.top_k
+    assert bg.moe_route_noalloc_get_error() == 0
