@@ -477,15 +477,15 @@ def measure_decode(w, layers, local, pg, ws, steps, warmup):
         pool = synth.decode_pool(w, 64, "cuda")
         x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
         xn = torch.empty_like(x)
-        y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+        arr = bg.moe_layers(layers)
         for i in range(3):
             x.copy_(pool[i])
-            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
         torch.cuda.synchronize()
         assert bg.moe_get_error(plan) == 0
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
         torch.cuda.synchronize()
         stream = torch.cuda.current_stream()
         for i in range(warmup):
@@ -520,7 +520,10 @@ def measure_decode(w, layers, local, pg, ws, steps, warmup):
                              "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
                              "algorithmic_bytes_per_step": step_bytes,
                              "distinct_routed_experts_per_layer": experts_per_layer},
-                "graph": "whole step replayed from one CUDA graph; fresh batch per step",
+                "graph": "whole step (moe_forward_stack) replayed from one CUDA graph; fresh "
+                         "batch per step",
+                "path": {1: "tensor-core", 2: "small-M", 3: "fused decode layer"}.get(
+                    bg.moe_last_gemm_path(plan)),
                 "clocks": clk.summary()}
     finally:
         bg.moe_plan_destroy(plan)
@@ -530,8 +533,10 @@ def decode_step_bytes(w, layers, plan, pool, samples=8):
     """Algorithmic HBM bytes of one decode step: for every layer, the packed
     weights, scales and biases of each distinct routed expert the layer's
     routing selects plus the shared expert's, and the router weight. Counted
-    by running the stack layer by layer (untimed) on `samples` pool batches
-    and averaging."""
+    by running the timed call (moe_forward_stack) one layer at a time
+    (untimed) on `samples` pool batches, reading each layer's routing from
+    the plan, and averaging."""
+    import numpy as np
     import torch
     from bit_grouped_gemm_gb300 import binding as bg, stack
     from tests import parity
@@ -542,18 +547,17 @@ def decode_step_bytes(w, layers, plan, pool, samples=8):
     alpha = stack.residual_alpha(w.layers)
     x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
     xn = torch.empty_like(x)
-    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+    x.copy_(pool[0])
+    r = bg.moe_route(plan, x, T, layers[0].router_w, layers[0].router_bias)   # array addresses
+    idx_view = parity.device_view(r.topk_idx, T * sh.top_k, torch.int32)
     total, experts = 0.0, 0
     for i in range(samples):
         x.copy_(pool[i])
-        bg.moe_residual_add(plan, x, None, T, 0.0, x, xn)
         for L in layers:
-            r = bg.moe_route(plan, xn, T, L.router_w, L.router_bias)
-            active = int((parity.routing_to_numpy(r, T, sh.top_k, sh.num_experts)["counts"] > 0).sum())
+            bg.moe_forward_stack(plan, x, xn, T, bg.moe_layers([L]), alpha)
+            active = len(np.unique(idx_view.cpu().numpy()))
             experts += active
             total += (active + int(sh.has_shared)) * per_expert + router
-            bg.moe_grouped_w4_ffn(plan, xn, T, r, L.routed_c, L.shared_c, y)
-            bg.moe_residual_add(plan, x, y, T, alpha, x, xn)
     torch.cuda.synchronize()
     return total / samples, experts / samples / w.layers
 
@@ -573,15 +577,15 @@ def run_decode(args, w, ws, rank, local, pg):
     pool = synth.decode_pool(w, 64, "cuda")
     x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
     xn = torch.empty_like(x)
-    y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+    arr = bg.moe_layers(layers)
     for i in range(3):
         x.copy_(pool[i])
-        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
     torch.cuda.synchronize()
     assert bg.moe_get_error(plan) == 0
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
@@ -612,7 +616,7 @@ def run_decode(args, w, ws, rank, local, pg):
     bg.moe_read_timing(plan)
     for i in range(min(args.steps, 50)):
         x.copy_(pool[i % pool.shape[0]])
-        stack.run_stack(plan, x, xn, layers, T, y, alpha)
+        bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
     torch.cuda.synchronize()
     kt = bg.moe_read_timing(plan)
     bg.moe_enable_timing(plan, False)

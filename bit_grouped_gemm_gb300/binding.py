@@ -21,7 +21,7 @@ STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED",
                 3: "MOE_ERR_CUDA", 4: "MOE_ERR_CAPACITY", 5: "MOE_ERR_DEVICE_TIMEOUT",
                 6: "MOE_ERR_OPERAND_RANGE"}
 KERNEL_KINDS = ("router", "scan", "scatter", "gather", "gate_up_gemm", "down_gemm",
-                "combine", "residual", "topk")
+                "combine", "residual", "topk", "decode_layer")
 
 
 class MoeError(RuntimeError):

@@ -1,0 +1,996 @@
+// decode_fused.cu -- one mixture-of-experts layer of a decode-sized batch
+// (T <= 8 tokens) in one cooperative launch.
+//
+// The block of "Perplexity libera Lily, un motor de IA que supera a MLX-LM en
+// Apple Silicon" (diariobitcoin.com): router and top-8 of section "Qwen3.6
+// combina tres cargas de trabajo", the grouped 4-bit GEMM with on-chip
+// dequantisation and FP32 accumulation of section "Las optimizaciones en el
+// prefill", in the regime of section "El decode busca mover menos datos",
+// where a layer moves its selected experts' packed bytes once and the time
+// between dependent steps, not arithmetic, decides the speed.
+//
+// The general path runs a decode layer as four dependent launches (routing,
+// gate/up, down, combine), each paying a launch boundary and one or two
+// dependent round trips through L2. Here one persistent CTA per SM does the
+// whole layer, with two grid barriers (arrival counter in device memory,
+// bounded waits):
+//   1. every CTA reads the residual rows x, computes their RMS norm and the
+//      normalised rows xn = bf16(x / rms(x)) (kept in shared memory as the
+//      fp16 MMA operand), and router CTA c computes the logits of its
+//      experts (router weight slice copied before the previous launch ends);
+//   -- barrier 1 (all logits written) --
+//   2. every CTA selects each token's top-k (the same warp top-k as the
+//      routing kernels, so every CTA holds the same routing) and numbers the
+//      active experts in ascending order: slot 0 the shared expert, then one
+//      slot per selected routed expert with its list of tokens;
+//   3. gate/up units (16 gate + 16 up rows of one slot's expert) are dealt to
+//      CTAs round-robin; their packed rows arrive by TMA (3D boxes, 128-byte
+//      swizzle: one request per matrix) into a ring of shared-memory buffers,
+//      and the shared expert's first unit is fetched before the previous
+//      launch ends. mma.sync with the exact affine split
+//          sum_k w_k x_k = s sum_k (1024+q_k) x_k + (b - 1024 s) sum_k x_k
+//      per group of 64, split K over the 8 warps, SwiGLU in FP32, activations
+//      stored as fp16 rows per (slot, token);
+//   -- barrier 2 (all activations written) --
+//   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
+//      those 16 down rows (fetched into the ring while step 3 ran) by the
+//      slot's activation rows, then forms
+//          y[t] = shared[t] + sum_j w[t][j] * expert_j[t]   (FP32, j in rank order)
+//      and updates x[t] = bf16(x[t] + alpha * y[t]) in place.
+// The next layer's launch (programmatic dependent launch) is the barrier
+// between layers. Every wait is bounded: a CTA that gives up latches the
+// error word, lets its own copies land and exits.
+#include "moe_common.cuh"
+#include "topk.cuh"
+
+namespace moe {
+namespace dec {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = 8;
+constexpr int kMaxT = 8;            // tokens
+constexpr int kMaxSlots = 80;       // shared + distinct routed experts
+constexpr int kRu = 16;             // gate rows (and up rows) per unit
+constexpr int kDn = 16;             // down rows (output columns) per CTA
+constexpr int kSlotsPerChunk = 8;   // down slabs per ring buffer (one per warp)
+constexpr int kRing = 4;            // shared-memory slab buffers
+constexpr int kRBoxE = 8;           // router weight columns per TMA box (16-byte rows)
+constexpr int kIssuer = 224;        // the thread that issues the ring's copies (warp 7, lane 0)
+constexpr int kRedStride = 9;       // floats per (warp, lane) in the split-K reduction (padded)
+constexpr int kRBox = 256;          // router weight rows per TMA box
+
+struct Params {
+  int T, H, I, E, k, has_shared;
+  float alpha, eps;
+  int n_dn;                  // CTAs that own output columns (H / kDn)
+  uint16_t* x;               // residual rows bf16 [T][H], updated in place
+  const uint16_t* wr;        // router weight bf16 [H][E]
+  const float* rbias;        // [E] or null
+  W4Dev gate, up, down, sgate, sup, sdown;   // scales and biases (words via the maps)
+  CUtensorMap mg, mu, md, msg, msu, msd;     // packed words, 3D boxes (32 words, rows, K/256)
+  CUtensorMap mr;            // router weight bf16 [H][E], boxes of 8 experts x 256 rows
+  float* logits;             // [T][E]
+  uint16_t* act;             // [rows][I] fp16, K order perm8 (row = slot offset + token)
+  int32_t* topk_idx;         // [T][k] (written by CTA 0)
+  float* topk_w;             // [T][k]
+  float* y_out;              // [T][H] FP32 block output, or null
+  const uint16_t* next_wr;   // the next layer's router weight and shared expert (L2
+  W4Dev next_sgate, next_sup, next_sdown;   // prefetch during step 4), or null
+  unsigned* bar;             // grid-barrier arrival counter, 0 at launch
+  DevErr err;
+};
+
+// Byte offsets of the dynamic shared memory (from a 1024-aligned base).
+struct Smem {
+  uint32_t slab, xw, xstride, xg, wr, red, total, dsum_cap;
+};
+
+__host__ __device__ inline uint32_t align_u(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// The router slice (H x 8 bf16: the 16-byte box holding this CTA's columns)
+// lives in the last ring buffer, which the ring does not use before the
+// routing is known.
+__host__ __device__ inline Smem smem_layout(int H, int I) {
+  Smem L;
+  const uint32_t gu = 2u * kRu * (H / 2) + 4u * kRu * (H / 64) * 2;
+  const uint32_t dn = kSlotsPerChunk * (kDn * (I / 2) + 2u * kDn * (I / 64) * 2);
+  L.slab = align_u(gu > dn ? gu : dn, 1024);
+  uint32_t o = kRing * L.slab;
+  L.xw = o;
+  L.xstride = H / 2 + 1;                       // words per token row (padded)
+  o += (kMaxT + 1) * L.xstride * 4;            // + one zero row
+  L.dsum_cap = (kMaxT + 1) * L.xstride * 4;    // the down pass reuses the token rows
+  o = align_u(o, 16);
+  L.xg = o;
+  o += (kMaxT + 1) * (H / 64) * 4;
+  o = align_u(o, 16);
+  L.wr = (kRing - 1) * L.slab;
+  L.red = o;
+  o += 2 * kWarps * 32 * kRedStride * 4;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier: every CTA adds one arrival, then waits (bounded) until the
+// counter reaches `target`. Returns false on timeout (error latched).
+__device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, int site,
+                             int* flag_s) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(bar, 1u);
+    int ok = 1;
+    if (ld_acquire_u32(bar) < target) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (ld_acquire_u32(bar) < target) {
+        __nanosleep(32);
+        if (globaltimer_ns() - t0 > err.limit_ns) {
+          report_timeout(err, site);
+          ok = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *flag_s = ok;
+  }
+  __syncthreads();
+  return *flag_s != 0;
+}
+
+__device__ __forceinline__ uint2 lds_v2(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+
+// Byte offset, inside a 3D box of (32 words) x (rows) x (K/256 chunks) with
+// the 128-byte swizzle, of the two packed words 8 j + 2 c and 8 j + 2 c + 1 of
+// row y (group j of 64 K): chunk j / 4, 16-byte piece 2 (j % 4) + c / 2
+// stored at piece ^ (y % 8), half c % 2 of it.
+__device__ __forceinline__ uint32_t qoff(int y, int j, int c, int rows) {
+  const int z = j >> 2, piece = 2 * (j & 3) + (c >> 1);
+  return (uint32_t)((z * rows + y) * 128 + ((piece ^ (y & 7)) << 4) + ((c & 1) << 3));
+}
+
+#ifdef MOE_DEC_TRACE
+// Profiling build only: %globaltimer at the phase boundaries of every CTA of
+// the last launch (read with moe_debug_dec_trace).
+__device__ unsigned long long g_dec_trace[256][16];
+#define DEC_TRACE(i) \
+  if (threadIdx.x == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][(i)] = globaltimer_ns()
+#else
+#define DEC_TRACE(i)
+#endif
+
+// Reduce-scatter of N partial sums over the 32 lanes of a warp by halving
+// exchanges: for N >= 32 lane l ends with the sums of values l N/32 ..
+// (l+1) N/32 - 1 in v[0 ..]; for N < 32 every lane holds the sum of value
+// (lane * N) / 32 in v[0].
+template <int N>
+__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
+  int n = N;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const bool up = (lane & o) != 0;
+    if (n >= 2) {
+#pragma unroll
+      for (int i = 0; i < N / 2; ++i)
+        if (i < n / 2) {
+          const float send = up ? v[i] : v[i + n / 2];
+          const float keep = up ? v[i + n / 2] : v[i];
+          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+      n >>= 1;
+    } else {
+      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+    }
+  }
+}
+
+// Exclusive scan of one int per thread over the CTA; *total gets the sum.
+__device__ __forceinline__ int block_excl_scan_i(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int inc = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += n;
+  }
+  if (lane == 31) warp_sums[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    const int ws = lane < nw ? warp_sums[lane] : 0;
+    int wi = ws;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += n;
+    }
+    if (lane < nw) warp_sums[lane] = wi - ws;
+    if (lane == 31) *total = wi;
+  }
+  __syncthreads();
+  const int r = inc - v + warp_sums[warp];
+  __syncthreads();
+  return r;
+}
+
+template <int VPL, int EPC>   // top-k values per lane; router experts per CTA
+__global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ __align__(8) uint64_t wbar;       // router slice landed
+  __shared__ int idx_s[kMaxT][32];
+  __shared__ float w_s[kMaxT][32];
+  __shared__ int sc_s[kMaxT][32];              // slot * 16 + column of (token, rank)
+  __shared__ unsigned tmask_s[512];            // per expert: tokens that selected it
+  __shared__ int slot_of_s[512];
+  __shared__ int slot_e[kMaxSlots], cnt_s[kMaxSlots], soff_s[kMaxSlots];
+  __shared__ int tok_s[kMaxSlots][kMaxT];
+  __shared__ float ss_w[kWarps][kMaxT];
+  __shared__ float pr_w[kWarps][kMaxT * EPC];
+  __shared__ float x_s[kMaxT][kDn];
+  __shared__ int nslots_s, flag_s, abort_s;
+
+  const int H = p.H, I = p.I, E = p.E, T = p.T, k = p.k;
+  const int G = H / 64, GI = I / 64;
+  const Smem L = smem_layout(H, I);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, c = lane & 3;
+  const int cta = blockIdx.x, ncta = gridDim.x;
+  const uint32_t sbase = smem_u32(smem);
+  uint32_t* xw = reinterpret_cast<uint32_t*>(smem + L.xw);
+  float* xg = reinterpret_cast<float*>(smem + L.xg);
+  const uint16_t* wrs = reinterpret_cast<const uint16_t*>(smem + L.wr);
+  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.slab);   // xn bf16 [T][H] (ring buffer 1)
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  const int upe = I / kRu;                     // gate/up units per slot
+  const uint32_t gu_q = (uint32_t)kRu * (H / 2), gu_s = (uint32_t)kRu * G * 2;
+  const uint32_t dn_q = (uint32_t)kDn * (I / 2), dn_s = (uint32_t)kDn * GI * 2;
+  const int e0 = cta * EPC;                    // this CTA's router columns [e0, e0 + EPC)
+  const bool router_cta = e0 < E;
+  const int ebox = e0 & ~(kRBoxE - 1), ecol = e0 - ebox;   // the 16-byte box holding them
+
+#ifdef MOE_DEC_TRACE
+  unsigned long long tr_wait, tr_comp, tr_mark;
+#endif
+  DEC_TRACE(0);
+  // ------------------------------------------------ prologue (weights only)
+  if (tid == 0) {
+    for (int b = 0; b < kRing; ++b) mbar_init(&full[b], 1);
+    mbar_init(&wbar, 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&p.mg);
+    tma_prefetch_desc(&p.mu);
+    tma_prefetch_desc(&p.md);
+    if (p.has_shared) {
+      tma_prefetch_desc(&p.msg);
+      tma_prefetch_desc(&p.msu);
+      tma_prefetch_desc(&p.msd);
+    }
+    abort_s = 0;
+    if (router_cta) {   // the router slice [H][8] by TMA, H / 256 boxes
+      mbar_arrive_expect_tx(&wbar, (uint32_t)H * kRBoxE * 2);
+      for (int y = 0; y < H; y += kRBox)
+        tma_load_2d(smem + L.wr + (size_t)y * kRBoxE * 2, &p.mr, ebox, y, &wbar);
+    }
+  }
+  __syncthreads();
+
+  // The ring: item i (gate/up units first, then down chunks) goes to buffer
+  // i % kRing; one elected thread issues its copies when the buffer is free.
+  int n_units = 0, n_gu = 0, n_dc = 0;   // set once the routing is known
+  int issued = 0;                        // items issued so far (thread 0), a prefix
+  auto issue = [&](int i) {
+    const int b = i % kRing;
+    issued = i + 1;
+    uint8_t* buf = smem + (size_t)b * L.slab;
+    if (i < n_gu) {
+      const int u = cta + i * ncta, s = u / upe, r = u - s * upe;
+      const bool sh = p.has_shared && s == 0;
+      const int row0 = (sh ? 0 : slot_e[s] * I) + kRu * r;
+      const W4Dev& wg = sh ? p.sgate : p.gate;
+      const W4Dev& wu = sh ? p.sup : p.up;
+      mbar_arrive_expect_tx(&full[b], 2 * gu_q + 4 * gu_s);
+      tma_load_3d(buf, sh ? &p.msg : &p.mg, 0, row0, 0, &full[b]);
+      tma_load_3d(buf + gu_q, sh ? &p.msu : &p.mu, 0, row0, 0, &full[b]);
+      bulk_load(buf + 2 * gu_q, wg.s + (size_t)row0 * G, gu_s, &full[b]);
+      bulk_load(buf + 2 * gu_q + gu_s, wg.b + (size_t)row0 * G, gu_s, &full[b]);
+      bulk_load(buf + 2 * gu_q + 2 * gu_s, wu.s + (size_t)row0 * G, gu_s, &full[b]);
+      bulk_load(buf + 2 * gu_q + 3 * gu_s, wu.b + (size_t)row0 * G, gu_s, &full[b]);
+    } else {
+      const int ch = i - n_gu, s0 = kSlotsPerChunk * ch;
+      const int ns = min(kSlotsPerChunk, nslots_s - s0);
+      mbar_arrive_expect_tx(&full[b], (uint32_t)ns * (dn_q + 2 * dn_s));
+      for (int q = 0; q < ns; ++q) {
+        const int s = s0 + q;
+        const bool sh = p.has_shared && s == 0;
+        const int row0 = (sh ? 0 : slot_e[s] * H) + kDn * cta;
+        const W4Dev& wd = sh ? p.sdown : p.down;
+        tma_load_3d(buf + q * dn_q, sh ? &p.msd : &p.md, 0, row0, 0, &full[b]);
+        bulk_load(buf + kSlotsPerChunk * dn_q + q * dn_s, wd.s + (size_t)row0 * GI, dn_s, &full[b]);
+        bulk_load(buf + kSlotsPerChunk * (dn_q + dn_s) + q * dn_s, wd.b + (size_t)row0 * GI, dn_s,
+                  &full[b]);
+      }
+    }
+  };
+  // The shared expert's units come first and need no routing: a CTA whose
+  // first unit is one starts its copy now (slot 0 is always the shared one).
+  const bool early0 = p.has_shared && cta < upe;
+  if (early0 && tid == kIssuer) {
+    n_gu = 1;
+    issue(0);
+  }
+
+  DEC_TRACE(1);
+  pdl_begin();   // x and everything below come from the previous launch
+  DEC_TRACE(2);
+
+  // ------------------------------------------- 1. norms, operand rows, router
+  for (int e = tid; e < E; e += kThreads) tmask_s[e] = 0u;
+  const int pieces = H / 8;                    // 8 hidden values per piece, <= 2 per thread
+  // this CTA's output columns of x (only this CTA writes them), with the rows
+  const bool own_x = cta < p.n_dn && tid < T * kDn;
+  const float xo = own_x ? bf16_to_f32(p.x[(size_t)(tid / kDn) * H + kDn * cta + tid % kDn]) : 0.f;
+  uint4 xv4[2][kMaxT];                         // this thread's pieces of every token row
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int pc = tid + it * kThreads;
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t)
+      xv4[it][t] = (pc < pieces && t < T)
+                       ? *reinterpret_cast<const uint4*>(p.x + (size_t)t * H + 8 * pc)
+                       : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float ss[kMaxT];
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    ss[t] = 0.f;
+#pragma unroll
+    for (int it = 0; it < 2; ++it) {
+      const uint32_t wv[4] = {xv4[it][t].x, xv4[it][t].y, xv4[it][t].z, xv4[it][t].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        ss[t] = fmaf(bf16_lo(wv[i]), bf16_lo(wv[i]), ss[t]);
+        ss[t] = fmaf(bf16_hi(wv[i]), bf16_hi(wv[i]), ss[t]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t)
+    if (t < T) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
+      if (lane == 0) ss_w[warp][t] = ss[t];
+    }
+  if (own_x) x_s[tid / kDn][tid % kDn] = xo;
+  __syncthreads();
+  float rinv[kMaxT];
+#pragma unroll
+  for (int t = 0; t < kMaxT; ++t) {
+    float tot = 0.f;
+    if (t < T)
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) tot += ss_w[w][t];
+    rinv[t] = 1.0f / sqrtf(tot / (float)H + p.eps);
+  }
+  if (router_cta && !mbar_wait_drain(&wbar, 0, p.err.limit_ns)) {
+    if (lane == 0) report_timeout(p.err, 44);
+    abort_s = 1;
+  }
+  // xn = bf16(x * rinv): fp16 operand rows (perm8 K order) and their group
+  // sums; router partial sums over this thread's hidden indices
+  float pr[kMaxT * EPC];
+#pragma unroll
+  for (int q = 0; q < kMaxT * EPC; ++q) pr[q] = 0.f;
+  uint32_t over = 0u;
+#pragma unroll
+  for (int it = 0; it < 2; ++it) {
+    const int pc = tid + it * kThreads;
+    if (pc >= pieces) continue;   // (uniform over each group of 8 lanes)
+#pragma unroll
+    for (int t = 0; t < kMaxT; ++t) {
+      if (t >= T) continue;
+      const uint32_t wv[4] = {xv4[it][t].x, xv4[it][t].y, xv4[it][t].z, xv4[it][t].w};
+      uint32_t nb[4];   // xn as bf16 pairs
+#pragma unroll
+      for (int i = 0; i < 4; ++i) nb[i] = pack_bf16x2(bf16_lo(wv[i]) * rinv[t], bf16_hi(wv[i]) * rinv[t]);
+      over |= bf16x2_f16_overflow(nb[0]) | bf16x2_f16_overflow(nb[1]) | bf16x2_f16_overflow(nb[2]) |
+              bf16x2_f16_overflow(nb[3]);
+      if (router_cta)   // xn rows as bf16 for the router (ring buffer 1, idle until routing)
+        *reinterpret_cast<uint4*>(xb + (size_t)t * H + 8 * pc) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
+      const uint4 o = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(nb[0]), bf16x2_to_f16x2_sat(nb[1]),
+                                                bf16x2_to_f16x2_sat(nb[2]), bf16x2_to_f16x2_sat(nb[3])));
+      uint32_t* dst = xw + t * L.xstride + 4 * pc;
+      dst[0] = o.x;
+      dst[1] = o.y;
+      dst[2] = o.z;
+      dst[3] = o.w;
+      float gs = f16_lo(o.x) + f16_hi(o.x) + f16_lo(o.y) + f16_hi(o.y) + f16_lo(o.z) + f16_hi(o.z) +
+                 f16_lo(o.w) + f16_hi(o.w);
+      // group of 64 = 8 pieces = 8 adjacent lanes
+      gs += __shfl_xor_sync(0xffffffffu, gs, 1);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 2);
+      gs += __shfl_xor_sync(0xffffffffu, gs, 4);
+      if ((lane & 7) == 0) xg[t * G + pc / 8] = gs;
+    }
+  }
+  report_range_warp(p.err, over != 0u);
+  if (router_cta) {
+    // router partials: thread tid takes hidden rows tid, tid + 256, ... so
+    // that a warp reads consecutive rows of the weight slice and of xn
+    __syncthreads();
+    for (int h = tid; h < H; h += kThreads) {
+      const uint16_t* wrow = wrs + (size_t)h * kRBoxE + ecol;
+      float wv[EPC];
+#pragma unroll
+      for (int q = 0; q < EPC / 2; ++q) {
+        const uint32_t w2 = reinterpret_cast<const uint32_t*>(wrow)[q];
+        wv[2 * q] = bf16_lo(w2);
+        wv[2 * q + 1] = bf16_hi(w2);
+      }
+#pragma unroll
+      for (int t = 0; t < kMaxT; ++t)
+        if (t < T) {
+          const float xv = bf16_to_f32(xb[(size_t)t * H + h]);
+#pragma unroll
+          for (int q = 0; q < EPC; ++q) pr[t * EPC + q] = fmaf(xv, wv[q], pr[t * EPC + q]);
+        }
+    }
+  }
+  // the zero token row (columns of a tile past its tokens)
+  for (int i = tid; i < (int)L.xstride; i += kThreads) xw[kMaxT * L.xstride + i] = 0u;
+  for (int i = tid; i < G; i += kThreads) xg[kMaxT * G + i] = 0.f;
+  if (router_cta) {
+    // the warp's sums of the kMaxT * EPC partials, scattered over its lanes
+    warp_reduce_scatter<kMaxT * EPC>(pr, lane);
+    constexpr int kN = kMaxT * EPC;
+    if (kN >= 32) {
+#pragma unroll
+      for (int i = 0; i < (kN >= 32 ? kN / 32 : 1); ++i) pr_w[warp][lane * (kN / 32) + i] = pr[i];
+    } else if ((lane & (32 / kN - 1)) == 0) {
+      pr_w[warp][(lane * kN) / 32] = pr[0];
+    }
+  }
+  __syncthreads();
+  if (router_cta && tid < T * EPC) {
+    const int t = tid / EPC, q = tid % EPC;
+    float v = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) v += pr_w[w][t * EPC + q];
+    const int e = e0 + q;
+    if (e < E) p.logits[(size_t)t * E + e] = v + (p.rbias ? p.rbias[e] : 0.f);
+  }
+
+  DEC_TRACE(3);
+  bool ok = grid_barrier(p.bar, (unsigned)ncta, p.err, 40, &flag_s);
+  DEC_TRACE(4);
+  if (!ok || abort_s) goto drain;
+
+  // ------------------------------------------------------- 2. top-k, slots
+  if (warp < T) {
+    int idx;
+    float w;
+    topk_warp<VPL>(p.logits + (size_t)warp * E, E, k, idx, w);
+    if (lane < k) {
+      idx_s[warp][lane] = idx;
+      w_s[warp][lane] = w;
+      atomicOr(&tmask_s[idx], 1u << warp);
+      if (cta == 0) {
+        if (p.topk_idx) p.topk_idx[warp * k + lane] = idx;
+        if (p.topk_w) p.topk_w[warp * k + lane] = w;
+      }
+    }
+  }
+  __syncthreads();
+  if (warp == 0) {
+    // slots: 0 = shared (if any), then the selected experts in ascending
+    // order, each with its tokens in ascending order
+    int base = p.has_shared;
+    for (int eb = 0; eb < E; eb += 32) {
+      const int e = eb + lane;
+      const unsigned m = e < E ? tmask_s[e] : 0u;
+      const unsigned act = __ballot_sync(0xffffffffu, m != 0u);
+      if (m) {
+        const int sl = base + __popc(act & ((1u << lane) - 1u));
+        slot_of_s[e] = sl;
+        slot_e[sl] = e;
+        cnt_s[sl] = __popc(m);
+        int col = 0;
+        for (int t = 0; t < T; ++t)
+          if (m & (1u << t)) tok_s[sl][col++] = t;
+      }
+      base += __popc(act);
+    }
+    if (p.has_shared && lane < T) tok_s[0][lane] = lane;
+    if (lane == 0) {
+      nslots_s = base;
+      if (p.has_shared) {
+        slot_e[0] = -1;
+        cnt_s[0] = T;
+      }
+    }
+    __syncwarp();
+    // activation row offsets (exclusive scan of the slots' token counts)
+    int carry = 0;
+    for (int s0 = 0; s0 < base; s0 += 32) {
+      const int sl = s0 + lane;
+      const int v = sl < base ? cnt_s[sl] : 0;
+      int inc = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += n;
+      }
+      if (sl < base) soff_s[sl] = carry + inc - v;
+      carry += __shfl_sync(0xffffffffu, inc, 31);
+    }
+  }
+  __syncthreads();
+  n_units = nslots_s * upe;
+  n_gu = cta < n_units ? (n_units - cta + ncta - 1) / ncta : 0;
+  n_dc = cta < p.n_dn ? (nslots_s + kSlotsPerChunk - 1) / kSlotsPerChunk : 0;
+  if (tid == kIssuer)
+    for (int i = (early0 ? 1 : 0); i < kRing && i < n_gu + n_dc; ++i) issue(i);
+  DEC_TRACE(5);
+  for (int i = tid; i < T * k; i += kThreads) {   // used by the combine, after later barriers
+    const int t = i / k, j = i - t * k, e = idx_s[t][j];
+    sc_s[t][j] = slot_of_s[e] * 16 + __popc(tmask_s[e] & ((1u << t) - 1u));
+  }
+
+  // ----------------------------------------------- 3. gate/up + SwiGLU units
+#ifdef MOE_DEC_TRACE
+  tr_wait = 0;
+  tr_comp = 0;
+  tr_mark = globaltimer_ns();
+  if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][14] = g_dec_trace[blockIdx.x][15] = 0;
+#endif
+  for (int i = 0; i < n_gu; ++i) {
+    const int b = i % kRing;
+    if (!mbar_wait_drain(&full[b], (uint32_t)((i / kRing) & 1), p.err.limit_ns)) {
+      if (lane == 0) report_timeout(p.err, 41);
+      abort_s = 1;
+    }
+    // (also: every warp has finished the epilogue of unit i - 2, which used
+    // the reduction buffer this unit writes)
+    __syncthreads();
+#ifdef MOE_DEC_TRACE
+    {
+      const unsigned long long now = globaltimer_ns();
+      tr_wait += now - tr_mark;
+      tr_mark = now;
+    }
+#endif
+    if (abort_s) goto drain;
+    const int u = cta + i * ncta, s = u / upe, r = u - s * upe;
+    const int cnt = cnt_s[s];
+    const uint32_t bq = sbase + (uint32_t)b * L.slab;
+    const uint16_t* sb = reinterpret_cast<const uint16_t*>(smem + (size_t)b * L.slab + 2 * gu_q);
+    // token rows of this lane's B column (g) and of its two D columns
+    const int trow = g < cnt ? tok_s[s][g] : kMaxT;
+    const int t0 = 2 * c < cnt ? tok_s[s][2 * c] : kMaxT;
+    const int t1 = 2 * c + 1 < cnt ? tok_s[s][2 * c + 1] : kMaxT;
+    const uint32_t* xr = xw + trow * L.xstride;
+    float tot[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) tot[mt][q] = 0.f;
+    // this warp's K groups, four at a time: every shared-memory operand of
+    // the four is loaded before the first MMA, so their chains overlap
+    const int gpw = G / kWarps;   // a multiple of 4 (host-checked)
+    for (int gb = 0; gb < gpw; gb += 4) {
+      uint2 qw[4][2][2];
+      uint32_t bf[4][4][2];
+      float sc[4][2][2], cb[4][2][2], xs0[4], xs1[4];
+      // groups warp*gpw + gb .. + 3 are the 4 groups of one 32-word chunk
+      const uint32_t zb = bq + (uint32_t)((warp * gpw + gb) >> 2) * (kRu * 128);
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi) {
+        const bool v = true;
+        const int grp = warp * gpw + gb + gi;
+        const uint32_t col = (uint32_t)(((2 * gi + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            qw[gi][mt][h] = lds_v2(zb + mt * gu_q + (uint32_t)((g + 8 * h) * 128) + col);
+            const int row = g + 8 * h;
+            const float s1 = v ? bf16_to_f32(sb[(2 * mt) * (kRu * G) + row * G + grp]) : 0.f;
+            const float b1 = v ? bf16_to_f32(sb[(2 * mt + 1) * (kRu * G) + row * G + grp]) : 0.f;
+            sc[gi][mt][h] = s1;
+            cb[gi][mt][h] = fmaf(-1024.0f, s1, b1);
+          }
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
+          bf[gi][st][0] = v ? xr[4 * wabs + psel] : 0u;
+          bf[gi][st][1] = v ? xr[4 * wabs + psel + 1] : 0u;
+        }
+        xs0[gi] = v ? xg[t0 * G + grp] : 0.f;
+        xs1[gi] = v ? xg[t1 * G + grp] : 0.f;
+      }
+      // 8 independent accumulator chains (4 groups x gate/up), k-step
+      // outermost so that consecutive MMAs never depend on each other
+      float acc[4][2][4];
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[gi][mt][q] = 0.f;
+#pragma unroll
+      for (int st = 0; st < 4; ++st) {
+        const int psel = 2 * (st & 1);
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t w0 = (st >> 1) ? qw[gi][mt][0].y : qw[gi][mt][0].x;
+            const uint32_t w1 = (st >> 1) ? qw[gi][mt][1].y : qw[gi][mt][1].x;
+            mma_m16n8k16_f16(acc[gi][mt], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
+                             nibble_pair_1024(w0, psel + 1), nibble_pair_1024(w1, psel + 1),
+                             bf[gi][st][0], bf[gi][st][1]);
+          }
+      }
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            tot[mt][2 * h] += fmaf(sc[gi][mt][h], acc[gi][mt][2 * h], cb[gi][mt][h] * xs0[gi]);
+            tot[mt][2 * h + 1] += fmaf(sc[gi][mt][h], acc[gi][mt][2 * h + 1], cb[gi][mt][h] * xs1[gi]);
+          }
+    }
+#ifdef MOE_DEC_TRACE
+    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][14] += globaltimer_ns() - tr_mark;
+#endif
+    // split-K partials of the 8 warps (double-buffered by unit parity)
+    float* rbuf = red + (i & 1) * (kWarps * 32 * kRedStride);
+    float* rw = rbuf + (warp * 32 + lane) * kRedStride;
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) rw[mt * 4 + q] = tot[mt][q];
+    __syncthreads();   // partials complete; every read of this slab done
+#ifdef MOE_DEC_TRACE
+    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][15] += globaltimer_ns() - tr_mark;
+#endif
+    if (tid == kIssuer && i + kRing < n_gu + n_dc) issue(i + kRing);
+    if (warp < 4) {
+      // warp q adds (in warp order) and finishes output q of every lane:
+      // gate (partial q) and up (partial 4 + q) of row g + 8 (q / 2), column 2 c + q % 2
+      const int q = warp;
+      float gate = 0.f, up = 0.f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        const float* rr = rbuf + (w * 32 + lane) * kRedStride;
+        gate += rr[q];
+        up += rr[4 + q];
+      }
+      const int col = 2 * c + (q & 1), row = g + 8 * (q >> 1);
+      uint32_t big = 0u;
+      if (col < cnt) {
+        const float a = silu_fast(gate) * up;
+        big = fabsf(a) > kF16Max ? 1u : 0u;
+        p.act[(size_t)(soff_s[s] + col) * I + perm8_pos(kRu * r + row)] = f32_to_f16_sat(a);
+      }
+      report_range_warp(p.err, big != 0u);
+    }
+#ifdef MOE_DEC_TRACE
+    {
+      const unsigned long long now = globaltimer_ns();
+      tr_comp += now - tr_mark;
+      tr_mark = now;
+    }
+#endif
+  }
+#ifdef MOE_DEC_TRACE
+  if (tid == 0 && blockIdx.x < 256) {
+    g_dec_trace[blockIdx.x][9] = tr_wait;
+    g_dec_trace[blockIdx.x][10] = tr_comp;
+    g_dec_trace[blockIdx.x][11] = (unsigned long long)n_gu;
+  }
+#endif
+
+  DEC_TRACE(6);
+  ok = grid_barrier(p.bar, 2u * ncta, p.err, 42, &flag_s);
+  DEC_TRACE(7);
+  if (!ok) goto drain;
+
+  // ------------------------------------------ 4. down, combine, stack update
+  // HBM is idle from here on: pull the next layer's routing-independent
+  // weights (router weight, shared expert) into L2, a slice per CTA
+  if (tid == 0 && p.next_wr) {
+    const size_t rbytes = (size_t)H * E * 2;
+    const size_t per = ((rbytes + ncta - 1) / ncta + 255) / 256 * 256;
+    const size_t b0 = per * cta;
+    if (b0 < rbytes)
+      bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.next_wr) + b0,
+                       (uint32_t)(b0 + per <= rbytes ? per : rbytes - b0));
+    if (p.has_shared) {
+      // shared gate/up/down packed rows, then scales and biases: 9 arrays
+      const W4Dev* m3[3] = {&p.next_sgate, &p.next_sup, &p.next_sdown};
+      for (int m = 0; m < 3; ++m) {
+        const size_t qb = (size_t)H * I / 2, sbb = (size_t)H * I / 64 * 2;
+        const size_t pq = ((qb + ncta - 1) / ncta + 255) / 256 * 256;
+        const size_t ps = ((sbb + ncta - 1) / ncta + 255) / 256 * 256;
+        if (pq * cta < qb)
+          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->q) + pq * cta,
+                           (uint32_t)(pq * cta + pq <= qb ? pq : qb - pq * cta));
+        if (ps * cta < sbb) {
+          const uint32_t n = (uint32_t)(ps * cta + ps <= sbb ? ps : sbb - ps * cta);
+          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->s) + ps * cta, n);
+          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->b) + ps * cta, n);
+        }
+      }
+    }
+  }
+  if (n_dc > 0) {
+    float* dsum = reinterpret_cast<float*>(smem + L.xw);   // [slot][kDn][kMaxT]
+    // The activation row of this lane's column for slot s, all of its groups:
+    // 16-byte pieces 8 grp + 2 c and the next (K blocks of 8), issued at once.
+    auto load_act = [&](int s, uint4 (&v)[16]) {
+      const bool have = s < nslots_s && g < cnt_s[s];
+      const uint4* arow =
+          reinterpret_cast<const uint4*>(p.act + (size_t)(have ? soff_s[s] + g : 0) * I);
+#pragma unroll
+      for (int grp = 0; grp < 8; ++grp) {
+        v[2 * grp] = (have && grp < GI) ? __ldcg(arow + 8 * grp + 2 * c) : make_uint4(0u, 0u, 0u, 0u);
+        v[2 * grp + 1] = (have && grp < GI) ? __ldcg(arow + 8 * grp + 2 * c + 1) : make_uint4(0u, 0u, 0u, 0u);
+      }
+    };
+    // One slot: its 16 down rows (ring buffer b, position q) times its
+    // activation rows; the FP32 result goes to dsum.
+    auto down_slot = [&](int s, int b, int q, const uint4 (&v)[16]) {
+      const uint32_t bq = sbase + (uint32_t)b * L.slab + (uint32_t)q * dn_q;
+      const uint16_t* ssc = reinterpret_cast<const uint16_t*>(
+          smem + (size_t)b * L.slab + kSlotsPerChunk * dn_q + q * dn_s);
+      const uint16_t* sbi = reinterpret_cast<const uint16_t*>(
+          smem + (size_t)b * L.slab + kSlotsPerChunk * (dn_q + dn_s) + q * dn_s);
+      float tot[4] = {0.f, 0.f, 0.f, 0.f};
+      const uint32_t one2 = 0x3C003C00u;   // fp16 (1, 1)
+#pragma unroll
+      for (int g0 = 0; g0 < 8; g0 += 4) {
+        if (g0 >= GI) break;
+        // four groups at a time: their A words, then 8 independent MMA chains
+        // (the groups' products, and their activation column sums by an
+        // all-ones A: every D row is then the column sum, exact products)
+        uint2 qw[4][2];
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) qw[gi][h] = lds_v2(bq + qoff(g + 8 * h, g0 + gi, c, kDn));
+        float acc[4][4], gsum[4][4];
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[gi][q] = gsum[gi][q] = 0.f;
+#pragma unroll
+        for (int st = 0; st < 4; ++st) {
+          const int psel = 2 * (st & 1);
+#pragma unroll
+          for (int gi = 0; gi < 4; ++gi) {
+            const uint4 vv = v[2 * (g0 + gi) + (st >> 1)];
+            const uint32_t b0 = psel ? vv.z : vv.x, b1 = psel ? vv.w : vv.y;
+            const uint32_t w0 = (st >> 1) ? qw[gi][0].y : qw[gi][0].x;
+            const uint32_t w1 = (st >> 1) ? qw[gi][1].y : qw[gi][1].x;
+            mma_m16n8k16_f16(acc[gi], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
+                             nibble_pair_1024(w0, psel + 1), nibble_pair_1024(w1, psel + 1), b0, b1);
+            mma_m16n8k16_f16(gsum[gi], one2, one2, one2, one2, b0, b1);
+          }
+        }
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const int row = g + 8 * h, grp = g0 + gi;
+            const float sc = bf16_to_f32(ssc[row * GI + grp]);
+            const float cb = fmaf(-1024.0f, sc, bf16_to_f32(sbi[row * GI + grp]));
+            tot[2 * h] += fmaf(sc, acc[gi][2 * h], cb * gsum[gi][0]);       // column 2c
+            tot[2 * h + 1] += fmaf(sc, acc[gi][2 * h + 1], cb * gsum[gi][1]);   // column 2c + 1
+          }
+      }
+#pragma unroll
+      for (int qq = 0; qq < 4; ++qq) {
+        const int col = 2 * c + (qq & 1), row = g + 8 * (qq >> 1);
+        dsum[(s * kDn + row) * kMaxT + col] = tot[qq];
+      }
+    };
+#ifdef MOE_DEC_TRACE
+    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][12] = globaltimer_ns();
+#endif
+    if (n_dc <= kRing) {
+      // every down chunk's copy was issued during step 3: each warp walks its
+      // slots (s = warp, warp + 8, ...), loading the next slot's activations
+      // while it computes the current one
+      uint4 cur[16], nxt[16];
+      load_act(warp, cur);
+      for (int s = warp; s < nslots_s; s += kSlotsPerChunk) {
+        load_act(s + kSlotsPerChunk, nxt);
+        const int i = n_gu + s / kSlotsPerChunk, b = i % kRing;
+        if (!mbar_wait_drain(&full[b], (uint32_t)((i / kRing) & 1), p.err.limit_ns)) {
+          if (lane == 0) report_timeout(p.err, 43);
+          abort_s = 1;
+          break;
+        }
+        down_slot(s, b, s % kSlotsPerChunk, cur);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) cur[j] = nxt[j];
+      }
+      __syncthreads();
+      if (abort_s) goto drain;
+    } else {
+      // more chunks than buffers: chunk by chunk, reusing buffers
+      for (int ch = 0; ch < n_dc; ++ch) {
+        const int i = n_gu + ch, b = i % kRing;
+        uint4 cur[16];
+        const int s = kSlotsPerChunk * ch + warp;
+        load_act(s, cur);
+        if (!mbar_wait_drain(&full[b], (uint32_t)((i / kRing) & 1), p.err.limit_ns)) {
+          if (lane == 0) report_timeout(p.err, 43);
+          abort_s = 1;
+        }
+        __syncthreads();
+        if (abort_s) goto drain;
+        if (s < nslots_s) down_slot(s, b, warp, cur);
+        __syncthreads();
+        if (tid == kIssuer && i + kRing < n_gu + n_dc) issue(i + kRing);
+      }
+    }
+#ifdef MOE_DEC_TRACE
+    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][13] = globaltimer_ns();
+#endif
+    // y[t] = shared + sum_j w[t][j] * expert_j[t] (FP32, rank order); x update
+    if (tid < T * kDn) {
+      const int t = tid / kDn, hh = tid % kDn;
+      float y = p.has_shared ? dsum[(0 * kDn + hh) * kMaxT + t] : 0.f;
+      for (int j = 0; j < k; ++j) {
+        const int scv = sc_s[t][j];
+        y = fmaf(w_s[t][j], dsum[((scv >> 4) * kDn + hh) * kMaxT + (scv & 15)], y);
+      }
+      const int h = kDn * cta + hh;
+      p.x[(size_t)t * H + h] = f32_to_bf16(fmaf(p.alpha, y, x_s[t][hh]));
+      if (p.y_out) p.y_out[(size_t)t * H + h] = y;
+    }
+  }
+  // the last CTA to leave sets the counter back to 0 for the next launch
+  __syncthreads();
+  DEC_TRACE(8);
+  if (tid == 0 && atomicAdd(p.bar, 1u) == 3u * ncta - 1u) *p.bar = 0u;
+  return;
+
+drain:
+  // a wait gave up: let this CTA's own copies land before it exits (the
+  // counter stays set; moe_get_error clears it with the error word)
+  __syncthreads();
+  if (tid == 0 && router_cta) mbar_wait_drain(&wbar, 0, p.err.limit_ns);
+  if (tid == kIssuer) {
+    for (int b = 0; b < kRing && b < issued; ++b) {
+      const int last = b + ((issued - 1 - b) / kRing) * kRing;   // last item in buffer b
+      mbar_wait_drain(&full[b], (uint32_t)((last / kRing) & 1), p.err.limit_ns);
+    }
+  }
+  __syncthreads();
+}
+
+}  // namespace dec
+
+#ifdef MOE_DEC_TRACE
+extern "C" int moe_debug_dec_trace(unsigned long long* out) {
+  return (int)cudaMemcpyFromSymbol(out, dec::g_dec_trace, sizeof(dec::g_dec_trace));
+}
+#endif
+
+bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int num_sms) {
+  if (T < 1 || T > dec::kMaxT || k > 32 || E > 512 || E % 8) return false;
+  if (H % 512 || I % 256 || I / 64 > 8 || H / 8 > 2 * dec::kThreads || H / dec::kDn > num_sms)
+    return false;
+  if (E % dec::kRBoxE || E / dec::kRBoxE > num_sms) return false;
+  if ((H / 64) % (4 * dec::kWarps)) return false;   // K groups per warp a multiple of 4
+  const dec::Smem L = dec::smem_layout(H, I);
+  if ((uint32_t)H * dec::kRBoxE * 2 > L.slab) return false;   // router slice in one ring buffer
+  if ((uint32_t)dec::kMaxT * H * 2 > L.slab) return false;     // bf16 token rows in another
+  const int slots = T * k + has_shared;
+  if (slots > dec::kMaxSlots || (uint32_t)slots * dec::kDn * dec::kMaxT * 4 > L.dsum_cap) return false;
+  if (L.total + 1024 > 227 * 1024) return false;
+  int dev = 0, coop = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess || !coop)
+    return false;
+  auto kern = E <= 256 ? (E <= 2 * num_sms ? dec::moe_decode_layer_kernel<8, 2> : dec::moe_decode_layer_kernel<8, 8>)
+                       : dec::moe_decode_layer_kernel<16, 8>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.total + 1024) !=
+      cudaSuccess)
+    return false;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, dec::kThreads, L.total + 1024) !=
+      cudaSuccess)
+    return false;
+  return per_sm >= 1;
+}
+
+cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sms, cudaStream_t st) {
+  dec::Params p;
+  p.T = a.T;
+  p.H = a.H;
+  p.I = a.I;
+  p.E = a.E;
+  p.k = a.k;
+  p.has_shared = a.has_shared;
+  p.alpha = a.alpha;
+  p.eps = a.eps;
+  p.n_dn = a.H / dec::kDn;
+  p.x = a.x;
+  p.wr = a.router_w;
+  p.rbias = a.router_bias;
+  p.gate = a.gate;
+  p.up = a.up;
+  p.down = a.down;
+  p.sgate = a.sgate;
+  p.sup = a.sup;
+  p.sdown = a.sdown;
+  p.mg = a.maps[0];
+  p.mu = a.maps[1];
+  p.md = a.maps[2];
+  p.msg = a.maps[3];
+  p.msu = a.maps[4];
+  p.msd = a.maps[5];
+  p.mr = a.router_map;
+  p.logits = a.logits;
+  p.act = a.act;
+  p.topk_idx = a.topk_idx;
+  p.topk_w = a.topk_w;
+  p.y_out = a.y_out;
+  p.next_wr = a.next_router_w;
+  p.next_sgate = a.next_sgate;
+  p.next_sup = a.next_sup;
+  p.next_sdown = a.next_sdown;
+  p.bar = a.bar;
+  p.err = err;
+  const dec::Smem L = dec::smem_layout(a.H, a.I);
+  const size_t smem = L.total + 1024;
+  auto kern = a.E <= 256 ? (a.E <= 2 * num_sms ? dec::moe_decode_layer_kernel<8, 2>
+                                                : dec::moe_decode_layer_kernel<8, 8>)
+                         : dec::moe_decode_layer_kernel<16, 8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(num_sms);
+  cfg.blockDim = dim3(dec::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  // cooperative (the CTAs wait on one another at the grid barriers), and,
+  // where the runtime takes both, with programmatic dependent launch so the
+  // prologue's weight copies overlap the previous launch
+  static int pdl_ok = -1;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  if (pdl_ok != 0) {
+    cfg.numAttrs = 2;
+    e = cudaLaunchKernelEx(&cfg, kern, p);
+    if (e == cudaSuccess) {
+      pdl_ok = 1;
+      return e;
+    }
+    cudaGetLastError();   // the combination was refused: cooperative only from now on
+    pdl_ok = 0;
+  }
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace moe

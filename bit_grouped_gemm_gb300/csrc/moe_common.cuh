@@ -219,6 +219,29 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const void* tmap, in
       : "memory");
 }
 
+// 3D tiled load global -> shared, completion counted on `bar` (bytes).
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const void* tmap, int x, int y, int z,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// ---------------------------------------------------------------- mma.sync ---
+// D (+)= A * B, m16n8k16, fp16 operands, fp32 accumulation. Not volatile:
+// the compiler may interleave independent MMAs to hide their latency.
+__device__ __forceinline__ void mma_m16n8k16_f16(float (&c)[4], uint32_t a0, uint32_t a1,
+                                                 uint32_t a2, uint32_t a3, uint32_t b0,
+                                                 uint32_t b1) {
+  asm(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
 // ---------------------------------------------------------------- tcgen05 ---
 __device__ __forceinline__ void tmem_alloc(uint32_t* smem_result, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
@@ -366,6 +389,13 @@ __device__ __forceinline__ void nibbles_to_f16x2_1024(uint32_t w, uint32_t (&p)[
   p[1] = lop3_and_or(w >> 4, 0x000F000Fu, 0x64006400u);
   p[2] = lop3_and_or(w >> 8, 0x000F000Fu, 0x64006400u);
   p[3] = lop3_and_or(w >> 12, 0x000F000Fu, 0x64006400u);
+}
+
+// Nibble pair j (j = 0..3: nibbles j and j + 4) of a packed word as the
+// f16x2 word (1024 + q_j, 1024 + q_{j+4}) -- one element of
+// nibbles_to_f16x2_1024, for callers that need only some of the four.
+__device__ __forceinline__ uint32_t nibble_pair_1024(uint32_t w, int j) {
+  return lop3_and_or(w >> (4 * j), 0x000F000Fu, 0x64006400u);
 }
 
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {

@@ -146,4 +146,39 @@ bool smallm_fits(int H, int I);
 cudaError_t launch_gemm_smallm(int mode, const GemmProblem& p, const SmallMaps& maps, DevErr err,
                                int num_sms, cudaStream_t st);
 
+// ------------------------------------------------------ fused decode layer ---
+// One whole layer of a decode-sized batch (T <= 8) in one cooperative launch
+// (decode_fused.cu): router, top-k, gate/up + SwiGLU, down, combine and the
+// stack update x = bf16(x + alpha * y), with the RMS norm of x taken inside.
+struct DecodeLayerArgs {
+  int T, H, I, E, k, has_shared;
+  float alpha, eps;
+  uint16_t* x;                   // residual bf16 [T][H], updated in place
+  const uint16_t* router_w;
+  const float* router_bias;
+  W4Dev gate, up, down, sgate, sup, sdown;
+  CUtensorMap maps[6];           // gate, up, down, shared gate, up, down (encode_slab_3d)
+  CUtensorMap router_map;        // router weight, encode_router_slices
+  float* logits;                 // [T][E] scratch
+  uint16_t* act;                 // [T*k + T][I] fp16 scratch
+  int32_t* topk_idx;             // [T][k] routing of the layer (outputs)
+  float* topk_w;
+  float* y_out;                  // [T][H] FP32 block output, or null
+  unsigned* bar;                 // grid-barrier counter, 0 between launches
+  // the next layer's router weight and shared expert, pulled into L2 while
+  // this layer's down pass runs (next_router_w null: none)
+  const uint16_t* next_router_w;
+  W4Dev next_sgate, next_sup, next_sdown;
+};
+bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int num_sms);
+cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sms, cudaStream_t st);
+
+// 2D map of the router weight bf16 [H][E] with boxes of 8 experts x 256 rows
+// (16-byte rows, no swizzle).
+bool encode_router_slices(CUtensorMap* m, const void* base, int H, int E);
+
+// 3D map of a packed-word matrix uint32 [rows][K/8] as boxes of 32 words x
+// box_rows rows x K/256 chunks (one box = box_rows whole rows), 128-byte swizzle.
+bool encode_slab_3d(CUtensorMap* m, const void* base, uint64_t rows, int K, uint32_t box_rows);
+
 }  // namespace moe

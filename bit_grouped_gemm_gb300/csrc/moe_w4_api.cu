@@ -108,6 +108,35 @@ struct moe_plan {
   // weight sets (scales, biases, count) whose fp16 operand range was checked
   std::set<std::tuple<const void*, const void*, size_t>> range_checked;
 
+  // 3D slab map (encode_slab_3d) of a packed-word matrix [rows][K/8], cached
+  // under the same table with the top bit of the box height set
+  bool qmap3(CUtensorMap* out, const void* base, uint64_t rows, int K, uint32_t box_rows) {
+    const auto key = std::make_tuple(base, rows, (uint64_t)K, box_rows | 0x80000000u);
+    auto it = qmaps.find(key);
+    if (it == qmaps.end()) {
+      CUtensorMap m;
+      if (!encode_slab_3d(&m, base, rows, K, box_rows)) return false;
+      if (qmaps.size() >= 4096) qmaps.clear();
+      it = qmaps.emplace(key, m).first;
+    }
+    *out = it->second;
+    return true;
+  }
+
+  // router-weight map (encode_router_slices), cached under the same table
+  bool rmap(CUtensorMap* out, const void* base, int H, int E) {
+    const auto key = std::make_tuple(base, (uint64_t)H, (uint64_t)E, 0x40000000u);
+    auto it = qmaps.find(key);
+    if (it == qmaps.end()) {
+      CUtensorMap m;
+      if (!encode_router_slices(&m, base, H, E)) return false;
+      if (qmaps.size() >= 4096) qmaps.clear();
+      it = qmaps.emplace(key, m).first;
+    }
+    *out = it->second;
+    return true;
+  }
+
   bool qmap(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
     const auto key = std::make_tuple(base, rows, cols, box_rows);
     auto it = qmaps.find(key);
@@ -265,6 +294,93 @@ moe_status route_impl(moe_plan* p, const uint16_t* x, int T, const uint16_t* rou
   return MOE_OK;
 }
 
+// The scales and biases of a weight set are checked against the fp16
+// operand range once, on the first call that sees the set (by address), in a
+// kernel on the stream; a value out of range latches DEVERR_RANGE.
+cudaError_t check_weight_range(moe_plan* p, const moe_experts* routed, const moe_experts* shared,
+                               cudaStream_t st) {
+  const moe_plan_desc& d = p->d;
+  const int H = d.hidden, I = d.inter, E = d.num_experts;
+  auto range_check = [&](const moe_w4& m, size_t n) {
+    if (p->range_checked.size() >= 4096) p->range_checked.clear();
+    if (!p->range_checked.insert(std::make_tuple((const void*)m.scales, (const void*)m.biases, n)).second)
+      return cudaSuccess;
+    return launch_w4_range_check(m.scales, m.biases, n, p->err(), p->num_sms, st);
+  };
+  const size_t n_gu = (size_t)I * (H / kGroup), n_dn = (size_t)H * (I / kGroup);
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
+    const moe_w4& m = i == 0 ? routed->gate : i == 1 ? routed->up : routed->down;
+    e = range_check(m, (i < 2 ? n_gu : n_dn) * E);
+    if (e == cudaSuccess && d.has_shared && shared) {
+      const moe_w4& ms = i == 0 ? shared->gate : i == 1 ? shared->up : shared->down;
+      e = range_check(ms, i < 2 ? n_gu : n_dn);
+    }
+  }
+  return e;
+}
+
+// Whether a T-token chunk of moe_forward_stack takes the fused decode layer.
+bool use_decode_fused(const moe_plan* p, int T) {
+  const moe_plan_desc& d = p->d;
+  return ffn_path(p, T) == 2 &&
+         decode_fused_fits(T, d.hidden, d.inter, d.num_experts, d.top_k, d.has_shared, p->num_sms);
+}
+
+// One layer of a decode-sized chunk in one launch: x = bf16(x + alpha *
+// moe(rmsnorm(x))); the routing lands in the plan's routing arrays and y (FP32)
+// in the shared-output buffer, for inspection.
+moe_status decode_layer_impl(moe_plan* p, uint16_t* x, int T, const moe_layer& Ly, float alpha,
+                             cudaStream_t st, const moe_layer* next) {
+  const moe_plan_desc& d = p->d;
+  const int H = d.hidden, I = d.inter, E = d.num_experts;
+  const moe_experts* shared = d.has_shared ? &Ly.shared : nullptr;
+  if (check_weight_range(p, &Ly.routed, shared, st) != cudaSuccess) return MOE_ERR_CUDA;
+  DecodeLayerArgs a;
+  a.T = T;
+  a.H = H;
+  a.I = I;
+  a.E = E;
+  a.k = d.top_k;
+  a.has_shared = d.has_shared;
+  a.alpha = alpha;
+  a.eps = kRmsEps;
+  a.x = x;
+  a.router_w = Ly.router_w;
+  a.router_bias = Ly.router_bias;
+  a.gate = dev(Ly.routed.gate);
+  a.up = dev(Ly.routed.up);
+  a.down = dev(Ly.routed.down);
+  const moe_experts& sh = d.has_shared ? Ly.shared : Ly.routed;
+  a.sgate = dev(sh.gate);
+  a.sup = dev(sh.up);
+  a.sdown = dev(sh.down);
+  const uint64_t er = d.has_shared ? 1 : (uint64_t)E;
+  bool ok = p->qmap3(&a.maps[0], Ly.routed.gate.qweight, (uint64_t)E * I, H, 16) &&
+            p->qmap3(&a.maps[1], Ly.routed.up.qweight, (uint64_t)E * I, H, 16) &&
+            p->qmap3(&a.maps[2], Ly.routed.down.qweight, (uint64_t)E * H, I, 16) &&
+            p->qmap3(&a.maps[3], sh.gate.qweight, er * I, H, 16) &&
+            p->qmap3(&a.maps[4], sh.up.qweight, er * I, H, 16) &&
+            p->qmap3(&a.maps[5], sh.down.qweight, er * H, I, 16) &&
+            p->rmap(&a.router_map, Ly.router_w, H, E);
+  if (!ok) return MOE_ERR_CUDA;
+  a.logits = p->at<float>(p->L.logits);
+  a.act = p->at<uint16_t>(p->L.act);
+  a.topk_idx = p->at<int32_t>(p->L.topk_idx);
+  a.topk_w = p->at<float>(p->L.topk_w);
+  a.y_out = d.has_shared ? p->at<float>(p->L.dsh) : nullptr;
+  a.bar = p->at<unsigned>(p->L.arrive) + 2;
+  a.next_router_w = next ? next->router_w : nullptr;
+  a.next_sgate = a.next_sup = a.next_sdown = W4Dev{nullptr, nullptr, nullptr};
+  if (next && d.has_shared) {
+    a.next_sgate = dev(next->shared.gate);
+    a.next_sup = dev(next->shared.up);
+    a.next_sdown = dev(next->shared.down);
+  }
+  p->last_path = 3;
+  return st_of(timed(p, 9, st, [&] { return launch_decode_layer(a, p->err(), p->num_sms, st); }));
+}
+
 // The stack update fused into the combine (moe_forward_layer_residual).
 struct ResidualUpdate {
   float alpha;
@@ -283,25 +399,7 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   const int path = ffn_path(p, T);
   p->last_path = path;
 
-  // The scales and biases of a weight set are checked against the fp16
-  // operand range once, on the first call that sees the set (by address), in
-  // a kernel on the stream; a value out of range latches DEVERR_RANGE.
-  cudaError_t e = cudaSuccess;
-  auto range_check = [&](const moe_w4& m, size_t n) {
-    if (p->range_checked.size() >= 4096) p->range_checked.clear();
-    if (!p->range_checked.insert(std::make_tuple((const void*)m.scales, (const void*)m.biases, n)).second)
-      return cudaSuccess;
-    return launch_w4_range_check(m.scales, m.biases, n, p->err(), p->num_sms, st);
-  };
-  const size_t n_gu = (size_t)I * (H / kGroup), n_dn = (size_t)H * (I / kGroup);
-  for (int i = 0; i < 3 && e == cudaSuccess; ++i) {
-    const moe_w4& m = i == 0 ? routed->gate : i == 1 ? routed->up : routed->down;
-    e = range_check(m, (i < 2 ? n_gu : n_dn) * E);
-    if (e == cudaSuccess && hs) {
-      const moe_w4& ms = i == 0 ? shared->gate : i == 1 ? shared->up : shared->down;
-      e = range_check(ms, i < 2 ? n_gu : n_dn);
-    }
-  }
+  cudaError_t e = check_weight_range(p, routed, shared, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
 
   // the tensor-core path reads gathered rows with TMA; the small-M path reads
@@ -613,6 +711,17 @@ moe_status moe_forward_stack(moe_plan_t p, uint16_t* x, uint16_t* xn, int T,
   for (int c0 = 0; c0 < T; c0 += chunk) {
     const int Tc = T - c0 < chunk ? T - c0 : chunk;
     uint16_t* xc = x + (size_t)c0 * H;
+    if (use_decode_fused(p, Tc)) {
+      // decode-sized chunk: one launch per layer (the norm is taken inside),
+      // then the chunk's normalised stream for the caller
+      cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+      for (int l = 0; l < num_layers; ++l)
+        if ((s = decode_layer_impl(p, xc, Tc, layers[l], alpha, st,
+                                   l + 1 < num_layers ? &layers[l + 1] : nullptr)) != MOE_OK)
+          return s;
+      if ((s = moe_residual_add(p, xc, nullptr, Tc, 0.f, xc, xn, stream)) != MOE_OK) return s;
+      continue;
+    }
     if ((s = moe_residual_add(p, xc, nullptr, Tc, 0.f, xc, xn, stream)) != MOE_OK) return s;
     for (int l = 0; l < num_layers; ++l) {
       const moe_layer& L = layers[l];
@@ -649,6 +758,8 @@ moe_status moe_get_error(moe_plan_t p) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(h, p->at<int>(p->L.err), 8, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(p->at<int>(p->L.err), 0, 8);
+  // a launch that gave up at a barrier leaves its arrival counters set
+  if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT)) e = cudaMemset(p->at<int>(p->L.arrive), 0, 16);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaSetDevice(prev);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

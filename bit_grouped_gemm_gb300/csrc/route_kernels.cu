@@ -13,6 +13,7 @@
 #include <mutex>
 
 #include "moe_common.cuh"
+#include "topk.cuh"
 
 namespace moe {
 
@@ -51,6 +52,32 @@ bool encode_2d(CUtensorMap* m, CUtensorMapDataType dt, int elem_bytes, const voi
   cuuint32_t es[2] = {1, 1};
   CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, es,
                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_router_slices(CUtensorMap* m, const void* base, int H, int E) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc || H % 256 || E % 8) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)H};
+  cuuint64_t strides[1] = {(cuuint64_t)E * 2};
+  cuuint32_t box[2] = {8, 256};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool encode_slab_3d(CUtensorMap* m, const void* base, uint64_t rows, int K, uint32_t box_rows) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc || K % 256) return false;
+  cuuint64_t dims[3] = {32, rows, (cuuint64_t)(K / 256)};
+  cuuint64_t strides[2] = {(cuuint64_t)K / 2, 128};   // row, 128-byte chunk
+  cuuint32_t box[3] = {32, box_rows, (cuuint32_t)(K / 256)};
+  cuuint32_t es[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<void*>(base), dims, strides, box,
+                   es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -200,62 +227,6 @@ __global__ void __launch_bounds__(256) router_logits_kernel(
 // logits (equal to softmax over all E renormalised over the k). The block
 // writes its per-expert counts to blk_cnt[block][E].
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t order_key(float f) {   // monotone float -> uint32
-  const uint32_t u = __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(uint32_t k) {
-  return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
-}
-
-// One token's selection by one warp, from its logits row (read through L2:
-// the row may have been written by other CTAs of the same launch). Lane j < k
-// gets the j-th selected expert and its renormalised softmax weight.
-template <int VPL>   // values per lane, E <= 32 * VPL
-__device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k,
-                                          int& idx, float& w) {
-  const int lane = threadIdx.x & 31;
-  uint32_t key[VPL];
-#pragma unroll
-  for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    const float l = e < E ? __ldcg(row + e) : -INFINITY;
-    key[i] = order_key(isnan(l) ? -INFINITY : l + 0.0f);   // + 0 turns -0 into +0
-  }
-  uint32_t live = 0;   // bit i: lane's value i not selected yet and e < E
-#pragma unroll
-  for (int i = 0; i < VPL; ++i)
-    if (lane + 32 * i < E) live |= 1u << i;
-  float sel_v0 = 0.f, zsum = 0.f, my_val = 0.f;
-  int my_idx = 0;
-  for (int j = 0; j < k; ++j) {
-    // this lane's best live value (lowest i, i.e. lowest expert, on ties)
-    uint32_t bk = 0;
-    int bi = -1;
-#pragma unroll
-    for (int i = 0; i < VPL; ++i)
-      if (((live >> i) & 1u) && (bi < 0 || key[i] > bk)) {
-        bk = key[i];
-        bi = i;
-      }
-    // every real key is above 0, so a lane with nothing live never wins
-    const uint32_t m = __reduce_max_sync(0xffffffffu, bi >= 0 ? bk : 0u);
-    const uint32_t cand = (bi >= 0 && bk == m) ? (uint32_t)(lane + 32 * bi) : 0xffffffffu;
-    const int be = (int)__reduce_min_sync(0xffffffffu, cand);
-    if ((be & 31) == lane) live &= ~(1u << (be >> 5));
-    const float bv = key_value(m);
-    if (j == 0) sel_v0 = bv;
-    const float pj = expf(bv - sel_v0);
-    zsum += pj;
-    if (lane == j) {
-      my_idx = be;
-      my_val = pj;
-    }
-  }
-  idx = my_idx;
-  w = my_val / zsum;
-}
-
 template <int VPL>
 __global__ void __launch_bounds__(1024) router_topk_kernel(
     const float* __restrict__ logits, int T, int E, int k, int32_t* __restrict__ topk_idx,

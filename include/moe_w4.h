@@ -27,6 +27,11 @@
  *     a status; nothing is enqueued then. Errors found on the device (a
  *     bounded wait that ran out) are latched in a device word and reported by
  *     moe_get_error.
+ *   - Weights (router weights, packed experts, scales, biases) are read by
+ *     some kernels before they wait for the previous launch on the stream
+ *     (programmatic dependent launch): no kernel running just before a call
+ *     on the same stream may write them (record an event, or run any other
+ *     launch in between). Token inputs are always read after that wait.
  *   - A plan is not thread-safe: calls on one plan must come from one host
  *     thread at a time, and calls that share a plan's scratch must be ordered
  *     on the device (same stream, or explicit events).
@@ -214,9 +219,15 @@ typedef struct {
  * treats every token on its own, so each chunk's result is the one of the
  * whole prompt). xn is caller scratch, bf16 [min(T, max_tokens)][H], and holds
  * the last chunk's normalised stream on return. Every layer of a chunk is one
- * moe_forward_layer_residual; stream-ordered, no host sync. Errors: as for
- * the per-layer calls (checked for every layer before any launch);
- * MOE_ERR_INVALID_ARG for num_layers < 1 or a NULL layers array. */
+ * moe_forward_layer_residual, except for decode-sized chunks (at most 8
+ * tokens, on the small-M path): there every layer is one launch of a fused
+ * kernel that takes the RMS norm, routes, runs both expert passes and
+ * updates x (the same arithmetic up to rounding: the routed experts' outputs
+ * stay FP32 until the combine; the routing lands in the plan's routing
+ * arrays and y in its FP32 shared-output buffer, moe_debug_buffer 3).
+ * Stream-ordered, no host sync. Errors: as for the per-layer calls (checked
+ * for every layer before any launch); MOE_ERR_INVALID_ARG for num_layers < 1
+ * or a NULL layers array. */
 moe_status moe_forward_stack(moe_plan_t plan, uint16_t* x, uint16_t* xn, int T,
                              const moe_layer* layers, int num_layers, float alpha,
                              moe_stream_t stream);
@@ -294,8 +305,9 @@ moe_status moe_debug_wait_timeout(moe_plan_t plan, int limit_us, moe_stream_t st
  * is bracketed by CUDA events on its stream. moe_read_timing synchronises,
  * adds up the elapsed times per kernel kind since the last read, and resets.
  * Kinds: 0 router logits, 1 scan, 2 scatter, 3 gather, 4 gate/up GEMM,
- * 5 down GEMM, 6 combine, 7 residual, 8 top-k selection. */
-#define MOE_NUM_KERNEL_KINDS 9
+ * 5 down GEMM, 6 combine, 7 residual, 8 top-k selection, 9 fused decode
+ * layer. */
+#define MOE_NUM_KERNEL_KINDS 10
 typedef struct {
   double ms[MOE_NUM_KERNEL_KINDS];
   long long launches[MOE_NUM_KERNEL_KINDS];
@@ -312,7 +324,8 @@ moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
  * unknown `which` or a plan without a shared expert (3). */
 void* moe_debug_buffer(moe_plan_t plan, int which);
 
-/* Which GEMM path the last moe_grouped_w4_ffn took: 1 tensor-core, 2 small-M. */
+/* Which GEMM path the last layer call took: 1 tensor-core, 2 small-M, 3 the
+ * fused decode layer of moe_forward_stack. */
 int moe_last_gemm_path(moe_plan_t plan);
 
 /* Text of a status code. */

@@ -214,12 +214,97 @@ def test_decode_stack_l40_chain(T):
     assert sum(st[1] for st in stats) >= 0.9 * T * w.layers, stats
 
 
+def routing_pointers(plan, x, T, L):
+    """Device addresses of the plan's routing arrays (stable for a plan)."""
+    return bg.moe_route(plan, x, T, L.router_w, L.router_bias)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_decode_fused_layer_chain(T):
+    """The fused decode layer (moe_forward_stack on a chunk of at most 8
+    tokens: router, top-k, gate/up, down, combine and stack update in one
+    launch per layer) against the oracle over the 40-layer stack. At every
+    layer the GPU runs that one layer on the oracle's residual rows; its
+    routing must equal the oracle's (rows with the gap), its FP32 block output
+    (kept in the plan's scratch) must be within 2e-2 * rms of the oracle's,
+    and the updated rows must be bf16(x + y/sqrt(L)) of that output."""
+    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    sh = w.shape
+    k, H = sh.top_k, sh.hidden
+    layers = stack.make_layers(w, "cuda")
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
+    alpha = stack.residual_alpha(w.layers)
+    orc = oracle.get()
+    try:
+        x = synth.decode_pool(w, 1, "cuda")[0].contiguous()
+        xn = torch.empty_like(x)
+        r = routing_pointers(plan, x, T, layers[0])
+        y_view = parity.device_view(bg.moe_debug_buffer(plan, 3), T * H, torch.float32)
+        xo = parity.bits(x)
+        compared = 0
+        for li, L in enumerate(layers):
+            one = bg.moe_layers([L])
+            x_chk = to_dev_bits(xo)
+            bg.moe_forward_stack(plan, x_chk, xn, T, one, alpha)
+            torch.cuda.synchronize()
+            assert bg.moe_last_gemm_path(plan) == 3
+            gidx = parity.device_view(r.topk_idx, T * k, torch.int32).cpu().numpy().reshape(T, k)
+            y_gpu = y_view.cpu().numpy().reshape(T, H)
+            o = oracle_layer_for_rows(L, orc.rmsnorm(xo), sh)
+            ok = o["gap"] >= parity.GAP_MIN
+            assert np.array_equal(gidx[ok], o["topk_idx"][ok]), li
+            if ok.any():
+                parity.check_y(y_gpu[ok].astype(np.float64), o["y"][ok])
+            compared += int(ok.sum())
+            xc = bits_f64(parity.bits(x_chk))
+            want = bits_f64(xo) + np.float64(np.float32(alpha)) * y_gpu.astype(np.float64)
+            slack = 0.5 * parity.bf16_ulp(np.maximum(np.abs(xc), np.abs(want))) * (1 + 2.0 ** -15)
+            assert np.all(np.abs(xc - want) <= slack + 1e-30), li
+            assert np.array_equal(parity.bits(xn), orc.rmsnorm(parity.bits(x_chk))) or np.all(
+                np.abs(bits_f64(parity.bits(xn)) - bits_f64(orc.rmsnorm(parity.bits(x_chk))))
+                <= parity.bf16_ulp(bits_f64(orc.rmsnorm(parity.bits(x_chk)))) + 1e-30), li
+            xo = orc.residual(xo, o["y"], alpha)
+        assert compared >= 0.9 * T * w.layers
+        assert bg.moe_get_error(plan) == 0
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("T", [1, 8])
-def test_decode_graph_replay_matches_eager(T):
+def test_decode_fused_stack_matches_layer_by_layer(T):
+    """One moe_forward_stack call over the 40 layers (the launch sequence the
+    decode benchmark replays) gives the bits of 40 one-layer calls, which the
+    chain test above compares with the oracle layer by layer."""
+    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    sh = w.shape
+    layers = stack.make_layers(w, "cuda")
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), T), 0)
+    alpha = stack.residual_alpha(w.layers)
+    try:
+        x0 = synth.decode_pool(w, 1, "cuda")[0].contiguous()
+        xn = torch.empty_like(x0)
+        a = x0.clone()
+        bg.moe_forward_stack(plan, a, xn, T, bg.moe_layers(layers), alpha)
+        b = x0.clone()
+        for L in layers:
+            bg.moe_forward_stack(plan, b, xn, T, bg.moe_layers([L]), alpha)
+        torch.cuda.synchronize()
+        assert np.array_equal(a.view(torch.int16).cpu().numpy(), b.view(torch.int16).cpu().numpy())
+        assert bg.moe_get_error(plan) == 0
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T,fused", [(1, True), (8, True), (8, False), (16, True)])
+def test_decode_graph_replay_matches_eager(T, fused):
     """The decode benchmark replays the whole 40-layer step from one CUDA
     graph; the replay gives the bits of the same calls issued eagerly (which
-    the chain test above compares with the oracle)."""
-    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    the chain tests above compare with the oracle): moe_forward_stack (the
+    fused decode layer at T <= 8, the general small-M path at T = 16), or the
+    per-layer calls."""
+    w = dataclasses.replace(synth.standard_workloads()["decode_t8_l40"], tokens=T)
     sh = w.shape
     layers = stack.make_layers(w, "cuda")
     plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
@@ -230,15 +315,23 @@ def test_decode_graph_replay_matches_eager(T):
         x = torch.empty((T, sh.hidden), dtype=torch.bfloat16, device="cuda")
         xn = torch.empty_like(x)
         y = torch.empty(x.shape, dtype=torch.float32, device="cuda")
+        arr = bg.moe_layers(layers)
+
+        def step():
+            if fused:
+                bg.moe_forward_stack(plan, x, xn, T, arr, alpha)
+            else:
+                stack.run_stack(plan, x, xn, layers, T, y, alpha)
+
         x.copy_(pool[0])
-        stack.run_stack(plan, x, xn, layers, T, y, alpha)       # warm (one-time work)
+        step()                                                 # warm (one-time work)
         torch.cuda.synchronize()
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, capture_error_mode="thread_local"):
-            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            step()
         for i in (1, 2, 3):
             x.copy_(pool[i])
-            stack.run_stack(plan, x, xn, layers, T, y, alpha)
+            step()
             torch.cuda.synchronize()
             eager = x.view(torch.int16).cpu().numpy().copy()
             x.copy_(pool[i])
