@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 OBJ = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_w4.so")
 SOURCES = ["route_kernels.cu", "gemm_tc.cu", "gemm_smallm.cu", "moe_w4_api.cu",
-           "route_noalloc.cu", "decode_fused.cu"]
+           "route_noalloc.cu", "decode_fused.cu", "gemm_tc2.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall"]
 

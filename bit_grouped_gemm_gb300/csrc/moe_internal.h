@@ -135,6 +135,17 @@ struct TcMaps {
 cudaError_t launch_gemm_tc(int mode, const GemmProblem& p, const TcMaps& maps, DevErr err,
                            int num_sms, cudaStream_t st);
 
+// Pair kernel (cta_group::2, gemm_tc2.cu): units of 256-row tiles (bmap2,
+// from launch_build_tiles256) x 256 weight rows. maps.q0/q1 (and sq0/sq1)
+// use boxes of 64 rows for the gate/up pass (mode 0) and 128 rows for the
+// down pass (mode 1).
+cudaError_t launch_gemm_tc2(int mode, const GemmProblem& p, const TcMaps& maps,
+                            const int32_t* bmap2, const int32_t* num_tiles2, int max_tiles2,
+                            DevErr err, int num_sms, cudaStream_t st);
+cudaError_t launch_build_tiles256(const int32_t* off, int E, int32_t* bmap2, int32_t* num_tiles2,
+                                  cudaStream_t st);
+bool tc2_supported();
+
 // small-M mma.sync path (decode-sized token groups). `maps` holds the packed
 // words of w0/w1 (routed) and sw0/sw1 (shared) as uint32 [rows][K/8] maps with
 // 128-byte swizzle and boxes of 32 words x smallm_rows_per_unit(mode) rows.

@@ -27,8 +27,8 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
   size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
-      err, arrive, xs, act, d, dsh, total;
-  int nblk_max, max_tiles, rows_cap;
+      bmap2, num_tiles2, err, arrive, xs, act, d, dsh, total;
+  int nblk_max, max_tiles, max_tiles2, rows_cap;
 };
 
 Layout make_layout(const moe_plan_desc& d) {
@@ -55,6 +55,9 @@ Layout make_layout(const moe_plan_desc& d) {
   L.perm = take(Tm * k * 4);
   L.inv = take(Tm * k * 4);
   L.bmap = take((size_t)L.max_tiles * 3 * 4);
+  L.max_tiles2 = (int)((Tm * k + 255) / 256 + E);
+  L.bmap2 = take((size_t)L.max_tiles2 * 3 * 4);
+  L.num_tiles2 = take(16);
   L.err = take(16);
   L.arrive = take(16);
   L.xs = take((size_t)L.rows_cap * d.hidden * 2);
@@ -78,7 +81,7 @@ moe_status check_desc(const moe_plan_desc* d) {
   if (d->top_k > d->num_experts) return MOE_ERR_INVALID_ARG;
   if (d->top_k > 32) return MOE_ERR_UNSUPPORTED;
   if (d->has_shared != 0 && d->has_shared != 1) return MOE_ERR_INVALID_ARG;
-  if (d->gemm_path < 0 || d->gemm_path > 2) return MOE_ERR_INVALID_ARG;
+  if (d->gemm_path < 0 || d->gemm_path > 3) return MOE_ERR_INVALID_ARG;
   if (d->gemm_path == 2 && !smallm_fits(d->hidden, d->inter)) return MOE_ERR_UNSUPPORTED;
   if (d->small_m_max_tokens < 0 || d->wait_limit_ms < 0) return MOE_ERR_INVALID_ARG;
   // 32-bit row/element indices inside the kernels
@@ -211,8 +214,13 @@ W4Dev dev(const moe_w4& m) { return W4Dev{m.qweight, m.scales, m.biases}; }
 int ffn_path(const moe_plan* p, int T) {
   const moe_plan_desc& d = p->d;
   const int small_max = d.small_m_max_tokens > 0 ? d.small_m_max_tokens : 16;
-  return d.gemm_path != 0 ? d.gemm_path : (T <= small_max && smallm_fits(d.hidden, d.inter) ? 2 : 1);
+  const int p0 = d.gemm_path == 3 ? 1 : d.gemm_path;
+  return p0 != 0 ? p0 : (T <= small_max && smallm_fits(d.hidden, d.inter) ? 2 : 1);
 }
+
+// Whether the tensor-core path takes the SM-pair kernel (gemm_path 3, on a
+// device that launches clusters).
+bool use_pair_gemm(const moe_plan* p) { return p->d.gemm_path == 3 && tc2_supported(); }
 
 // Routing. With `fuse_gather`, a routing launch that can also does the
 // gather of the tensor-core path (x rows into the plan's xs) and sets
@@ -397,7 +405,7 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   const int H = d.hidden, I = d.inter, E = d.num_experts, k = d.top_k;
   const int hs = d.has_shared;
   const int path = ffn_path(p, T);
-  p->last_path = path;
+  p->last_path = path == 1 && use_pair_gemm(p) ? 4 : path;
 
   cudaError_t e = check_weight_range(p, routed, shared, st);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -480,10 +488,40 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
       m1.sq0 = m1.sq1 = m1.q0;
     }
     if (!ok) return MOE_ERR_CUDA;
-    e = timed(p, 4, st, [&] { return launch_gemm_tc(0, g0, m0, p->err(), p->num_sms, st); });
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
-    e = timed(p, 5, st, [&] { return launch_gemm_tc(1, g1, m1, p->err(), p->num_sms, st); });
-    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (use_pair_gemm(p)) {
+      // 256-row tiles from the routing offsets, then both passes on SM pairs
+      // (gate/up weight boxes of 64 rows: each CTA takes 64 gate + 64 up rows)
+      int32_t* bmap2 = p->at<int32_t>(p->L.bmap2);
+      int32_t* nt2 = p->at<int32_t>(p->L.num_tiles2);
+      e = timed(p, 1, st, [&] { return launch_build_tiles256(r->offsets, E, bmap2, nt2, st); });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      TcMaps p0 = m0;
+      ok = p->qmap(&p0.q0, routed->gate.qweight, (uint64_t)E * I, H / 8, 64) &&
+           p->qmap(&p0.q1, routed->up.qweight, (uint64_t)E * I, H / 8, 64);
+      if (ok && hs)
+        ok = p->qmap(&p0.sq0, shared->gate.qweight, I, H / 8, 64) &&
+             p->qmap(&p0.sq1, shared->up.qweight, I, H / 8, 64);
+      if (!ok) return MOE_ERR_CUDA;
+      if (!hs) {
+        p0.sq0 = p0.q0;
+        p0.sq1 = p0.q1;
+      }
+      long long bound2 = ((long long)T * k + 255) / 256 + E;
+      if (bound2 > (long long)T * k) bound2 = (long long)T * k;
+      e = timed(p, 4, st, [&] {
+        return launch_gemm_tc2(0, g0, p0, bmap2, nt2, (int)bound2, p->err(), p->num_sms, st);
+      });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      e = timed(p, 5, st, [&] {
+        return launch_gemm_tc2(1, g1, m1, bmap2, nt2, (int)bound2, p->err(), p->num_sms, st);
+      });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    } else {
+      e = timed(p, 4, st, [&] { return launch_gemm_tc(0, g0, m0, p->err(), p->num_sms, st); });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+      e = timed(p, 5, st, [&] { return launch_gemm_tc(1, g1, m1, p->err(), p->num_sms, st); });
+      if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
   } else {
     const uint32_t r0 = smallm_rows_per_unit(0), r1 = smallm_rows_per_unit(1);
     SmallMaps s0{}, s1{};

@@ -90,7 +90,9 @@ typedef struct {
   int has_shared;        /* 1: one always-on shared expert with weight 1 */
   int max_tokens;        /* capacity: scratch is sized for this T, once */
   int block_m;           /* rows per block-map tile; must be 128 */
-  int gemm_path;         /* 0 auto, 1 tensor-core (tcgen05) path, 2 small-M path */
+  int gemm_path;         /* 0 auto, 1 tensor-core (tcgen05) path, 2 small-M path,
+                            3 tensor-core path on SM pairs (tcgen05 cta_group::2;
+                            falls back to 1 on a device without cluster launch) */
   int small_m_max_tokens;/* auto: T <= this uses the small-M path (default 16 if 0) */
   int wait_limit_ms;     /* device bounded-wait limit (default 1000 if 0) */
 } moe_plan_desc;
@@ -325,7 +327,7 @@ moe_status moe_read_timing(moe_plan_t plan, moe_timing* out);
 void* moe_debug_buffer(moe_plan_t plan, int which);
 
 /* Which GEMM path the last layer call took: 1 tensor-core, 2 small-M, 3 the
- * fused decode layer of moe_forward_stack. */
+ * fused decode layer of moe_forward_stack, 4 tensor-core on SM pairs. */
 int moe_last_gemm_path(moe_plan_t plan);
 
 /* Text of a status code. */

@@ -109,8 +109,11 @@ def run_layer(c: Case, plan: int):
     return y
 
 
+# gemm_path 1 and 0 (auto) take the single-SM tensor-core kernel, 3 the
+# SM-pair one, 2 the small-M kernel
 LAYER_CASES = [
-    ("t128_uniform", 1), ("t128_uniform", 2), ("t512_zipf", 0), ("t512_zipf", 2),
+    ("t128_uniform", 1), ("t128_uniform", 2), ("t128_uniform", 3), ("t512_zipf", 0),
+    ("t512_zipf", 2), ("t512_zipf", 3),
 ]
 
 
@@ -121,7 +124,7 @@ def test_layer_parity_full(name, path):
     plan = make_plan(w, path)
     try:
         y = run_layer(c, plan)
-        assert bg.moe_last_gemm_path(plan) == (path if path else 1)
+        assert bg.moe_last_gemm_path(plan) == {0: 1, 3: 4}.get(path, path)
         orc = c.oracle_layer()
         parity.check_y(y.double().cpu().numpy(), orc["y"])
     finally:
@@ -132,19 +135,25 @@ def test_layer_parity_full(name, path):
 def test_layer_parity_all_rows(name):
     """Every output row of a full-size layer against the oracle (layer 0 of
     the 40-layer stack for the 4096-token workload), so every tile of every
-    expert -- full, partial and the hot experts' many -- is compared."""
+    expert -- full, partial and the hot experts' many -- is compared; for the
+    default path and for the SM-pair tensor-core path (256-row tiles)."""
     w = WL[name]
     c = Case(w)
     plan = make_plan(w)
+    plan2 = make_plan(w, 3)
     try:
         y = run_layer(c, plan)
+        y2 = run_layer(c, plan2)
+        assert bg.moe_last_gemm_path(plan2) == 4
         orc = c.oracle_layer()
         r = bg.moe_route(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias)
         g = parity.routing_to_numpy(r, w.tokens, w.shape.top_k, w.shape.num_experts)
         assert np.array_equal(g["topk_idx"], orc["topk_idx"])
         parity.check_y(y.double().cpu().numpy(), orc["y"])
+        parity.check_y(y2.double().cpu().numpy(), orc["y"])
     finally:
         bg.moe_plan_destroy(plan)
+        bg.moe_plan_destroy(plan2)
 
 
 def _tie_bias(kind: str, E: int) -> np.ndarray:
@@ -307,7 +316,8 @@ def test_decode_sized_layer(T, path):
 
 @pytest.mark.parametrize("T,shared,path,routing", [
     (37, True, 1, "zipf"), (37, True, 2, "zipf"), (300, False, 1, "uniform"),
-    (300, False, 2, "uniform"), (129, True, 0, "zipf"),
+    (300, False, 2, "uniform"), (129, True, 0, "zipf"), (300, False, 3, "uniform"),
+    (600, True, 1, "zipf"),
 ])
 def test_small_shapes_ragged(T, shared, path, routing):
     sh = dataclasses.replace(SMALL, has_shared=shared)
@@ -369,7 +379,7 @@ def test_routing_fused_gather_matches_gather_launch(name):
         bg.moe_plan_destroy(plan)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3])
 def test_deterministic(path):
     w = WL["t512_zipf"]
     c = Case(w, gap=False)
