@@ -52,10 +52,7 @@ constexpr int kThreads = 640;
 // phase still pending, since it needs an arrival made after the wait.
 constexpr int kBStages = 8;               // token-half chunks (64 K) in flight
 constexpr int kQStages = 3;               // packed-weight chunks (256 K) in flight
-#ifndef MOE_TC2_ASTAGES
-#define MOE_TC2_ASTAGES 8
-#endif
-constexpr int kAStages = MOE_TC2_ASTAGES;   // TMEM weight stages (64 K, 32 columns)
+constexpr int kAStages = 8;               // TMEM weight stages (64 K, 32 columns)
 constexpr int kBTileBytes = 128 * 128;    // up to 128 token rows x 64 fp16
 constexpr int kQStageBytes = 128 * 128;   // 128 weight rows x 32 words
 constexpr int kOffB = 0;
@@ -248,20 +245,11 @@ __device__ __forceinline__ void mma2_f16_ts(uint32_t d_tmem, uint32_t a_tmem, ui
 // Arrive on the barrier at `bar`'s offset in both CTAs once every MMA issued
 // so far by this thread is done.
 __device__ __forceinline__ void mma2_commit_both(uint64_t* bar) {
-#ifdef MOE_TC2_COMMIT_SPLIT
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, 1;" : "=r"(remote) : "r"(smem_u32(bar)));
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-               : "memory");
-  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(remote)
-               : "memory");
-#else
   asm volatile(
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
           smem_u32(bar)),
       "h"((unsigned short)3)
       : "memory");
-#endif
 }
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
   asm volatile(
