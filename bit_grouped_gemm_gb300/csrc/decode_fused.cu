@@ -165,8 +165,13 @@ __device__ __forceinline__ uint32_t qoff(int y, int j, int c, int rows) {
 __device__ unsigned long long g_dec_trace[256][16];
 #define DEC_TRACE(i) \
   if (threadIdx.x == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][(i)] = globaltimer_ns()
+// finer marks inside phases 1 and 2
+__device__ unsigned long long g_dec_trace2[256][8];
+#define DEC_TRACE2(i) \
+  if (threadIdx.x == 0 && blockIdx.x < 256) g_dec_trace2[blockIdx.x][(i)] = globaltimer_ns()
 #else
 #define DEC_TRACE(i)
+#define DEC_TRACE2(i)
 #endif
 
 // Reduce-scatter of N partial sums over the 32 lanes of a warp by halving
@@ -240,6 +245,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   __shared__ float pr_w[kWarps][kMaxT * EPC];
   __shared__ float x_s[kMaxT][kDn];
   __shared__ int nslots_s, flag_s, abort_s;
+  __shared__ int scan_a[kWarps], scan_c[kWarps];
+  __shared__ float rinv_s[kMaxT];
 
   const int H = p.H, I = p.I, E = p.E, T = p.T, k = p.k;
   const int G = H / 64, GI = I / 64;
@@ -372,21 +379,22 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       for (int o = 16; o > 0; o >>= 1) ss[t] += __shfl_xor_sync(0xffffffffu, ss[t], o);
       if (lane == 0) ss_w[warp][t] = ss[t];
     }
+  DEC_TRACE2(0);
   if (own_x) x_s[tid / kDn][tid % kDn] = xo;
+  __syncthreads();
+  DEC_TRACE2(1);
+  // each token's 1 / rms once (thread t), shared with the block
+  if (tid < T) {
+    float tot = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) tot += ss_w[w][tid];
+    rinv_s[tid] = 1.0f / sqrtf(tot / (float)H + p.eps);
+  }
   __syncthreads();
   float rinv[kMaxT];
 #pragma unroll
-  for (int t = 0; t < kMaxT; ++t) {
-    float tot = 0.f;
-    if (t < T)
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) tot += ss_w[w][t];
-    rinv[t] = 1.0f / sqrtf(tot / (float)H + p.eps);
-  }
-  if (router_cta && !mbar_wait_drain(&wbar, 0, p.err.limit_ns)) {
-    if (lane == 0) report_timeout(p.err, 44);
-    abort_s = 1;
-  }
+  for (int t = 0; t < kMaxT; ++t) rinv[t] = t < T ? rinv_s[t] : 0.f;
+  DEC_TRACE2(2);
   // xn = bf16(x * rinv): fp16 operand rows (perm8 K order) and their group
   // sums; router partial sums over this thread's hidden indices
   float pr[kMaxT * EPC];
@@ -425,28 +433,39 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     }
   }
   report_range_warp(p.err, over != 0u);
+  DEC_TRACE2(3);
   if (router_cta) {
     // router partials: thread tid takes hidden rows tid, tid + 256, ... so
-    // that a warp reads consecutive rows of the weight slice and of xn
+    // that a warp reads consecutive rows of the weight slice and of xn. The
+    // slice's copy (thousands of 16-byte rows) was issued at launch; the
+    // operand rows above were built while it landed.
+    if (!mbar_wait_drain(&wbar, 0, p.err.limit_ns)) {
+      if (lane == 0) report_timeout(p.err, 44);
+      abort_s = 1;
+    }
     __syncthreads();
-    for (int h = tid; h < H; h += kThreads) {
-      const uint16_t* wrow = wrs + (size_t)h * kRBoxE + ecol;
-      float wv[EPC];
+    {
+#pragma unroll 8
+      for (int h = tid; h < H; h += kThreads) {
+        const uint16_t* wrow = wrs + (size_t)h * kRBoxE + ecol;
+        float wv[EPC];
 #pragma unroll
-      for (int q = 0; q < EPC / 2; ++q) {
-        const uint32_t w2 = reinterpret_cast<const uint32_t*>(wrow)[q];
-        wv[2 * q] = bf16_lo(w2);
-        wv[2 * q + 1] = bf16_hi(w2);
-      }
-#pragma unroll
-      for (int t = 0; t < kMaxT; ++t)
-        if (t < T) {
-          const float xv = bf16_to_f32(xb[(size_t)t * H + h]);
-#pragma unroll
-          for (int q = 0; q < EPC; ++q) pr[t * EPC + q] = fmaf(xv, wv[q], pr[t * EPC + q]);
+        for (int q = 0; q < EPC / 2; ++q) {
+          const uint32_t w2 = reinterpret_cast<const uint32_t*>(wrow)[q];
+          wv[2 * q] = bf16_lo(w2);
+          wv[2 * q + 1] = bf16_hi(w2);
         }
+#pragma unroll
+        for (int t = 0; t < kMaxT; ++t)
+          if (t < T) {
+            const float xv = bf16_to_f32(xb[(size_t)t * H + h]);
+#pragma unroll
+            for (int q = 0; q < EPC; ++q) pr[t * EPC + q] = fmaf(xv, wv[q], pr[t * EPC + q]);
+          }
+      }
     }
   }
+  DEC_TRACE2(4);
   // the zero token row (columns of a tile past its tokens)
   for (int i = tid; i < (int)L.xstride; i += kThreads) xw[kMaxT * L.xstride + i] = 0u;
   for (int i = tid; i < G; i += kThreads) xg[kMaxT * G + i] = 0.f;
@@ -462,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     }
   }
   __syncthreads();
+  DEC_TRACE2(5);
   if (router_cta && tid < T * EPC) {
     const int t = tid / EPC, q = tid % EPC;
     float v = 0.f;
@@ -492,50 +512,70 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     }
   }
   __syncthreads();
-  if (warp == 0) {
+  DEC_TRACE2(6);
+  {
     // slots: 0 = shared (if any), then the selected experts in ascending
-    // order, each with its tokens in ascending order
-    int base = p.has_shared;
-    for (int eb = 0; eb < E; eb += 32) {
-      const int e = eb + lane;
-      const unsigned m = e < E ? tmask_s[e] : 0u;
-      const unsigned act = __ballot_sync(0xffffffffu, m != 0u);
+    // order, each with its tokens in ascending order; activation row offsets
+    // likewise. One block-wide scan: thread i takes experts 2i and 2i + 1
+    // and counts (selected experts, their tokens) up to itself.
+    const int ea = 2 * tid, eb = 2 * tid + 1;
+    const unsigned ma = ea < E ? tmask_s[ea] : 0u, mb = eb < E ? tmask_s[eb] : 0u;
+    const int na = (ma != 0u) + (mb != 0u), nc = __popc(ma) + __popc(mb);
+    int ia = na, ic = nc;   // inclusive scans over the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int xa = __shfl_up_sync(0xffffffffu, ia, o), xc = __shfl_up_sync(0xffffffffu, ic, o);
+      if (lane >= o) {
+        ia += xa;
+        ic += xc;
+      }
+    }
+    if (lane == 31) {
+      scan_a[warp] = ia;
+      scan_c[warp] = ic;
+    }
+    __syncthreads();
+    int pa = 0, pc = 0, ta = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const int va = scan_a[w];
+      if (w < warp) {
+        pa += va;
+        pc += scan_c[w];
+      }
+      ta += va;
+    }
+    int sl = p.has_shared + pa + ia - na;          // first slot of this thread's experts
+    int so = p.has_shared * T + pc + ic - nc;       // their first activation row
+    const unsigned mm[2] = {ma, mb};
+#pragma unroll
+    for (int q = 0; q < 2; ++q) {
+      const unsigned m = mm[q];
       if (m) {
-        const int sl = base + __popc(act & ((1u << lane) - 1u));
+        const int e = ea + q;
         slot_of_s[e] = sl;
         slot_e[sl] = e;
         cnt_s[sl] = __popc(m);
+        soff_s[sl] = so;
         int col = 0;
         for (int t = 0; t < T; ++t)
           if (m & (1u << t)) tok_s[sl][col++] = t;
+        ++sl;
+        so += __popc(m);
       }
-      base += __popc(act);
     }
-    if (p.has_shared && lane < T) tok_s[0][lane] = lane;
-    if (lane == 0) {
-      nslots_s = base;
+    if (tid == 0) {
+      nslots_s = p.has_shared + ta;
       if (p.has_shared) {
         slot_e[0] = -1;
         cnt_s[0] = T;
+        soff_s[0] = 0;
       }
     }
-    __syncwarp();
-    // activation row offsets (exclusive scan of the slots' token counts)
-    int carry = 0;
-    for (int s0 = 0; s0 < base; s0 += 32) {
-      const int sl = s0 + lane;
-      const int v = sl < base ? cnt_s[sl] : 0;
-      int inc = v;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, inc, o);
-        if (lane >= o) inc += n;
-      }
-      if (sl < base) soff_s[sl] = carry + inc - v;
-      carry += __shfl_sync(0xffffffffu, inc, 31);
-    }
+    if (p.has_shared && tid < T) tok_s[0][tid] = tid;
   }
   __syncthreads();
+  DEC_TRACE2(7);
   n_units = nslots_s * upe;
   n_gu = cta < n_units ? (n_units - cta + ncta - 1) / ncta : 0;
   n_dc = cta < p.n_dn ? (nslots_s + kSlotsPerChunk - 1) / kSlotsPerChunk : 0;
@@ -889,6 +929,9 @@ drain:
 #ifdef MOE_DEC_TRACE
 extern "C" int moe_debug_dec_trace(unsigned long long* out) {
   return (int)cudaMemcpyFromSymbol(out, dec::g_dec_trace, sizeof(dec::g_dec_trace));
+}
+extern "C" int moe_debug_dec_trace2(unsigned long long* out) {
+  return (int)cudaMemcpyFromSymbol(out, dec::g_dec_trace2, sizeof(dec::g_dec_trace2));
 }
 #endif
 
