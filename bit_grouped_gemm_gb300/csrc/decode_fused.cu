@@ -58,6 +58,7 @@ constexpr int kRBoxE = 8;           // router weight columns per TMA box (16-byt
 constexpr int kIssuer = 224;        // the thread that issues the ring's copies (warp 7, lane 0)
 constexpr int kRedStride = 9;       // floats per (warp, lane) in the split-K reduction (padded)
 constexpr int kRBox = 256;          // router weight rows per TMA box
+constexpr int kGB = 4;              // K groups per batch of a gate/up warp's loads and MMAs
 
 struct Params {
   int T, H, I, E, k, has_shared;
@@ -625,45 +626,44 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
       for (int q = 0; q < 4; ++q) tot[mt][q] = 0.f;
-    // this warp's K groups, four at a time: every shared-memory operand of
-    // the four is loaded before the first MMA, so their chains overlap
+    // this warp's K groups, kGB at a time: every shared-memory operand of a
+    // batch is loaded before its first MMA, so their chains overlap
     const int gpw = G / kWarps;   // a multiple of 4 (host-checked)
-    for (int gb = 0; gb < gpw; gb += 4) {
-      uint2 qw[4][2][2];
-      uint32_t bf[4][4][2];
-      float sc[4][2][2], cb[4][2][2], xs0[4], xs1[4];
-      // groups warp*gpw + gb .. + 3 are the 4 groups of one 32-word chunk
-      const uint32_t zb = bq + (uint32_t)((warp * gpw + gb) >> 2) * (kRu * 128);
+    for (int gb = 0; gb < gpw; gb += kGB) {
+      uint2 qw[kGB][2][2];
+      uint32_t bf[kGB][4][2];
+      float sc[kGB][2][2], cb[kGB][2][2], xs0[kGB], xs1[kGB];
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi) {
-        const bool v = true;
+      for (int gi = 0; gi < kGB; ++gi) {
         const int grp = warp * gpw + gb + gi;
-        const uint32_t col = (uint32_t)(((2 * gi + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
+        // group grp is group grp % 4 of 32-word chunk grp / 4
+        const uint32_t zb = bq + (uint32_t)(grp >> 2) * (kRu * 128);
+        const uint32_t col = (uint32_t)(((2 * (grp & 3) + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
             qw[gi][mt][h] = lds_v2(zb + mt * gu_q + (uint32_t)((g + 8 * h) * 128) + col);
             const int row = g + 8 * h;
-            const float s1 = v ? bf16_to_f32(sb[(2 * mt) * (kRu * G) + row * G + grp]) : 0.f;
-            const float b1 = v ? bf16_to_f32(sb[(2 * mt + 1) * (kRu * G) + row * G + grp]) : 0.f;
+            const float s1 = bf16_to_f32(sb[(2 * mt) * (kRu * G) + row * G + grp]);
+            const float b1 = bf16_to_f32(sb[(2 * mt + 1) * (kRu * G) + row * G + grp]);
             sc[gi][mt][h] = s1;
             cb[gi][mt][h] = fmaf(-1024.0f, s1, b1);
           }
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
           const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
-          bf[gi][st][0] = v ? xr[4 * wabs + psel] : 0u;
-          bf[gi][st][1] = v ? xr[4 * wabs + psel + 1] : 0u;
+          bf[gi][st][0] = xr[4 * wabs + psel];
+          bf[gi][st][1] = xr[4 * wabs + psel + 1];
         }
-        xs0[gi] = v ? xg[t0 * G + grp] : 0.f;
-        xs1[gi] = v ? xg[t1 * G + grp] : 0.f;
+        xs0[gi] = xg[t0 * G + grp];
+        xs1[gi] = xg[t1 * G + grp];
       }
-      // 8 independent accumulator chains (4 groups x gate/up), k-step
+      // 2 kGB independent accumulator chains (groups x gate/up), k-step
       // outermost so that consecutive MMAs never depend on each other
-      float acc[4][2][4];
+      float acc[kGB][2][4];
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi)
+      for (int gi = 0; gi < kGB; ++gi)
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -672,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       for (int st = 0; st < 4; ++st) {
         const int psel = 2 * (st & 1);
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi)
+        for (int gi = 0; gi < kGB; ++gi)
 #pragma unroll
           for (int mt = 0; mt < 2; ++mt) {
             const uint32_t w0 = (st >> 1) ? qw[gi][mt][0].y : qw[gi][mt][0].x;
@@ -683,7 +683,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
           }
       }
 #pragma unroll
-      for (int gi = 0; gi < 4; ++gi)
+      for (int gi = 0; gi < kGB; ++gi)
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
