@@ -170,10 +170,7 @@ __device__ __forceinline__ bool try_wait_cluster(uint64_t* bar, uint32_t parity,
 
 // Suspend-time hint of the waits: a thread whose phase is not complete
 // sleeps at most this long before it looks again.
-#ifndef MOE_TC2_WAIT_HINT_NS
-#define MOE_TC2_WAIT_HINT_NS 100000
-#endif
-constexpr uint32_t kHintNs = MOE_TC2_WAIT_HINT_NS;
+constexpr uint32_t kHintNs = 100000;
 
 #ifdef MOE_TC2_STATS
 // Profiling build only: cycles spent in each wait site (site - 50), summed
