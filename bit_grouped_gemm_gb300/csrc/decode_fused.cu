@@ -23,17 +23,17 @@
 //      routing kernels, so every CTA holds the same routing) and numbers the
 //      active experts in ascending order: slot 0 the shared expert, then one
 //      slot per selected routed expert with its list of tokens;
-//   3. gate/up units (16 gate + 16 up rows of one slot's expert) are dealt to
-//      CTAs round-robin; their packed rows arrive by TMA (3D boxes, 128-byte
-//      swizzle: one request per matrix) into a ring of shared-memory buffers,
-//      and the shared expert's first unit is fetched before the previous
-//      launch ends. mma.sync with the exact affine split
+//   3. gate/up units (8 gate + the matching 8 up rows of one slot's expert,
+//      one m16 tile) are dealt to warps over the whole grid; each warp takes
+//      its unit's packed rows by TMA (3D boxes of 8 rows x all K, 128-byte
+//      swizzle) into its own shared-memory buffer and runs
+//      mma.sync with the exact affine split
 //          sum_k w_k x_k = s sum_k (1024+q_k) x_k + (b - 1024 s) sum_k x_k
-//      per group of 64, split K over the 8 warps, SwiGLU in FP32, activations
-//      stored as fp16 rows per (slot, token);
+//      per group of 64, SwiGLU in FP32 registers, activations stored as fp16
+//      rows per (slot, token); no block barrier per unit;
 //   -- barrier 2 (all activations written) --
 //   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
-//      those 16 down rows (fetched into the ring while step 3 ran) by the
+//      those 16 down rows (prefetched into L2 during step 3) by the
 //      slot's activation rows, then forms
 //          y[t] = shared[t] + sum_j w[t][j] * expert_j[t]   (FP32, j in rank order)
 //      and updates x[t] = bf16(x[t] + alpha * y[t]) in place.
@@ -50,15 +50,15 @@ constexpr int kThreads = 256;
 constexpr int kWarps = 8;
 constexpr int kMaxT = 8;            // tokens
 constexpr int kMaxSlots = 80;       // shared + distinct routed experts
-constexpr int kRu = 16;             // gate rows (and up rows) per unit
+constexpr int kGU = 8;              // gate rows (and the matching up rows) per unit: one m16 tile
+// a gate/up warp's buffer: its unit's 8 gate and 8 up rows, all K (H / 2 bytes a row)
+__host__ __device__ constexpr uint32_t unit_bytes(int H) { return 2u * kGU * (uint32_t)H / 2; }
 constexpr int kDn = 16;             // down rows (output columns) per CTA
 constexpr int kSlotsPerChunk = 8;   // down slabs per ring buffer (one per warp)
 constexpr int kRing = 4;            // shared-memory slab buffers
 constexpr int kRBoxE = 8;           // router weight columns per TMA box (16-byte rows)
 constexpr int kIssuer = 224;        // the thread that issues the ring's copies (warp 7, lane 0)
-constexpr int kRedStride = 9;       // floats per (warp, lane) in the split-K reduction (padded)
 constexpr int kRBox = 256;          // router weight rows per TMA box
-constexpr int kGB = 4;              // K groups per batch of a gate/up warp's loads and MMAs
 
 struct Params {
   int T, H, I, E, k, has_shared;
@@ -68,7 +68,8 @@ struct Params {
   const uint16_t* wr;        // router weight bf16 [H][E]
   const float* rbias;        // [E] or null
   W4Dev gate, up, down, sgate, sup, sdown;   // scales and biases (words via the maps)
-  CUtensorMap mg, mu, md, msg, msu, msd;     // packed words, 3D boxes (32 words, rows, K/256)
+  CUtensorMap mg, mu, msg, msu;   // gate/up packed words, 3D boxes (32 words, 8 rows, K/256)
+  CUtensorMap md, msd;             // down packed words, 3D boxes (32 words, 16 rows, K/256)
   CUtensorMap mr;            // router weight bf16 [H][E], boxes of 8 experts x 256 rows
   float* logits;             // [T][E]
   uint16_t* act;             // [rows][I] fp16, K order perm8 (row = slot offset + token)
@@ -83,19 +84,20 @@ struct Params {
 
 // Byte offsets of the dynamic shared memory (from a 1024-aligned base).
 struct Smem {
-  uint32_t slab, xw, xstride, xg, wr, red, total, dsum_cap;
+  uint32_t slab, xw, xstride, xg, wr, total, dsum_cap;
 };
 
 __host__ __device__ inline uint32_t align_u(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 // The router slice (H x 8 bf16: the 16-byte box holding this CTA's columns)
-// lives in the last ring buffer, which the ring does not use before the
-// routing is known.
+// lives in the last ring buffer and the router's bf16 token rows in buffer 1,
+// both before the routing is known; then the gate/up warps' unit buffers
+// (kWarps x unit_bytes) take the whole ring, and after them the down slabs.
 __host__ __device__ inline Smem smem_layout(int H, int I) {
   Smem L;
-  const uint32_t gu = 2u * kRu * (H / 2) + 4u * kRu * (H / 64) * 2;
   const uint32_t dn = kSlotsPerChunk * (kDn * (I / 2) + 2u * kDn * (I / 64) * 2);
-  L.slab = align_u(gu > dn ? gu : dn, 1024);
+  const uint32_t gu = (kWarps * unit_bytes(H) + kRing - 1) / kRing;
+  L.slab = align_u(dn > gu ? dn : gu, 1024);
   uint32_t o = kRing * L.slab;
   L.xw = o;
   L.xstride = H / 2 + 1;                       // words per token row (padded)
@@ -106,8 +108,6 @@ __host__ __device__ inline Smem smem_layout(int H, int I) {
   o += (kMaxT + 1) * (H / 64) * 4;
   o = align_u(o, 16);
   L.wr = (kRing - 1) * L.slab;
-  L.red = o;
-  o += 2 * kWarps * 32 * kRedStride * 4;
   L.total = o;
   return L;
 }
@@ -120,10 +120,14 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 
 // Grid barrier: every CTA adds one arrival, then waits (bounded) until the
 // counter reaches `target`. Returns false on timeout (error latched).
+// `during` runs on the other threads while thread 0 arrives and waits.
+template <class F>
 __device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, int site,
-                             int* flag_s) {
+                             int* flag_s, F&& during) {
   __syncthreads();
-  if (threadIdx.x == 0) {
+  if (threadIdx.x != 0) {
+    during();
+  } else {
     __threadfence();
     atomicAdd(bar, 1u);
     int ok = 1;
@@ -143,6 +147,11 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, 
   }
   __syncthreads();
   return *flag_s != 0;
+}
+
+__device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, int site,
+                             int* flag_s) {
+  return grid_barrier(bar, target, err, site, flag_s, [] {});
 }
 
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
@@ -234,6 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   __shared__ __align__(8) uint64_t full[kRing];
+  __shared__ __align__(8) uint64_t wfull[kWarps];   // gate/up warps' unit buffers
   __shared__ __align__(8) uint64_t wbar;       // router slice landed
   __shared__ int idx_s[kMaxT][32];
   __shared__ float w_s[kMaxT][32];
@@ -260,21 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   float* xg = reinterpret_cast<float*>(smem + L.xg);
   const uint16_t* wrs = reinterpret_cast<const uint16_t*>(smem + L.wr);
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.slab);   // xn bf16 [T][H] (ring buffer 1)
-  float* red = reinterpret_cast<float*>(smem + L.red);
-  const int upe = I / kRu;                     // gate/up units per slot
-  const uint32_t gu_q = (uint32_t)kRu * (H / 2), gu_s = (uint32_t)kRu * G * 2;
+  const int upe = I / kGU;                     // gate/up units per slot
   const uint32_t dn_q = (uint32_t)kDn * (I / 2), dn_s = (uint32_t)kDn * GI * 2;
   const int e0 = cta * EPC;                    // this CTA's router columns [e0, e0 + EPC)
   const bool router_cta = e0 < E;
   const int ebox = e0 & ~(kRBoxE - 1), ecol = e0 - ebox;   // the 16-byte box holding them
 
-#ifdef MOE_DEC_TRACE
-  unsigned long long tr_wait, tr_comp, tr_mark;
-#endif
   DEC_TRACE(0);
   // ------------------------------------------------ prologue (weights only)
   if (tid == 0) {
     for (int b = 0; b < kRing; ++b) mbar_init(&full[b], 1);
+    for (int w = 0; w < kWarps; ++w) mbar_init(&wfull[w], 1);
     mbar_init(&wbar, 1);
     fence_mbar_init();
     tma_prefetch_desc(&p.mg);
@@ -294,50 +300,30 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   }
   __syncthreads();
 
-  // The ring: item i (gate/up units first, then down chunks) goes to buffer
-  // i % kRing; one elected thread issues its copies when the buffer is free.
-  int n_units = 0, n_gu = 0, n_dc = 0;   // set once the routing is known
-  int issued = 0;                        // items issued so far (thread 0), a prefix
+  // The ring of down slabs: chunk i (kSlotsPerChunk slots' 16 down rows) goes
+  // to buffer i % kRing once the gate/up units are done with the ring; one
+  // elected thread issues its copies when the buffer is free.
+  int n_units = 0, n_dc = 0;             // set once the routing is known
+  int issued = 0;                        // chunks issued so far (kIssuer), a prefix
+  auto ring_buf = [](int i) { return i % kRing; };
   auto issue = [&](int i) {
-    const int b = i % kRing;
+    const int b = ring_buf(i);
     issued = i + 1;
     uint8_t* buf = smem + (size_t)b * L.slab;
-    if (i < n_gu) {
-      const int u = cta + i * ncta, s = u / upe, r = u - s * upe;
+    const int s0 = kSlotsPerChunk * i;
+    const int ns = min(kSlotsPerChunk, nslots_s - s0);
+    mbar_arrive_expect_tx(&full[b], (uint32_t)ns * (dn_q + 2 * dn_s));
+    for (int q = 0; q < ns; ++q) {
+      const int s = s0 + q;
       const bool sh = p.has_shared && s == 0;
-      const int row0 = (sh ? 0 : slot_e[s] * I) + kRu * r;
-      const W4Dev& wg = sh ? p.sgate : p.gate;
-      const W4Dev& wu = sh ? p.sup : p.up;
-      mbar_arrive_expect_tx(&full[b], 2 * gu_q + 4 * gu_s);
-      tma_load_3d(buf, sh ? &p.msg : &p.mg, 0, row0, 0, &full[b]);
-      tma_load_3d(buf + gu_q, sh ? &p.msu : &p.mu, 0, row0, 0, &full[b]);
-      bulk_load(buf + 2 * gu_q, wg.s + (size_t)row0 * G, gu_s, &full[b]);
-      bulk_load(buf + 2 * gu_q + gu_s, wg.b + (size_t)row0 * G, gu_s, &full[b]);
-      bulk_load(buf + 2 * gu_q + 2 * gu_s, wu.s + (size_t)row0 * G, gu_s, &full[b]);
-      bulk_load(buf + 2 * gu_q + 3 * gu_s, wu.b + (size_t)row0 * G, gu_s, &full[b]);
-    } else {
-      const int ch = i - n_gu, s0 = kSlotsPerChunk * ch;
-      const int ns = min(kSlotsPerChunk, nslots_s - s0);
-      mbar_arrive_expect_tx(&full[b], (uint32_t)ns * (dn_q + 2 * dn_s));
-      for (int q = 0; q < ns; ++q) {
-        const int s = s0 + q;
-        const bool sh = p.has_shared && s == 0;
-        const int row0 = (sh ? 0 : slot_e[s] * H) + kDn * cta;
-        const W4Dev& wd = sh ? p.sdown : p.down;
-        tma_load_3d(buf + q * dn_q, sh ? &p.msd : &p.md, 0, row0, 0, &full[b]);
-        bulk_load(buf + kSlotsPerChunk * dn_q + q * dn_s, wd.s + (size_t)row0 * GI, dn_s, &full[b]);
-        bulk_load(buf + kSlotsPerChunk * (dn_q + dn_s) + q * dn_s, wd.b + (size_t)row0 * GI, dn_s,
-                  &full[b]);
-      }
+      const int row0 = (sh ? 0 : slot_e[s] * H) + kDn * cta;
+      const W4Dev& wd = sh ? p.sdown : p.down;
+      tma_load_3d(buf + q * dn_q, sh ? &p.msd : &p.md, 0, row0, 0, &full[b]);
+      bulk_load(buf + kSlotsPerChunk * dn_q + q * dn_s, wd.s + (size_t)row0 * GI, dn_s, &full[b]);
+      bulk_load(buf + kSlotsPerChunk * (dn_q + dn_s) + q * dn_s, wd.b + (size_t)row0 * GI, dn_s,
+                &full[b]);
     }
   };
-  // The shared expert's units come first and need no routing: a CTA whose
-  // first unit is one starts its copy now (slot 0 is always the shared one).
-  const bool early0 = p.has_shared && cta < upe;
-  if (early0 && tid == kIssuer) {
-    n_gu = 1;
-    issue(0);
-  }
 
   DEC_TRACE(1);
   pdl_begin();   // x and everything below come from the previous launch
@@ -578,10 +564,16 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   __syncthreads();
   DEC_TRACE2(7);
   n_units = nslots_s * upe;
-  n_gu = cta < n_units ? (n_units - cta + ncta - 1) / ncta : 0;
   n_dc = cta < p.n_dn ? (nslots_s + kSlotsPerChunk - 1) / kSlotsPerChunk : 0;
-  if (tid == kIssuer)
-    for (int i = (early0 ? 1 : 0); i < kRing && i < n_gu + n_dc; ++i) issue(i);
+  if (tid == kIssuer && n_dc > 0)   // the down slabs into L2 while the gate/up units run
+    for (int s = 0; s < nslots_s; ++s) {
+      const bool sh = p.has_shared && s == 0;
+      const size_t row0 = (size_t)(sh ? 0 : slot_e[s] * H) + kDn * cta;
+      const W4Dev& wd = sh ? p.sdown : p.down;
+      bulk_prefetch_l2(wd.q + row0 * (I / 8), dn_q);
+      bulk_prefetch_l2(wd.s + row0 * GI, dn_s);
+      bulk_prefetch_l2(wd.b + row0 * GI, dn_s);
+    }
   DEC_TRACE(5);
   for (int i = tid; i < T * k; i += kThreads) {   // used by the combine, after later barriers
     const int t = i / k, j = i - t * k, e = idx_s[t][j];
@@ -589,164 +581,167 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   }
 
   // ----------------------------------------------- 3. gate/up + SwiGLU units
-#ifdef MOE_DEC_TRACE
-  tr_wait = 0;
-  tr_comp = 0;
-  tr_mark = globaltimer_ns();
-  if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][14] = g_dec_trace[blockIdx.x][15] = 0;
-#endif
-  for (int i = 0; i < n_gu; ++i) {
-    const int b = i % kRing;
-    if (!mbar_wait_drain(&full[b], (uint32_t)((i / kRing) & 1), p.err.limit_ns)) {
-      if (lane == 0) report_timeout(p.err, 41);
-      abort_s = 1;
+  // One warp per unit: 8 gate rows and the matching 8 up rows of one slot's
+  // expert (an m16 tile: row g is gate feature g, row g + 8 its up feature),
+  // all K, with the exact affine split per group of 64 and SwiGLU in
+  // registers -- no reduction across warps, no block barrier per unit. Units
+  // are dealt over the CTAs first (unit u: CTA u % ncta, warp u / ncta), so
+  // every SM takes a share; a warp's unit arrives by TMA in two 3D boxes
+  // (8 rows x all K, 128-byte swizzle) into its own buffer, and the scales
+  // and biases are read from global memory a 256-K stage ahead.
+  {
+    const int nw = ncta * kWarps, wrank = warp * ncta + cta;   // this warp's place in the deal
+    const int nst = H / 256;                                   // 256-K stages per unit
+    const int my_units = wrank < n_units ? (n_units - wrank + nw - 1) / nw : 0;
+    const uint32_t ub = unit_bytes(H);
+    uint8_t* wb = smem + (size_t)warp * ub;                    // in the ring's buffers
+    const uint32_t wbase = smem_u32(wb);
+    uint64_t* wf = &wfull[warp];
+    auto wissue = [&](int ui) {   // lane 0: unit ui of this warp's deal
+      const int uu = wrank + ui * nw, s = uu / upe, r = uu - s * upe;
+      const bool sh = p.has_shared && s == 0;
+      const int row0 = (sh ? 0 : slot_e[s] * I) + kGU * r;
+      mbar_arrive_expect_tx(wf, ub);
+      tma_load_3d(wb, sh ? &p.msg : &p.mg, 0, row0, 0, wf);
+      tma_load_3d(wb + ub / 2, sh ? &p.msu : &p.mu, 0, row0, 0, wf);
+    };
+    if (lane == 0 && my_units > 0) {
+      wissue(0);
+      if (my_units > 1) {   // the second unit's rows into L2 while the first computes
+        const int uu = wrank + nw, s = uu / upe, r = uu - s * upe;
+        const bool sh = p.has_shared && s == 0;
+        const size_t row0 = (size_t)(sh ? 0 : slot_e[s] * I) + kGU * r;
+        bulk_prefetch_l2((sh ? p.sgate : p.gate).q + row0 * (H / 8), ub / 2);
+        bulk_prefetch_l2((sh ? p.sup : p.up).q + row0 * (H / 8), ub / 2);
+      }
     }
-    // (also: every warp has finished the epilogue of unit i - 2, which used
-    // the reduction buffer this unit writes)
-    __syncthreads();
-#ifdef MOE_DEC_TRACE
-    {
-      const unsigned long long now = globaltimer_ns();
-      tr_wait += now - tr_mark;
-      tr_mark = now;
-    }
-#endif
-    if (abort_s) goto drain;
-    const int u = cta + i * ncta, s = u / upe, r = u - s * upe;
-    const int cnt = cnt_s[s];
-    const uint32_t bq = sbase + (uint32_t)b * L.slab;
-    const uint16_t* sb = reinterpret_cast<const uint16_t*>(smem + (size_t)b * L.slab + 2 * gu_q);
-    // token rows of this lane's B column (g) and of its two D columns
-    const int trow = g < cnt ? tok_s[s][g] : kMaxT;
-    const int t0 = 2 * c < cnt ? tok_s[s][2 * c] : kMaxT;
-    const int t1 = 2 * c + 1 < cnt ? tok_s[s][2 * c + 1] : kMaxT;
-    const uint32_t* xr = xw + trow * L.xstride;
-    float tot[2][4];
+    bool wok = true;
+    int ui = 0;
+    for (; ui < my_units && wok; ++ui) {
+      const int uu = wrank + ui * nw, s = uu / upe, r = uu - s * upe;
+      const bool sh = p.has_shared && s == 0;
+      const int row0 = (sh ? 0 : slot_e[s] * I) + kGU * r;
+      const W4Dev& wg = sh ? p.sgate : p.gate;
+      const W4Dev& wu = sh ? p.sup : p.up;
+      const int cnt = cnt_s[s];
+      // the token of this lane's B column (g), and of its two D columns
+      const int trow = g < cnt ? tok_s[s][g] : kMaxT;
+      const int t0 = 2 * c < cnt ? tok_s[s][2 * c] : kMaxT;
+      const int t1 = 2 * c + 1 < cnt ? tok_s[s][2 * c + 1] : kMaxT;
+      const uint32_t* xr = xw + trow * L.xstride;
+      // this lane's rows: gate and up row row0 + g; their 4 groups of a stage
+      const size_t srow = (size_t)(row0 + g) * G;
+      auto ld_sb = [&](int q, uint2 (&v)[4]) {
+        v[0] = __ldg(reinterpret_cast<const uint2*>(wg.s + srow) + q);
+        v[1] = __ldg(reinterpret_cast<const uint2*>(wg.b + srow) + q);
+        v[2] = __ldg(reinterpret_cast<const uint2*>(wu.s + srow) + q);
+        v[3] = __ldg(reinterpret_cast<const uint2*>(wu.b + srow) + q);
+      };
+      uint2 sbv[4], sbn[4];
+      ld_sb(0, sbv);
+      const bool got = mbar_wait_drain(wf, (uint32_t)(ui & 1), p.err.limit_ns);
+      if (!(wok = __all_sync(0xffffffffu, got))) {   // (warp-uniform: the MMAs below are warp-wide)
+        if (lane == 0) report_timeout(p.err, 41);
+        break;
+      }
+      float tg0 = 0.f, tg1 = 0.f, tu0 = 0.f, tu1 = 0.f;   // gate and up sums, columns 2c and 2c + 1
+      for (int q = 0; q < nst; ++q) {
+        if (q + 1 < nst) ld_sb(q + 1, sbn);
+        const uint32_t zb = wbase + (uint32_t)q * (kGU * 128);   // 256-K chunk q of the gate rows
+        uint2 qw[4][2];
+        uint32_t bf[4][4][2];
+        float xs0[4], xs1[4];
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
+        for (int gi = 0; gi < 4; ++gi) {
+          const int grp = 4 * q + gi;
+          const uint32_t col = (uint32_t)(((2 * gi + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
+          qw[gi][0] = lds_v2(zb + (uint32_t)(g * 128) + col);            // gate row g
+          qw[gi][1] = lds_v2(zb + ub / 2 + (uint32_t)(g * 128) + col);   // up row g
 #pragma unroll
-      for (int q = 0; q < 4; ++q) tot[mt][q] = 0.f;
-    // this warp's K groups, kGB at a time: every shared-memory operand of a
-    // batch is loaded before its first MMA, so their chains overlap
-    const int gpw = G / kWarps;   // a multiple of 4 (host-checked)
-    for (int gb = 0; gb < gpw; gb += kGB) {
-      uint2 qw[kGB][2][2];
-      uint32_t bf[kGB][4][2];
-      float sc[kGB][2][2], cb[kGB][2][2], xs0[kGB], xs1[kGB];
-#pragma unroll
-      for (int gi = 0; gi < kGB; ++gi) {
-        const int grp = warp * gpw + gb + gi;
-        // group grp is group grp % 4 of 32-word chunk grp / 4
-        const uint32_t zb = bq + (uint32_t)(grp >> 2) * (kRu * 128);
-        const uint32_t col = (uint32_t)(((2 * (grp & 3) + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            qw[gi][mt][h] = lds_v2(zb + mt * gu_q + (uint32_t)((g + 8 * h) * 128) + col);
-            const int row = g + 8 * h;
-            const float s1 = bf16_to_f32(sb[(2 * mt) * (kRu * G) + row * G + grp]);
-            const float b1 = bf16_to_f32(sb[(2 * mt + 1) * (kRu * G) + row * G + grp]);
-            sc[gi][mt][h] = s1;
-            cb[gi][mt][h] = fmaf(-1024.0f, s1, b1);
+          for (int st = 0; st < 4; ++st) {
+            const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
+            bf[gi][st][0] = xr[4 * wabs + psel];
+            bf[gi][st][1] = xr[4 * wabs + psel + 1];
           }
+          xs0[gi] = xg[t0 * G + grp];
+          xs1[gi] = xg[t1 * G + grp];
+        }
+        float acc[4][4];
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) acc[gi][v] = 0.f;
+        // 4 independent chains (the groups), k-step outermost
 #pragma unroll
         for (int st = 0; st < 4; ++st) {
-          const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
-          bf[gi][st][0] = xr[4 * wabs + psel];
-          bf[gi][st][1] = xr[4 * wabs + psel + 1];
-        }
-        xs0[gi] = xg[t0 * G + grp];
-        xs1[gi] = xg[t1 * G + grp];
-      }
-      // 2 kGB independent accumulator chains (groups x gate/up), k-step
-      // outermost so that consecutive MMAs never depend on each other
-      float acc[kGB][2][4];
+          const int psel = 2 * (st & 1);
 #pragma unroll
-      for (int gi = 0; gi < kGB; ++gi)
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[gi][mt][q] = 0.f;
-#pragma unroll
-      for (int st = 0; st < 4; ++st) {
-        const int psel = 2 * (st & 1);
-#pragma unroll
-        for (int gi = 0; gi < kGB; ++gi)
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            const uint32_t w0 = (st >> 1) ? qw[gi][mt][0].y : qw[gi][mt][0].x;
-            const uint32_t w1 = (st >> 1) ? qw[gi][mt][1].y : qw[gi][mt][1].x;
-            mma_m16n8k16_f16(acc[gi][mt], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
+          for (int gi = 0; gi < 4; ++gi) {
+            const uint32_t w0 = (st >> 1) ? qw[gi][0].y : qw[gi][0].x;
+            const uint32_t w1 = (st >> 1) ? qw[gi][1].y : qw[gi][1].x;
+            mma_m16n8k16_f16(acc[gi], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
                              nibble_pair_1024(w0, psel + 1), nibble_pair_1024(w1, psel + 1),
                              bf[gi][st][0], bf[gi][st][1]);
           }
+        }
+        // D rows g (gate) and g + 8 (up) at columns 2c and 2c + 1; a group's
+        // share is s * sum (1024 + q) x + (b - 1024 s) * sum x
+#pragma unroll
+        for (int gi = 0; gi < 4; ++gi) {
+          auto pick = [&](const uint2& v) {
+            const uint32_t wd = (gi >> 1) ? v.y : v.x;
+            return bf16_to_f32((uint16_t)((gi & 1) ? wd >> 16 : wd & 0xFFFFu));
+          };
+          const float sg = pick(sbv[0]), su = pick(sbv[2]);
+          const float cg = fmaf(-1024.0f, sg, pick(sbv[1])), cu = fmaf(-1024.0f, su, pick(sbv[3]));
+          tg0 += fmaf(sg, acc[gi][0], cg * xs0[gi]);
+          tg1 += fmaf(sg, acc[gi][1], cg * xs1[gi]);
+          tu0 += fmaf(su, acc[gi][2], cu * xs0[gi]);
+          tu1 += fmaf(su, acc[gi][3], cu * xs1[gi]);
+        }
+        if (q + 1 < nst)
+#pragma unroll
+          for (int v = 0; v < 4; ++v) sbv[v] = sbn[v];
       }
-#pragma unroll
-      for (int gi = 0; gi < kGB; ++gi)
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            tot[mt][2 * h] += fmaf(sc[gi][mt][h], acc[gi][mt][2 * h], cb[gi][mt][h] * xs0[gi]);
-            tot[mt][2 * h + 1] += fmaf(sc[gi][mt][h], acc[gi][mt][2 * h + 1], cb[gi][mt][h] * xs1[gi]);
-          }
-    }
-#ifdef MOE_DEC_TRACE
-    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][14] += globaltimer_ns() - tr_mark;
-#endif
-    // split-K partials of the 8 warps (double-buffered by unit parity)
-    float* rbuf = red + (i & 1) * (kWarps * 32 * kRedStride);
-    float* rw = rbuf + (warp * 32 + lane) * kRedStride;
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int q = 0; q < 4; ++q) rw[mt * 4 + q] = tot[mt][q];
-    __syncthreads();   // partials complete; every read of this slab done
-#ifdef MOE_DEC_TRACE
-    if (tid == 0 && blockIdx.x < 256) g_dec_trace[blockIdx.x][15] += globaltimer_ns() - tr_mark;
-#endif
-    if (tid == kIssuer && i + kRing < n_gu + n_dc) issue(i + kRing);
-    if (warp < 4) {
-      // warp q adds (in warp order) and finishes output q of every lane:
-      // gate (partial q) and up (partial 4 + q) of row g + 8 (q / 2), column 2 c + q % 2
-      const int q = warp;
-      float gate = 0.f, up = 0.f;
-#pragma unroll
-      for (int w = 0; w < kWarps; ++w) {
-        const float* rr = rbuf + (w * 32 + lane) * kRedStride;
-        gate += rr[q];
-        up += rr[4 + q];
+      // every word of the unit has been read: the buffer takes the next unit
+      __syncwarp();
+      if (lane == 0 && ui + 1 < my_units) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        wissue(ui + 1);
       }
-      const int col = 2 * c + (q & 1), row = g + 8 * (q >> 1);
+      // SwiGLU: feature kGU r + g of the slot's tokens 2c and 2c + 1 (fp16, perm8 order)
+      const int fpos = perm8_pos(kGU * r + g);
       uint32_t big = 0u;
-      if (col < cnt) {
-        const float a = silu_fast(gate) * up;
-        big = fabsf(a) > kF16Max ? 1u : 0u;
-        p.act[(size_t)(soff_s[s] + col) * I + perm8_pos(kRu * r + row)] = f32_to_f16_sat(a);
+      if (2 * c < cnt) {
+        const float a = silu_fast(tg0) * tu0;
+        big |= fabsf(a) > kF16Max ? 1u : 0u;
+        p.act[(size_t)(soff_s[s] + 2 * c) * I + fpos] = f32_to_f16_sat(a);
+      }
+      if (2 * c + 1 < cnt) {
+        const float a = silu_fast(tg1) * tu1;
+        big |= fabsf(a) > kF16Max ? 1u : 0u;
+        p.act[(size_t)(soff_s[s] + 2 * c + 1) * I + fpos] = f32_to_f16_sat(a);
       }
       report_range_warp(p.err, big != 0u);
     }
-#ifdef MOE_DEC_TRACE
-    {
-      const unsigned long long now = globaltimer_ns();
-      tr_comp += now - tr_mark;
-      tr_mark = now;
+    if (!wok) {
+      // this warp's own copy (unit ui, issued) lands before the CTA gives up
+      mbar_wait_drain(wf, (uint32_t)(ui & 1), p.err.limit_ns);
+      if (lane == 0) abort_s = 1;
     }
-#endif
   }
-#ifdef MOE_DEC_TRACE
-  if (tid == 0 && blockIdx.x < 256) {
-    g_dec_trace[blockIdx.x][9] = tr_wait;
-    g_dec_trace[blockIdx.x][10] = tr_comp;
-    g_dec_trace[blockIdx.x][11] = (unsigned long long)n_gu;
-  }
-#endif
 
   DEC_TRACE(6);
-  ok = grid_barrier(p.bar, 2u * ncta, p.err, 42, &flag_s);
+  // the down slabs (in L2 by now) are issued while thread 0 takes barrier 2:
+  // every warp's unit buffer (the whole ring) has been read at its first sync
+  ok = grid_barrier(p.bar, 2u * ncta, p.err, 42, &flag_s, [&] {
+    if (tid == kIssuer && !abort_s) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int i = 0; i < kRing && i < n_dc; ++i) issue(i);
+    }
+  });
   DEC_TRACE(7);
-  if (!ok) goto drain;
+  if (!ok || abort_s) goto drain;
 
   // ------------------------------------------ 4. down, combine, stack update
   // HBM is idle from here on: pull the next layer's routing-independent
@@ -858,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       load_act(warp, cur);
       for (int s = warp; s < nslots_s; s += kSlotsPerChunk) {
         load_act(s + kSlotsPerChunk, nxt);
-        const int i = n_gu + s / kSlotsPerChunk, b = i % kRing;
+        const int i = s / kSlotsPerChunk, b = ring_buf(i);
         if (!mbar_wait_drain(&full[b], (uint32_t)((i / kRing) & 1), p.err.limit_ns)) {
           if (lane == 0) report_timeout(p.err, 43);
           abort_s = 1;
@@ -873,7 +868,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     } else {
       // more chunks than buffers: chunk by chunk, reusing buffers
       for (int ch = 0; ch < n_dc; ++ch) {
-        const int i = n_gu + ch, b = i % kRing;
+        const int i = ch, b = ring_buf(i);
         uint4 cur[16];
         const int s = kSlotsPerChunk * ch + warp;
         load_act(s, cur);
@@ -885,7 +880,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
         if (abort_s) goto drain;
         if (s < nslots_s) down_slot(s, b, warp, cur);
         __syncthreads();
-        if (tid == kIssuer && i + kRing < n_gu + n_dc) issue(i + kRing);
+        if (tid == kIssuer && i + kRing < n_dc) issue(i + kRing);
       }
     }
 #ifdef MOE_DEC_TRACE
@@ -917,8 +912,8 @@ drain:
   if (tid == 0 && router_cta) mbar_wait_drain(&wbar, 0, p.err.limit_ns);
   if (tid == kIssuer) {
     for (int b = 0; b < kRing && b < issued; ++b) {
-      const int last = b + ((issued - 1 - b) / kRing) * kRing;   // last item in buffer b
-      mbar_wait_drain(&full[b], (uint32_t)((last / kRing) & 1), p.err.limit_ns);
+      const int last = b + ((issued - 1 - b) / kRing) * kRing;   // last chunk i = b (mod kRing)
+      mbar_wait_drain(&full[ring_buf(b)], (uint32_t)((last / kRing) & 1), p.err.limit_ns);
     }
   }
   __syncthreads();
@@ -940,7 +935,6 @@ bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int nu
   if (H % 512 || I % 256 || I / 64 > 8 || H / 8 > 2 * dec::kThreads || H / dec::kDn > num_sms)
     return false;
   if (E % dec::kRBoxE || E / dec::kRBoxE > num_sms) return false;
-  if ((H / 64) % (4 * dec::kWarps)) return false;   // K groups per warp a multiple of 4
   const dec::Smem L = dec::smem_layout(H, I);
   if ((uint32_t)H * dec::kRBoxE * 2 > L.slab) return false;   // router slice in one ring buffer
   if ((uint32_t)dec::kMaxT * H * 2 > L.slab) return false;     // bf16 token rows in another

@@ -168,7 +168,8 @@ struct DecodeLayerArgs {
   const uint16_t* router_w;
   const float* router_bias;
   W4Dev gate, up, down, sgate, sup, sdown;
-  CUtensorMap maps[6];           // gate, up, down, shared gate, up, down (encode_slab_3d)
+  CUtensorMap maps[6];           // gate, up, down, shared gate, up, down (encode_slab_3d:
+                                 // 8-row boxes for gate/up, 16 for down)
   CUtensorMap router_map;        // router weight, encode_router_slices
   float* logits;                 // [T][E] scratch
   uint16_t* act;                 // [T*k + T][I] fp16 scratch

@@ -364,11 +364,12 @@ moe_status decode_layer_impl(moe_plan* p, uint16_t* x, int T, const moe_layer& L
   a.sup = dev(sh.up);
   a.sdown = dev(sh.down);
   const uint64_t er = d.has_shared ? 1 : (uint64_t)E;
-  bool ok = p->qmap3(&a.maps[0], Ly.routed.gate.qweight, (uint64_t)E * I, H, 16) &&
-            p->qmap3(&a.maps[1], Ly.routed.up.qweight, (uint64_t)E * I, H, 16) &&
+  // 3D slabs, all K: 8 rows for a gate/up warp's unit, 16 down rows per CTA
+  bool ok = p->qmap3(&a.maps[0], Ly.routed.gate.qweight, (uint64_t)E * I, H, 8) &&
+            p->qmap3(&a.maps[1], Ly.routed.up.qweight, (uint64_t)E * I, H, 8) &&
             p->qmap3(&a.maps[2], Ly.routed.down.qweight, (uint64_t)E * H, I, 16) &&
-            p->qmap3(&a.maps[3], sh.gate.qweight, er * I, H, 16) &&
-            p->qmap3(&a.maps[4], sh.up.qweight, er * I, H, 16) &&
+            p->qmap3(&a.maps[3], sh.gate.qweight, er * I, H, 8) &&
+            p->qmap3(&a.maps[4], sh.up.qweight, er * I, H, 8) &&
             p->qmap3(&a.maps[5], sh.down.qweight, er * H, I, 16) &&
             p->rmap(&a.router_map, Ly.router_w, H, E);
   if (!ok) return MOE_ERR_CUDA;
