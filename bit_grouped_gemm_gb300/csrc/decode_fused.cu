@@ -51,8 +51,12 @@ constexpr int kWarps = 8;
 constexpr int kMaxT = 8;            // tokens
 constexpr int kMaxSlots = 80;       // shared + distinct routed experts
 constexpr int kGU = 8;              // gate rows (and the matching up rows) per unit: one m16 tile
-// a gate/up warp's buffer: its unit's 8 gate and 8 up rows, all K (H / 2 bytes a row)
-__host__ __device__ constexpr uint32_t unit_bytes(int H) { return 2u * kGU * (uint32_t)H / 2; }
+// a gate/up warp's buffer: its unit's 8 gate and 8 up rows, all K (H / 2 bytes
+// a row), then their scales and biases (gate s, gate b, up s, up b: 8 rows x
+// H / 64 bf16 each)
+__host__ __device__ constexpr uint32_t unit_words_bytes(int H) { return 2u * kGU * (uint32_t)H / 2; }
+__host__ __device__ constexpr uint32_t unit_sb_bytes(int H) { return (uint32_t)kGU * (H / 64) * 2; }
+__host__ __device__ constexpr uint32_t unit_bytes(int H) { return unit_words_bytes(H) + 4 * unit_sb_bytes(H); }
 constexpr int kDn = 16;             // down rows (output columns) per CTA
 constexpr int kSlotsPerChunk = 8;   // down slabs per ring buffer (one per warp)
 constexpr int kRing = 4;            // shared-memory slab buffers
@@ -588,7 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   // are dealt over the CTAs first (unit u: CTA u % ncta, warp u / ncta), so
   // every SM takes a share; a warp's unit arrives by TMA in two 3D boxes
   // (8 rows x all K, 128-byte swizzle) into its own buffer, and the scales
-  // and biases are read from global memory a 256-K stage ahead.
+  // and biases by bulk copies behind them.
   {
     const int nw = ncta * kWarps, wrank = warp * ncta + cta;   // this warp's place in the deal
     const int nst = H / 256;                                   // 256-K stages per unit
@@ -597,13 +601,20 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     uint8_t* wb = smem + (size_t)warp * ub;                    // in the ring's buffers
     const uint32_t wbase = smem_u32(wb);
     uint64_t* wf = &wfull[warp];
+    const uint32_t uwb = unit_words_bytes(H), usb = unit_sb_bytes(H);
     auto wissue = [&](int ui) {   // lane 0: unit ui of this warp's deal
       const int uu = wrank + ui * nw, s = uu / upe, r = uu - s * upe;
       const bool sh = p.has_shared && s == 0;
       const int row0 = (sh ? 0 : slot_e[s] * I) + kGU * r;
+      const W4Dev& wg = sh ? p.sgate : p.gate;
+      const W4Dev& wu = sh ? p.sup : p.up;
       mbar_arrive_expect_tx(wf, ub);
       tma_load_3d(wb, sh ? &p.msg : &p.mg, 0, row0, 0, wf);
-      tma_load_3d(wb + ub / 2, sh ? &p.msu : &p.mu, 0, row0, 0, wf);
+      tma_load_3d(wb + uwb / 2, sh ? &p.msu : &p.mu, 0, row0, 0, wf);
+      bulk_load(wb + uwb, wg.s + (size_t)row0 * G, usb, wf);
+      bulk_load(wb + uwb + usb, wg.b + (size_t)row0 * G, usb, wf);
+      bulk_load(wb + uwb + 2 * usb, wu.s + (size_t)row0 * G, usb, wf);
+      bulk_load(wb + uwb + 3 * usb, wu.b + (size_t)row0 * G, usb, wf);
     };
     if (lane == 0 && my_units > 0) {
       wissue(0);
@@ -611,39 +622,34 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
         const int uu = wrank + nw, s = uu / upe, r = uu - s * upe;
         const bool sh = p.has_shared && s == 0;
         const size_t row0 = (size_t)(sh ? 0 : slot_e[s] * I) + kGU * r;
-        bulk_prefetch_l2((sh ? p.sgate : p.gate).q + row0 * (H / 8), ub / 2);
-        bulk_prefetch_l2((sh ? p.sup : p.up).q + row0 * (H / 8), ub / 2);
+        bulk_prefetch_l2((sh ? p.sgate : p.gate).q + row0 * (H / 8), uwb / 2);
+        bulk_prefetch_l2((sh ? p.sup : p.up).q + row0 * (H / 8), uwb / 2);
       }
     }
     bool wok = true;
     int ui = 0;
     for (; ui < my_units && wok; ++ui) {
       const int uu = wrank + ui * nw, s = uu / upe, r = uu - s * upe;
-      const bool sh = p.has_shared && s == 0;
-      const int row0 = (sh ? 0 : slot_e[s] * I) + kGU * r;
-      const W4Dev& wg = sh ? p.sgate : p.gate;
-      const W4Dev& wu = sh ? p.sup : p.up;
       const int cnt = cnt_s[s];
       // the token of this lane's B column (g), and of its two D columns
       const int trow = g < cnt ? tok_s[s][g] : kMaxT;
       const int t0 = 2 * c < cnt ? tok_s[s][2 * c] : kMaxT;
       const int t1 = 2 * c + 1 < cnt ? tok_s[s][2 * c + 1] : kMaxT;
       const uint32_t* xr = xw + trow * L.xstride;
-      // this lane's rows: gate and up row row0 + g; their 4 groups of a stage
-      const size_t srow = (size_t)(row0 + g) * G;
+      // this lane's rows (gate and up row row0 + g): scales and biases of the
+      // 4 groups of a stage, from the buffer
+      const uint32_t sbrow = wbase + uwb + (uint32_t)(g * G * 2);
       auto ld_sb = [&](int q, uint2 (&v)[4]) {
-        v[0] = __ldg(reinterpret_cast<const uint2*>(wg.s + srow) + q);
-        v[1] = __ldg(reinterpret_cast<const uint2*>(wg.b + srow) + q);
-        v[2] = __ldg(reinterpret_cast<const uint2*>(wu.s + srow) + q);
-        v[3] = __ldg(reinterpret_cast<const uint2*>(wu.b + srow) + q);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) v[a] = lds_v2(sbrow + a * usb + 8 * q);
       };
       uint2 sbv[4], sbn[4];
-      ld_sb(0, sbv);
       const bool got = mbar_wait_drain(wf, (uint32_t)(ui & 1), p.err.limit_ns);
       if (!(wok = __all_sync(0xffffffffu, got))) {   // (warp-uniform: the MMAs below are warp-wide)
         if (lane == 0) report_timeout(p.err, 41);
         break;
       }
+      ld_sb(0, sbv);
       float tg0 = 0.f, tg1 = 0.f, tu0 = 0.f, tu1 = 0.f;   // gate and up sums, columns 2c and 2c + 1
       for (int q = 0; q < nst; ++q) {
         if (q + 1 < nst) ld_sb(q + 1, sbn);
@@ -656,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
           const int grp = 4 * q + gi;
           const uint32_t col = (uint32_t)(((2 * gi + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
           qw[gi][0] = lds_v2(zb + (uint32_t)(g * 128) + col);            // gate row g
-          qw[gi][1] = lds_v2(zb + ub / 2 + (uint32_t)(g * 128) + col);   // up row g
+          qw[gi][1] = lds_v2(zb + uwb / 2 + (uint32_t)(g * 128) + col);   // up row g
 #pragma unroll
           for (int st = 0; st < 4; ++st) {
             const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
