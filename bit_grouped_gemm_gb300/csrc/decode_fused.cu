@@ -16,8 +16,9 @@
 // bounded waits):
 //   1. every CTA reads the residual rows x, computes their RMS norm and the
 //      normalised rows xn = bf16(x / rms(x)) (kept in shared memory as the
-//      fp16 MMA operand), and router CTA c computes the logits of its
-//      experts (router weight slice copied before the previous launch ends);
+//      fp16 MMA operand, in 16-byte pieces ordered for 128-bit fragment
+//      loads), and router CTA c computes the logits of its experts (router
+//      weight slice copied before the previous launch ends);
 //   -- barrier 1 (all logits written) --
 //   2. every CTA selects each token's top-k (the same warp top-k as the
 //      routing kernels, so every CTA holds the same routing) and numbers the
@@ -26,10 +27,10 @@
 //   3. gate/up units (8 gate + the matching 8 up rows of one slot's expert,
 //      one m16 tile) are dealt to warps over the whole grid; each warp takes
 //      its unit's packed rows by TMA (3D boxes of 8 rows x all K, 128-byte
-//      swizzle) into its own shared-memory buffer and runs
-//      mma.sync with the exact affine split
-//          sum_k w_k x_k = s sum_k (1024+q_k) x_k + (b - 1024 s) sum_k x_k
-//      per group of 64, SwiGLU in FP32 registers, activations stored as fp16
+//      swizzle) into its own shared-memory buffer, rebuilds each group's
+//      fp16 weights fp16(q s + b) in registers (one rounding, the same
+//      weights the tensor-core GEMM rebuilds) and runs mma.sync with FP32
+//      accumulation, SwiGLU in FP32 registers, activations stored as fp16
 //      rows per (slot, token); no block barrier per unit;
 //   -- barrier 2 (all activations written) --
 //   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
@@ -88,7 +89,7 @@ struct Params {
 
 // Byte offsets of the dynamic shared memory (from a 1024-aligned base).
 struct Smem {
-  uint32_t slab, xw, xstride, xg, wr, total, dsum_cap;
+  uint32_t slab, xw, xstride, wr, total, dsum_cap;
 };
 
 __host__ __device__ inline uint32_t align_u(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
@@ -104,12 +105,12 @@ __host__ __device__ inline Smem smem_layout(int H, int I) {
   L.slab = align_u(dn > gu ? dn : gu, 1024);
   uint32_t o = kRing * L.slab;
   L.xw = o;
-  L.xstride = H / 2 + 1;                       // words per token row (padded)
+  // words per token row: 16-byte pieces, rows 4 pieces (mod 8) apart, so that
+  // the two tokens of a 128-bit load phase hit disjoint banks when their row
+  // numbers differ in parity
+  L.xstride = H / 2 + 16;
   o += (kMaxT + 1) * L.xstride * 4;            // + one zero row
   L.dsum_cap = (kMaxT + 1) * L.xstride * 4;    // the down pass reuses the token rows
-  o = align_u(o, 16);
-  L.xg = o;
-  o += (kMaxT + 1) * (H / 64) * 4;
   o = align_u(o, 16);
   L.wr = (kRing - 1) * L.slab;
   L.total = o;
@@ -161,6 +162,13 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, 
 __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
+  return v;
+}
+// 128-bit load of shared memory that no copy rewrites while it is in use (the
+// token rows): not volatile, so the compiler may schedule it freely.
+__device__ __forceinline__ uint4 lds_v4(uint32_t a) {
+  uint4 v;
+  asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
   return v;
 }
 
@@ -271,7 +279,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   const int cta = blockIdx.x, ncta = gridDim.x;
   const uint32_t sbase = smem_u32(smem);
   uint32_t* xw = reinterpret_cast<uint32_t*>(smem + L.xw);
-  float* xg = reinterpret_cast<float*>(smem + L.xg);
   const uint16_t* wrs = reinterpret_cast<const uint16_t*>(smem + L.wr);
   uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.slab);   // xn bf16 [T][H] (ring buffer 1)
   const int upe = I / kGU;                     // gate/up units per slot
@@ -386,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
 #pragma unroll
   for (int t = 0; t < kMaxT; ++t) rinv[t] = t < T ? rinv_s[t] : 0.f;
   DEC_TRACE2(2);
-  // xn = bf16(x * rinv): fp16 operand rows (perm8 K order) and their group
-  // sums; router partial sums over this thread's hidden indices
+  // xn = bf16(x * rinv): fp16 operand rows (perm8 K order); router partial
+  // sums over this thread's hidden indices
   float pr[kMaxT * EPC];
 #pragma unroll
   for (int q = 0; q < kMaxT * EPC; ++q) pr[q] = 0.f;
@@ -409,18 +416,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
         *reinterpret_cast<uint4*>(xb + (size_t)t * H + 8 * pc) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
       const uint4 o = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(nb[0]), bf16x2_to_f16x2_sat(nb[1]),
                                                 bf16x2_to_f16x2_sat(nb[2]), bf16x2_to_f16x2_sat(nb[3])));
-      uint32_t* dst = xw + t * L.xstride + 4 * pc;
-      dst[0] = o.x;
-      dst[1] = o.y;
-      dst[2] = o.z;
-      dst[3] = o.w;
-      float gs = f16_lo(o.x) + f16_hi(o.x) + f16_lo(o.y) + f16_hi(o.y) + f16_lo(o.z) + f16_hi(o.z) +
-                 f16_lo(o.w) + f16_hi(o.w);
-      // group of 64 = 8 pieces = 8 adjacent lanes
-      gs += __shfl_xor_sync(0xffffffffu, gs, 1);
-      gs += __shfl_xor_sync(0xffffffffu, gs, 2);
-      gs += __shfl_xor_sync(0xffffffffu, gs, 4);
-      if ((lane & 7) == 0) xg[t * G + pc / 8] = gs;
+      // piece u = pc % 8 of its group of 64 goes to position 4 (u % 2) + u / 2,
+      // so that lane c of a B fragment finds its pieces 2c and 2c + 1 at
+      // positions c and 4 + c (two 128-bit loads, adjacent lanes adjacent)
+      const int u = pc & 7;
+      *reinterpret_cast<uint4*>(xw + t * L.xstride + 32 * (pc >> 3) + 4 * (4 * (u & 1) + (u >> 1))) = o;
     }
   }
   report_range_warp(p.err, over != 0u);
@@ -459,7 +459,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   DEC_TRACE2(4);
   // the zero token row (columns of a tile past its tokens)
   for (int i = tid; i < (int)L.xstride; i += kThreads) xw[kMaxT * L.xstride + i] = 0u;
-  for (int i = tid; i < G; i += kThreads) xg[kMaxT * G + i] = 0.f;
   if (router_cta) {
     // the warp's sums of the kMaxT * EPC partials, scattered over its lanes
     warp_reduce_scatter<kMaxT * EPC>(pr, lane);
@@ -587,8 +586,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   // ----------------------------------------------- 3. gate/up + SwiGLU units
   // One warp per unit: 8 gate rows and the matching 8 up rows of one slot's
   // expert (an m16 tile: row g is gate feature g, row g + 8 its up feature),
-  // all K, with the exact affine split per group of 64 and SwiGLU in
-  // registers -- no reduction across warps, no block barrier per unit. Units
+  // all K, its fp16 weights rebuilt in registers and SwiGLU in registers --
+  // no reduction across warps, no block barrier per unit. Units
   // are dealt over the CTAs first (unit u: CTA u % ncta, warp u / ncta), so
   // every SM takes a share; a warp's unit arrives by TMA in two 3D boxes
   // (8 rows x all K, 128-byte swizzle) into its own buffer, and the scales
@@ -631,84 +630,60 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     for (; ui < my_units && wok; ++ui) {
       const int uu = wrank + ui * nw, s = uu / upe, r = uu - s * upe;
       const int cnt = cnt_s[s];
-      // the token of this lane's B column (g), and of its two D columns
+      // the token of this lane's B column (g)
       const int trow = g < cnt ? tok_s[s][g] : kMaxT;
-      const int t0 = 2 * c < cnt ? tok_s[s][2 * c] : kMaxT;
-      const int t1 = 2 * c + 1 < cnt ? tok_s[s][2 * c + 1] : kMaxT;
-      const uint32_t* xr = xw + trow * L.xstride;
+      const uint32_t xrow = smem_u32(xw + trow * L.xstride);   // this lane's B column's token row
       // this lane's rows (gate and up row row0 + g): scales and biases of the
       // 4 groups of a stage, from the buffer
       const uint32_t sbrow = wbase + uwb + (uint32_t)(g * G * 2);
-      auto ld_sb = [&](int q, uint2 (&v)[4]) {
-#pragma unroll
-        for (int a = 0; a < 4; ++a) v[a] = lds_v2(sbrow + a * usb + 8 * q);
-      };
-      uint2 sbv[4], sbn[4];
       const bool got = mbar_wait_drain(wf, (uint32_t)(ui & 1), p.err.limit_ns);
       if (!(wok = __all_sync(0xffffffffu, got))) {   // (warp-uniform: the MMAs below are warp-wide)
         if (lane == 0) report_timeout(p.err, 41);
         break;
       }
-      ld_sb(0, sbv);
-      float tg0 = 0.f, tg1 = 0.f, tu0 = 0.f, tu1 = 0.f;   // gate and up sums, columns 2c and 2c + 1
+      // rows g (gate) and g + 8 (up) of the m16 tile, fp16 weights fp16(q s + b)
+      // rebuilt group by group (one rounding, as the tensor-core GEMM does);
+      // one accumulator chain per group of a stage, summed at the end
+      float acc[4][4];
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+        for (int v = 0; v < 4; ++v) acc[gi][v] = 0.f;
       for (int q = 0; q < nst; ++q) {
-        if (q + 1 < nst) ld_sb(q + 1, sbn);
+        uint2 sbq[4];   // gate s, gate b, up s, up b: groups 4q .. 4q + 3 of row g
+#pragma unroll
+        for (int a = 0; a < 4; ++a) sbq[a] = lds_v2(sbrow + a * usb + 8 * q);
         const uint32_t zb = wbase + (uint32_t)q * (kGU * 128);   // 256-K chunk q of the gate rows
-        uint2 qw[4][2];
-        uint32_t bf[4][4][2];
-        float xs0[4], xs1[4];
 #pragma unroll
         for (int gi = 0; gi < 4; ++gi) {
           const int grp = 4 * q + gi;
           const uint32_t col = (uint32_t)(((2 * gi + (c >> 1)) ^ g) << 4) + ((c & 1) << 3);
-          qw[gi][0] = lds_v2(zb + (uint32_t)(g * 128) + col);            // gate row g
-          qw[gi][1] = lds_v2(zb + uwb / 2 + (uint32_t)(g * 128) + col);   // up row g
-#pragma unroll
-          for (int st = 0; st < 4; ++st) {
-            const int wabs = grp * 8 + 2 * c + (st >> 1), psel = 2 * (st & 1);
-            bf[gi][st][0] = xr[4 * wabs + psel];
-            bf[gi][st][1] = xr[4 * wabs + psel + 1];
-          }
-          xs0[gi] = xg[t0 * G + grp];
-          xs1[gi] = xg[t1 * G + grp];
-        }
-        float acc[4][4];
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) acc[gi][v] = 0.f;
-        // 4 independent chains (the groups), k-step outermost
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          const int psel = 2 * (st & 1);
-#pragma unroll
-          for (int gi = 0; gi < 4; ++gi) {
-            const uint32_t w0 = (st >> 1) ? qw[gi][0].y : qw[gi][0].x;
-            const uint32_t w1 = (st >> 1) ? qw[gi][1].y : qw[gi][1].x;
-            mma_m16n8k16_f16(acc[gi], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
-                             nibble_pair_1024(w0, psel + 1), nibble_pair_1024(w1, psel + 1),
-                             bf[gi][st][0], bf[gi][st][1]);
-          }
-        }
-        // D rows g (gate) and g + 8 (up) at columns 2c and 2c + 1; a group's
-        // share is s * sum (1024 + q) x + (b - 1024 s) * sum x
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi) {
-          auto pick = [&](const uint2& v) {
+          const uint2 wg = lds_v2(zb + (uint32_t)(g * 128) + col);            // gate row g
+          const uint2 wu = lds_v2(zb + uwb / 2 + (uint32_t)(g * 128) + col);   // up row g
+          // the token row's pieces 2c (K steps 0, 1) and 2c + 1 (steps 2, 3)
+          const uint4 xa = lds_v4(xrow + (uint32_t)(grp * 32 + 4 * c) * 4);
+          const uint4 xb4 = lds_v4(xrow + (uint32_t)(grp * 32 + 16 + 4 * c) * 4);
+          auto h2 = [&](const uint2& v) {   // this group's bf16 of a table as fp16 (x, x)
             const uint32_t wd = (gi >> 1) ? v.y : v.x;
-            return bf16_to_f32((uint16_t)((gi & 1) ? wd >> 16 : wd & 0xFFFFu));
+            return __half2half2(__float2half_rn(bf16_to_f32((uint16_t)((gi & 1) ? wd >> 16 : wd & 0xFFFFu))));
           };
-          const float sg = pick(sbv[0]), su = pick(sbv[2]);
-          const float cg = fmaf(-1024.0f, sg, pick(sbv[1])), cu = fmaf(-1024.0f, su, pick(sbv[3]));
-          tg0 += fmaf(sg, acc[gi][0], cg * xs0[gi]);
-          tg1 += fmaf(sg, acc[gi][1], cg * xs1[gi]);
-          tu0 += fmaf(su, acc[gi][2], cu * xs0[gi]);
-          tu1 += fmaf(su, acc[gi][3], cu * xs1[gi]);
+          const __half2 sg2 = h2(sbq[0]), bg2 = h2(sbq[1]), su2 = h2(sbq[2]), bu2 = h2(sbq[3]);
+          uint32_t dg[2][4], du[2][4];
+          dequant_word_f16_perm8(wg.x, sg2, bg2, dg[0]);
+          dequant_word_f16_perm8(wg.y, sg2, bg2, dg[1]);
+          dequant_word_f16_perm8(wu.x, su2, bu2, du[0]);
+          dequant_word_f16_perm8(wu.y, su2, bu2, du[1]);
+          mma_m16n8k16_f16(acc[gi], dg[0][0], du[0][0], dg[0][1], du[0][1], xa.x, xa.y);
+          mma_m16n8k16_f16(acc[gi], dg[0][2], du[0][2], dg[0][3], du[0][3], xa.z, xa.w);
+          mma_m16n8k16_f16(acc[gi], dg[1][0], du[1][0], dg[1][1], du[1][1], xb4.x, xb4.y);
+          mma_m16n8k16_f16(acc[gi], dg[1][2], du[1][2], dg[1][3], du[1][3], xb4.z, xb4.w);
         }
-        if (q + 1 < nst)
-#pragma unroll
-          for (int v = 0; v < 4; ++v) sbv[v] = sbn[v];
       }
+      // D rows g (gate) and g + 8 (up) at columns 2c and 2c + 1
+      const float tg0 = (acc[0][0] + acc[1][0]) + (acc[2][0] + acc[3][0]);
+      const float tg1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
+      const float tu0 = (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]);
+      const float tu1 = (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]);
       // every word of the unit has been read: the buffer takes the next unit
       __syncwarp();
       if (lane == 0 && ui + 1 < my_units) {
@@ -792,56 +767,52 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       }
     };
     // One slot: its 16 down rows (ring buffer b, position q) times its
-    // activation rows; the FP32 result goes to dsum.
+    // activation rows; the FP32 result goes to dsum. The rows' fp16 weights
+    // fp16(q s + b) are rebuilt group by group, as in step 3.
     auto down_slot = [&](int s, int b, int q, const uint4 (&v)[16]) {
       const uint32_t bq = sbase + (uint32_t)b * L.slab + (uint32_t)q * dn_q;
       const uint16_t* ssc = reinterpret_cast<const uint16_t*>(
           smem + (size_t)b * L.slab + kSlotsPerChunk * dn_q + q * dn_s);
       const uint16_t* sbi = reinterpret_cast<const uint16_t*>(
           smem + (size_t)b * L.slab + kSlotsPerChunk * (dn_q + dn_s) + q * dn_s);
-      float tot[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t one2 = 0x3C003C00u;   // fp16 (1, 1)
+      float acc[4][4];
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi)
+#pragma unroll
+        for (int v4 = 0; v4 < 4; ++v4) acc[gi][v4] = 0.f;
 #pragma unroll
       for (int g0 = 0; g0 < 8; g0 += 4) {
         if (g0 >= GI) break;
-        // four groups at a time: their A words, then 8 independent MMA chains
-        // (the groups' products, and their activation column sums by an
-        // all-ones A: every D row is then the column sum, exact products)
-        uint2 qw[4][2];
+        // four groups at a time, one accumulator chain each
 #pragma unroll
-        for (int gi = 0; gi < 4; ++gi)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) qw[gi][h] = lds_v2(bq + qoff(g + 8 * h, g0 + gi, c, kDn));
-        float acc[4][4], gsum[4][4];
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[gi][q] = gsum[gi][q] = 0.f;
-#pragma unroll
-        for (int st = 0; st < 4; ++st) {
-          const int psel = 2 * (st & 1);
-#pragma unroll
-          for (int gi = 0; gi < 4; ++gi) {
-            const uint4 vv = v[2 * (g0 + gi) + (st >> 1)];
-            const uint32_t b0 = psel ? vv.z : vv.x, b1 = psel ? vv.w : vv.y;
-            const uint32_t w0 = (st >> 1) ? qw[gi][0].y : qw[gi][0].x;
-            const uint32_t w1 = (st >> 1) ? qw[gi][1].y : qw[gi][1].x;
-            mma_m16n8k16_f16(acc[gi], nibble_pair_1024(w0, psel), nibble_pair_1024(w1, psel),
-                             nibble_pair_1024(w0, psel + 1), nibble_pair_1024(w1, psel + 1), b0, b1);
-            mma_m16n8k16_f16(gsum[gi], one2, one2, one2, one2, b0, b1);
+        for (int gi = 0; gi < 4; ++gi) {
+          const int grp = g0 + gi;
+          // packed words of rows g (h = 0) and g + 8 (h = 1) of the tile
+          const uint2 w0 = lds_v2(bq + qoff(g, grp, c, kDn));
+          const uint2 w1 = lds_v2(bq + qoff(g + 8, grp, c, kDn));
+          auto h2 = [](uint16_t v) { return __half2half2(__float2half_rn(bf16_to_f32(v))); };
+          uint32_t d0[2][4], d1[2][4];
+          {
+            const __half2 s2 = h2(ssc[g * GI + grp]), b2 = h2(sbi[g * GI + grp]);
+            dequant_word_f16_perm8(w0.x, s2, b2, d0[0]);
+            dequant_word_f16_perm8(w0.y, s2, b2, d0[1]);
           }
+          {
+            const __half2 s2 = h2(ssc[(g + 8) * GI + grp]), b2 = h2(sbi[(g + 8) * GI + grp]);
+            dequant_word_f16_perm8(w1.x, s2, b2, d1[0]);
+            dequant_word_f16_perm8(w1.y, s2, b2, d1[1]);
+          }
+          const uint4 va = v[2 * grp], vb = v[2 * grp + 1];   // K steps 0, 1 and 2, 3
+          mma_m16n8k16_f16(acc[gi], d0[0][0], d1[0][0], d0[0][1], d1[0][1], va.x, va.y);
+          mma_m16n8k16_f16(acc[gi], d0[0][2], d1[0][2], d0[0][3], d1[0][3], va.z, va.w);
+          mma_m16n8k16_f16(acc[gi], d0[1][0], d1[1][0], d0[1][1], d1[1][1], vb.x, vb.y);
+          mma_m16n8k16_f16(acc[gi], d0[1][2], d1[1][2], d0[1][3], d1[1][3], vb.z, vb.w);
         }
-#pragma unroll
-        for (int gi = 0; gi < 4; ++gi)
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const int row = g + 8 * h, grp = g0 + gi;
-            const float sc = bf16_to_f32(ssc[row * GI + grp]);
-            const float cb = fmaf(-1024.0f, sc, bf16_to_f32(sbi[row * GI + grp]));
-            tot[2 * h] += fmaf(sc, acc[gi][2 * h], cb * gsum[gi][0]);       // column 2c
-            tot[2 * h + 1] += fmaf(sc, acc[gi][2 * h + 1], cb * gsum[gi][1]);   // column 2c + 1
-          }
       }
+      // D rows g and g + 8 at columns 2c and 2c + 1
+      float tot[4];
+#pragma unroll
+      for (int v4 = 0; v4 < 4; ++v4) tot[v4] = (acc[0][v4] + acc[1][v4]) + (acc[2][v4] + acc[3][v4]);
 #pragma unroll
       for (int qq = 0; qq < 4; ++qq) {
         const int col = 2 * c + (qq & 1), row = g + 8 * (qq >> 1);
