@@ -34,8 +34,8 @@
 //      rows per (slot, token); no block barrier per unit;
 //   -- barrier 2 (all activations written) --
 //   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
-//      those 16 down rows (prefetched into L2 during step 3) by the
-//      slot's activation rows, then forms
+//      those 16 down rows (copied while it waits at barrier 2) by the slot's
+//      activation rows, then forms
 //          y[t] = shared[t] + sum_j w[t][j] * expert_j[t]   (FP32, j in rank order)
 //      and updates x[t] = bf16(x[t] + alpha * y[t]) in place.
 // The next layer's launch (programmatic dependent launch) is the barrier
@@ -81,8 +81,6 @@ struct Params {
   int32_t* topk_idx;         // [T][k] (written by CTA 0)
   float* topk_w;             // [T][k]
   float* y_out;              // [T][H] FP32 block output, or null
-  const uint16_t* next_wr;   // the next layer's router weight and shared expert (L2
-  W4Dev next_sgate, next_sup, next_sdown;   // prefetch during step 4), or null
   unsigned* bar;             // grid-barrier arrival counter, 0 at launch
   DevErr err;
 };
@@ -269,6 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   __shared__ float x_s[kMaxT][kDn];
   __shared__ int nslots_s, flag_s, abort_s;
   __shared__ int scan_a[kWarps], scan_c[kWarps];
+  __shared__ unsigned ring_issued_s;           // first-round down chunks issued (bit per buffer)
   __shared__ float rinv_s[kMaxT];
 
   const int H = p.H, I = p.I, E = p.E, T = p.T, k = p.k;
@@ -303,6 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       tma_prefetch_desc(&p.msd);
     }
     abort_s = 0;
+    ring_issued_s = 0u;
     if (router_cta) {   // the router slice [H][8] by TMA, H / 256 boxes
       mbar_arrive_expect_tx(&wbar, (uint32_t)H * kRBoxE * 2);
       for (int y = 0; y < H; y += kRBox)
@@ -568,15 +568,6 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   DEC_TRACE2(7);
   n_units = nslots_s * upe;
   n_dc = cta < p.n_dn ? (nslots_s + kSlotsPerChunk - 1) / kSlotsPerChunk : 0;
-  if (tid == kIssuer && n_dc > 0)   // the down slabs into L2 while the gate/up units run
-    for (int s = 0; s < nslots_s; ++s) {
-      const bool sh = p.has_shared && s == 0;
-      const size_t row0 = (size_t)(sh ? 0 : slot_e[s] * H) + kDn * cta;
-      const W4Dev& wd = sh ? p.sdown : p.down;
-      bulk_prefetch_l2(wd.q + row0 * (I / 8), dn_q);
-      bulk_prefetch_l2(wd.s + row0 * GI, dn_s);
-      bulk_prefetch_l2(wd.b + row0 * GI, dn_s);
-    }
   DEC_TRACE(5);
   for (int i = tid; i < T * k; i += kThreads) {   // used by the combine, after later barriers
     const int t = i / k, j = i - t * k, e = idx_s[t][j];
@@ -615,16 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       bulk_load(wb + uwb + 2 * usb, wu.s + (size_t)row0 * G, usb, wf);
       bulk_load(wb + uwb + 3 * usb, wu.b + (size_t)row0 * G, usb, wf);
     };
-    if (lane == 0 && my_units > 0) {
-      wissue(0);
-      if (my_units > 1) {   // the second unit's rows into L2 while the first computes
-        const int uu = wrank + nw, s = uu / upe, r = uu - s * upe;
-        const bool sh = p.has_shared && s == 0;
-        const size_t row0 = (size_t)(sh ? 0 : slot_e[s] * I) + kGU * r;
-        bulk_prefetch_l2((sh ? p.sgate : p.gate).q + row0 * (H / 8), uwb / 2);
-        bulk_prefetch_l2((sh ? p.sup : p.up).q + row0 * (H / 8), uwb / 2);
-      }
-    }
+    // (no L2 prefetches anywhere in this kernel: bulk prefetches of the second
+    // unit's rows, of the down slabs or of the next layer's router and shared
+    // expert each measured slower, as they hold up the issuing SM's copies)
+    if (lane == 0 && my_units > 0) wissue(0);
     bool wok = true;
     int ui = 0;
     for (; ui < my_units && wok; ++ui) {
@@ -713,45 +698,21 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   }
 
   DEC_TRACE(6);
-  // the down slabs (in L2 by now) are issued while thread 0 takes barrier 2:
-  // every warp's unit buffer (the whole ring) has been read at its first sync
+  // the first down chunks are issued while thread 0 takes barrier 2 (every
+  // warp's unit buffer, the whole ring, has been read at its first sync),
+  // one chunk per issuing thread: lane 0 of warps 4 .. 7 takes chunk warp - 4
   ok = grid_barrier(p.bar, 2u * ncta, p.err, 42, &flag_s, [&] {
-    if (tid == kIssuer && !abort_s) {
+    const int b = warp - (kWarps - kRing);
+    if (lane == 0 && b >= 0 && b < n_dc && !abort_s) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      for (int i = 0; i < kRing && i < n_dc; ++i) issue(i);
+      issue(b);
+      atomicOr(&ring_issued_s, 1u << b);
     }
   });
   DEC_TRACE(7);
   if (!ok || abort_s) goto drain;
 
   // ------------------------------------------ 4. down, combine, stack update
-  // HBM is idle from here on: pull the next layer's routing-independent
-  // weights (router weight, shared expert) into L2, a slice per CTA
-  if (tid == 0 && p.next_wr) {
-    const size_t rbytes = (size_t)H * E * 2;
-    const size_t per = ((rbytes + ncta - 1) / ncta + 255) / 256 * 256;
-    const size_t b0 = per * cta;
-    if (b0 < rbytes)
-      bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(p.next_wr) + b0,
-                       (uint32_t)(b0 + per <= rbytes ? per : rbytes - b0));
-    if (p.has_shared) {
-      // shared gate/up/down packed rows, then scales and biases: 9 arrays
-      const W4Dev* m3[3] = {&p.next_sgate, &p.next_sup, &p.next_sdown};
-      for (int m = 0; m < 3; ++m) {
-        const size_t qb = (size_t)H * I / 2, sbb = (size_t)H * I / 64 * 2;
-        const size_t pq = ((qb + ncta - 1) / ncta + 255) / 256 * 256;
-        const size_t ps = ((sbb + ncta - 1) / ncta + 255) / 256 * 256;
-        if (pq * cta < qb)
-          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->q) + pq * cta,
-                           (uint32_t)(pq * cta + pq <= qb ? pq : qb - pq * cta));
-        if (ps * cta < sbb) {
-          const uint32_t n = (uint32_t)(ps * cta + ps <= sbb ? ps : sbb - ps * cta);
-          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->s) + ps * cta, n);
-          bulk_prefetch_l2(reinterpret_cast<const uint8_t*>(m3[m]->b) + ps * cta, n);
-        }
-      }
-    }
-  }
   if (n_dc > 0) {
     float* dsum = reinterpret_cast<float*>(smem + L.xw);   // [slot][kDn][kMaxT]
     // The activation row of this lane's column for slot s, all of its groups:
@@ -888,8 +849,13 @@ drain:
   __syncthreads();
   if (tid == 0 && router_cta) mbar_wait_drain(&wbar, 0, p.err.limit_ns);
   if (tid == kIssuer) {
-    for (int b = 0; b < kRing && b < issued; ++b) {
-      const int last = b + ((issued - 1 - b) / kRing) * kRing;   // last chunk i = b (mod kRing)
+    // buffer b holds first-round chunk b if its bit is set, then (step 4 with
+    // more chunks than buffers, issued by kIssuer) chunks b + kRing, ... below
+    // `issued`
+    const int hi = issued > kRing ? issued : kRing;
+    for (int b = 0; b < kRing; ++b) {
+      if (!((ring_issued_s >> b) & 1u)) continue;
+      const int last = b + ((hi - 1 - b) / kRing) * kRing;   // last chunk i = b (mod kRing)
       mbar_wait_drain(&full[ring_buf(b)], (uint32_t)((last / kRing) & 1), p.err.limit_ns);
     }
   }
@@ -965,10 +931,6 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sm
   p.topk_idx = a.topk_idx;
   p.topk_w = a.topk_w;
   p.y_out = a.y_out;
-  p.next_wr = a.next_router_w;
-  p.next_sgate = a.next_sgate;
-  p.next_sup = a.next_sup;
-  p.next_sdown = a.next_sdown;
   p.bar = a.bar;
   p.err = err;
   const dec::Smem L = dec::smem_layout(a.H, a.I);

@@ -177,10 +177,6 @@ struct DecodeLayerArgs {
   float* topk_w;
   float* y_out;                  // [T][H] FP32 block output, or null
   unsigned* bar;                 // grid-barrier counter, 0 between launches
-  // the next layer's router weight and shared expert, pulled into L2 while
-  // this layer's down pass runs (next_router_w null: none)
-  const uint16_t* next_router_w;
-  W4Dev next_sgate, next_sup, next_sdown;
 };
 bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int num_sms);
 cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sms, cudaStream_t st);

@@ -339,7 +339,7 @@ bool use_decode_fused(const moe_plan* p, int T) {
 // moe(rmsnorm(x))); the routing lands in the plan's routing arrays and y (FP32)
 // in the shared-output buffer, for inspection.
 moe_status decode_layer_impl(moe_plan* p, uint16_t* x, int T, const moe_layer& Ly, float alpha,
-                             cudaStream_t st, const moe_layer* next) {
+                             cudaStream_t st) {
   const moe_plan_desc& d = p->d;
   const int H = d.hidden, I = d.inter, E = d.num_experts;
   const moe_experts* shared = d.has_shared ? &Ly.shared : nullptr;
@@ -379,13 +379,6 @@ moe_status decode_layer_impl(moe_plan* p, uint16_t* x, int T, const moe_layer& L
   a.topk_w = p->at<float>(p->L.topk_w);
   a.y_out = d.has_shared ? p->at<float>(p->L.dsh) : nullptr;
   a.bar = p->at<unsigned>(p->L.arrive) + 2;
-  a.next_router_w = next ? next->router_w : nullptr;
-  a.next_sgate = a.next_sup = a.next_sdown = W4Dev{nullptr, nullptr, nullptr};
-  if (next && d.has_shared) {
-    a.next_sgate = dev(next->shared.gate);
-    a.next_sup = dev(next->shared.up);
-    a.next_sdown = dev(next->shared.down);
-  }
   p->last_path = 3;
   return st_of(timed(p, 9, st, [&] { return launch_decode_layer(a, p->err(), p->num_sms, st); }));
 }
@@ -755,8 +748,7 @@ moe_status moe_forward_stack(moe_plan_t p, uint16_t* x, uint16_t* xn, int T,
       // then the chunk's normalised stream for the caller
       cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
       for (int l = 0; l < num_layers; ++l)
-        if ((s = decode_layer_impl(p, xc, Tc, layers[l], alpha, st,
-                                   l + 1 < num_layers ? &layers[l + 1] : nullptr)) != MOE_OK)
+        if ((s = decode_layer_impl(p, xc, Tc, layers[l], alpha, st)) != MOE_OK)
           return s;
       if ((s = moe_residual_add(p, xc, nullptr, Tc, 0.f, xc, xn, stream)) != MOE_OK) return s;
       continue;
