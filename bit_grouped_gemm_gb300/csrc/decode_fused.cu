@@ -121,18 +121,37 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   return v;
 }
 
-// Grid barrier: every CTA adds one arrival, then waits (bounded) until the
+#ifdef MOE_DEC_TRACE
+// Profiling build only: %globaltimer inside the two grid barriers of every CTA
+// (after the first sync, the fence, the arrival, the wait, the last sync).
+__device__ unsigned long long g_dec_btrace[256][2][5];
+#define DEC_BTRACE(i) \
+  if (blockIdx.x < 256) g_dec_btrace[blockIdx.x][site == 40 ? 0 : 1][(i)] = globaltimer_ns()
+#else
+#define DEC_BTRACE(i)
+#endif
+
+// Grid barrier: every CTA adds one arrival (after a fence that makes the
+// CTA's writes visible), then waits (bounded, acquire loads) until the
 // counter reaches `target`. Returns false on timeout (error latched).
-// `during` runs on the other threads while thread 0 arrives and waits.
+// `during` runs on the other threads while thread 0 waits.
 template <class F>
 __device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, int site,
                              int* flag_s, F&& during) {
   __syncthreads();
+  if (threadIdx.x == 0) {
+    DEC_BTRACE(0);
+    __threadfence();
+    DEC_BTRACE(1);
+    atomicAdd(bar, 1u);
+    DEC_BTRACE(2);
+  }
+  // `during` starts after the arrival: copies issued while the fence waits
+  // for the CTA's stores delayed it (measured: 1.9% of a T = 8 decode step)
+  __syncthreads();
   if (threadIdx.x != 0) {
     during();
   } else {
-    __threadfence();
-    atomicAdd(bar, 1u);
     int ok = 1;
     if (ld_acquire_u32(bar) < target) {
       const unsigned long long t0 = globaltimer_ns();
@@ -145,10 +164,14 @@ __device__ bool grid_barrier(unsigned* bar, unsigned target, const DevErr& err, 
         }
       }
     }
-    __threadfence();
+    DEC_BTRACE(3);
+    // (no fence here: the acquire load that saw the count, then the CTA
+    // barrier, order every thread's later reads after the other CTAs' writes;
+    // a trailing fence measured ~0.5 us per barrier)
     *flag_s = ok;
   }
   __syncthreads();
+  if (threadIdx.x == 0) { DEC_BTRACE(4); }
   return *flag_s != 0;
 }
 
@@ -189,9 +212,15 @@ __device__ unsigned long long g_dec_trace[256][16];
 __device__ unsigned long long g_dec_trace2[256][8];
 #define DEC_TRACE2(i) \
   if (threadIdx.x == 0 && blockIdx.x < 256) g_dec_trace2[blockIdx.x][(i)] = globaltimer_ns()
+// per warp in step 3: copy issued, landed, MMAs done, stored (first unit),
+// then landed and stored for a second unit
+__device__ unsigned long long g_dec_wtrace[256][8][6];
+#define DEC_WTRACE(i) \
+  if ((threadIdx.x & 31) == 0 && blockIdx.x < 256) g_dec_wtrace[blockIdx.x][threadIdx.x >> 5][(i)] = globaltimer_ns()
 #else
 #define DEC_TRACE(i)
 #define DEC_TRACE2(i)
+#define DEC_WTRACE(i)
 #endif
 
 // Reduce-scatter of N partial sums over the 32 lanes of a warp by halving
@@ -610,6 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     // unit's rows, of the down slabs or of the next layer's router and shared
     // expert each measured slower, as they hold up the issuing SM's copies)
     if (lane == 0 && my_units > 0) wissue(0);
+    DEC_WTRACE(0);
     bool wok = true;
     int ui = 0;
     for (; ui < my_units && wok; ++ui) {
@@ -626,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
         if (lane == 0) report_timeout(p.err, 41);
         break;
       }
+      if (ui == 0) { DEC_WTRACE(1); } else { DEC_WTRACE(4); }
       // rows g (gate) and g + 8 (up) of the m16 tile, fp16 weights fp16(q s + b)
       // rebuilt group by group (one rounding, as the tensor-core GEMM does);
       // one accumulator chain per group of a stage, summed at the end
@@ -669,6 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       const float tg1 = (acc[0][1] + acc[1][1]) + (acc[2][1] + acc[3][1]);
       const float tu0 = (acc[0][2] + acc[1][2]) + (acc[2][2] + acc[3][2]);
       const float tu1 = (acc[0][3] + acc[1][3]) + (acc[2][3] + acc[3][3]);
+      if (ui == 0) { DEC_WTRACE(2); }
       // every word of the unit has been read: the buffer takes the next unit
       __syncwarp();
       if (lane == 0 && ui + 1 < my_units) {
@@ -689,6 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
         p.act[(size_t)(soff_s[s] + 2 * c + 1) * I + fpos] = f32_to_f16_sat(a);
       }
       report_range_warp(p.err, big != 0u);
+      if (ui == 0) { DEC_WTRACE(3); } else { DEC_WTRACE(5); }
     }
     if (!wok) {
       // this warp's own copy (unit ui, issued) lands before the CTA gives up
@@ -870,6 +903,12 @@ extern "C" int moe_debug_dec_trace(unsigned long long* out) {
 }
 extern "C" int moe_debug_dec_trace2(unsigned long long* out) {
   return (int)cudaMemcpyFromSymbol(out, dec::g_dec_trace2, sizeof(dec::g_dec_trace2));
+}
+extern "C" int moe_debug_dec_btrace(unsigned long long* out) {
+  return (int)cudaMemcpyFromSymbol(out, dec::g_dec_btrace, sizeof(dec::g_dec_btrace));
+}
+extern "C" int moe_debug_dec_wtrace(unsigned long long* out) {
+  return (int)cudaMemcpyFromSymbol(out, dec::g_dec_wtrace, sizeof(dec::g_dec_wtrace));
 }
 #endif
 
