@@ -662,7 +662,8 @@ def run_decode(args, w, ws, rank, local, pg):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": None,
-                     "kernel": "whole 40-layer decode step (small-M grouped GEMMs + routing)",
+                     "kernel": "whole 40-layer decode step (one fused launch per layer for T <= 8, "
+                               "else routing and small-M grouped GEMMs)",
                      "peak_source": f"{peak_src} hbm_gbs (of {peak_src})",
                      "algorithmic_bytes_per_step": step_bytes,
                      "distinct_routed_experts_per_layer": experts_per_layer},
