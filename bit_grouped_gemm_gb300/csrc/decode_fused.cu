@@ -185,6 +185,25 @@ __device__ __forceinline__ uint2 lds_v2(uint32_t a) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a));
   return v;
 }
+// ldmatrix of four 8x8 b16 matrices (row addresses from lanes 8j .. 8j + 7 for
+// matrix j), plain and transposed, and the bf16 m16n8k16 MMA (FP32 accumulation).
+__device__ __forceinline__ void ldsm4(uint32_t a, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void ldsm4_t(uint32_t a, uint32_t (&r)[4]) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(a));
+}
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                               uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+      "{%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
 // 128-bit load of shared memory that no copy rewrites while it is in use (the
 // token rows): not volatile, so the compiler may schedule it freely.
 __device__ __forceinline__ uint4 lds_v4(uint32_t a) {
@@ -222,31 +241,6 @@ __device__ unsigned long long g_dec_wtrace[256][8][6];
 #define DEC_TRACE2(i)
 #define DEC_WTRACE(i)
 #endif
-
-// Reduce-scatter of N partial sums over the 32 lanes of a warp by halving
-// exchanges: for N >= 32 lane l ends with the sums of values l N/32 ..
-// (l+1) N/32 - 1 in v[0 ..]; for N < 32 every lane holds the sum of value
-// (lane * N) / 32 in v[0].
-template <int N>
-__device__ __forceinline__ void warp_reduce_scatter(float (&v)[N], int lane) {
-  int n = N;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const bool up = (lane & o) != 0;
-    if (n >= 2) {
-#pragma unroll
-      for (int i = 0; i < N / 2; ++i)
-        if (i < n / 2) {
-          const float send = up ? v[i] : v[i + n / 2];
-          const float keep = up ? v[i + n / 2] : v[i];
-          v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-      n >>= 1;
-    } else {
-      v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
-    }
-  }
-}
 
 // Exclusive scan of one int per thread over the CTA; *total gets the sum.
 __device__ __forceinline__ int block_excl_scan_i(int v, int* warp_sums, int* total) {
@@ -292,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   __shared__ int slot_e[kMaxSlots], cnt_s[kMaxSlots], soff_s[kMaxSlots];
   __shared__ int tok_s[kMaxSlots][kMaxT];
   __shared__ float ss_w[kWarps][kMaxT];
-  __shared__ float pr_w[kWarps][kMaxT * EPC];
+  __shared__ float rpart_s[kWarps][kMaxT][kRBoxE];   // router partial sums per warp
   __shared__ float x_s[kMaxT][kDn];
   __shared__ int nslots_s, flag_s, abort_s;
   __shared__ int scan_a[kWarps], scan_c[kWarps];
@@ -308,7 +302,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   const uint32_t sbase = smem_u32(smem);
   uint32_t* xw = reinterpret_cast<uint32_t*>(smem + L.xw);
   const uint16_t* wrs = reinterpret_cast<const uint16_t*>(smem + L.wr);
-  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.slab);   // xn bf16 [T][H] (ring buffer 1)
+  uint16_t* xb = reinterpret_cast<uint16_t*>(smem + L.slab);   // xn bf16 [T][H + 8] (ring buffer 1)
   const int upe = I / kGU;                     // gate/up units per slot
   const uint32_t dn_q = (uint32_t)kDn * (I / 2), dn_s = (uint32_t)kDn * GI * 2;
   const int e0 = cta * EPC;                    // this CTA's router columns [e0, e0 + EPC)
@@ -422,11 +416,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
 #pragma unroll
   for (int t = 0; t < kMaxT; ++t) rinv[t] = t < T ? rinv_s[t] : 0.f;
   DEC_TRACE2(2);
-  // xn = bf16(x * rinv): fp16 operand rows (perm8 K order); router partial
-  // sums over this thread's hidden indices
-  float pr[kMaxT * EPC];
-#pragma unroll
-  for (int q = 0; q < kMaxT * EPC; ++q) pr[q] = 0.f;
+  // xn = bf16(x * rinv): fp16 operand rows (perm8 K order), and bf16 rows for
+  // the router (router CTAs)
   uint32_t over = 0u;
 #pragma unroll
   for (int it = 0; it < 2; ++it) {
@@ -442,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       over |= bf16x2_f16_overflow(nb[0]) | bf16x2_f16_overflow(nb[1]) | bf16x2_f16_overflow(nb[2]) |
               bf16x2_f16_overflow(nb[3]);
       if (router_cta)   // xn rows as bf16 for the router (ring buffer 1, idle until routing)
-        *reinterpret_cast<uint4*>(xb + (size_t)t * H + 8 * pc) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
+        *reinterpret_cast<uint4*>(xb + (size_t)t * (H + 8) + 8 * pc) = make_uint4(nb[0], nb[1], nb[2], nb[3]);
       const uint4 o = f16x8_to_perm8(make_uint4(bf16x2_to_f16x2_sat(nb[0]), bf16x2_to_f16x2_sat(nb[1]),
                                                 bf16x2_to_f16x2_sat(nb[2]), bf16x2_to_f16x2_sat(nb[3])));
       // piece u = pc % 8 of its group of 64 goes to position 4 (u % 2) + u / 2,
@@ -455,57 +446,45 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   report_range_warp(p.err, over != 0u);
   DEC_TRACE2(3);
   if (router_cta) {
-    // router partials: thread tid takes hidden rows tid, tid + 256, ... so
-    // that a warp reads consecutive rows of the weight slice and of xn. The
-    // slice's copy (thousands of 16-byte rows) was issued at launch; the
-    // operand rows above were built while it landed.
+    // router logits of the 8 experts of this CTA's weight box on mma.sync:
+    // A = the bf16 token rows (rows 8 .. 15 of the tile hold no token), B = the
+    // box's 16-byte weight rows by ldmatrix.trans; warp w takes K in
+    // [w H/8, (w+1) H/8), FP32 accumulation. The slice's copy (thousands of
+    // 16-byte rows) was issued at launch; the operand rows above were built
+    // while it landed.
     if (!mbar_wait_drain(&wbar, 0, p.err.limit_ns)) {
       if (lane == 0) report_timeout(p.err, 44);
       abort_s = 1;
     }
     __syncthreads();
-    {
-#pragma unroll 8
-      for (int h = tid; h < H; h += kThreads) {
-        const uint16_t* wrow = wrs + (size_t)h * kRBoxE + ecol;
-        float wv[EPC];
-#pragma unroll
-        for (int q = 0; q < EPC / 2; ++q) {
-          const uint32_t w2 = reinterpret_cast<const uint32_t*>(wrow)[q];
-          wv[2 * q] = bf16_lo(w2);
-          wv[2 * q + 1] = bf16_hi(w2);
-        }
-#pragma unroll
-        for (int t = 0; t < kMaxT; ++t)
-          if (t < T) {
-            const float xv = bf16_to_f32(xb[(size_t)t * H + h]);
-#pragma unroll
-            for (int q = 0; q < EPC; ++q) pr[t * EPC + q] = fmaf(xv, wv[q], pr[t * EPC + q]);
-          }
-      }
+    const int kw = H / kWarps;
+    // lane l gives the row address of matrix l / 8: token l % 8 at K offset
+    // 8 (l / 8) (A), weight row 8 (l / 8) + l % 8 (B); token rows past T are
+    // stale and only feed product rows that are never read
+    const uint32_t xa = smem_u32(xb) + (uint32_t)(((lane & 7) * (H + 8) + 8 * (lane >> 3)) * 2);
+    const uint32_t wa = smem_u32(wrs) + (uint32_t)((8 * (lane >> 3) + (lane & 7)) * kRBoxE * 2);
+    float d[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int k0 = warp * kw; k0 < (warp + 1) * kw; k0 += 32) {
+      uint32_t av[4], bv[4];
+      ldsm4(xa + (uint32_t)k0 * 2, av);
+      ldsm4_t(wa + (uint32_t)k0 * kRBoxE * 2, bv);
+      mma_bf16_16816(d, av[0], 0u, av[1], 0u, bv[0], bv[1]);   // K k0 .. k0 + 15
+      mma_bf16_16816(d, av[2], 0u, av[3], 0u, bv[2], bv[3]);   // K k0 + 16 .. k0 + 31
     }
+    // D row g = token g, columns 2c and 2c + 1 = the box's experts
+    rpart_s[warp][g][2 * c] = d[0];
+    rpart_s[warp][g][2 * c + 1] = d[1];
   }
   DEC_TRACE2(4);
   // the zero token row (columns of a tile past its tokens)
   for (int i = tid; i < (int)L.xstride; i += kThreads) xw[kMaxT * L.xstride + i] = 0u;
-  if (router_cta) {
-    // the warp's sums of the kMaxT * EPC partials, scattered over its lanes
-    warp_reduce_scatter<kMaxT * EPC>(pr, lane);
-    constexpr int kN = kMaxT * EPC;
-    if (kN >= 32) {
-#pragma unroll
-      for (int i = 0; i < (kN >= 32 ? kN / 32 : 1); ++i) pr_w[warp][lane * (kN / 32) + i] = pr[i];
-    } else if ((lane & (32 / kN - 1)) == 0) {
-      pr_w[warp][(lane * kN) / 32] = pr[0];
-    }
-  }
   __syncthreads();
   DEC_TRACE2(5);
-  if (router_cta && tid < T * EPC) {
+  if (router_cta && tid < T * EPC) {   // the warps' partial sums in warp order
     const int t = tid / EPC, q = tid % EPC;
     float v = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) v += pr_w[w][t * EPC + q];
+    for (int w = 0; w < kWarps; ++w) v += rpart_s[w][t][ecol + q];
     const int e = e0 + q;
     if (e < E) p.logits[(size_t)t * E + e] = v + (p.rbias ? p.rbias[e] : 0.f);
   }
@@ -919,7 +898,7 @@ bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int nu
   if (E % dec::kRBoxE || E / dec::kRBoxE > num_sms) return false;
   const dec::Smem L = dec::smem_layout(H, I);
   if ((uint32_t)H * dec::kRBoxE * 2 > L.slab) return false;   // router slice in one ring buffer
-  if ((uint32_t)dec::kMaxT * H * 2 > L.slab) return false;     // bf16 token rows in another
+  if ((uint32_t)dec::kMaxT * (H + 8) * 2 > L.slab) return false;   // bf16 token rows in another
   const int slots = T * k + has_shared;
   if (slots > dec::kMaxSlots || (uint32_t)slots * dec::kDn * dec::kMaxT * 4 > L.dsum_cap) return false;
   if (L.total + 1024 > 227 * 1024) return false;
