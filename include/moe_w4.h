@@ -267,8 +267,8 @@ moe_status moe_residual_add(moe_plan_t plan, const uint16_t* x, const float* y, 
  * loads the library until the process exits; hence T <= 4096 and
  * num_experts <= 512, and larger requests return MOE_ERR_CAPACITY. Nothing
  * in that array needs clearing between calls. The first call on a device
- * looks up the array's device address (with that device current); make
- * that first call before any stream capture. All calls share the array:
+ * looks up the array's device address (a host-side runtime query, with that
+ * device current) and keeps it for later calls. All calls share the array:
  * calls that can overlap on the GPU (different streams without ordering)
  * race and must not be made.
  * A bounded wait of the routing kernels that runs out (1 s) leaves the

@@ -2,7 +2,7 @@
 against moe_route, through the C ABI.
 
 Callers that cannot call cudaMalloc -- code inside another framework's
-memory pool or capture region, allocator-less runtimes -- pass every output
+memory pool, allocator-less runtimes -- pass every output
 buffer themselves; the library's only scratch for this call is a fixed
 device array. The test allocates the output buffers (the entry point does
 not), runs two calls in a row with different inputs, and requires the same
