@@ -235,9 +235,11 @@ class ClockSampler:
 # ------------------------------------------------------------- the oracle
 
 
-def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers):
+def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers, min_seconds=0.0):
     """Oracle tokens/s of the whole stack, from `sample_tokens` rows through
-    `sample_layers` layers, scaled by sample_layers / layers."""
+    `sample_layers` layers (or, with min_seconds, through layers 0, 1, ...
+    until that much CPU time has been spent, at most sample_layers), scaled by
+    the layers done / layers. Returns (rate, seconds, layers done)."""
     import oracle
     from bit_grouped_gemm_gb300 import synth
     from tests import parity
@@ -245,7 +247,10 @@ def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers):
     xb = parity.bits(synth.tokens_x(w, "cpu")[:sample_tokens])
     orc = oracle.get()
     elapsed = 0.0
+    done = 0
     for li in range(sample_layers):
+        if min_seconds and done and elapsed >= min_seconds:
+            break
         L = layers_dev[li]
         wr = parity.bits(L.router_w)
         rb = None if L.router_bias is None else L.router_bias.cpu().numpy()
@@ -257,7 +262,8 @@ def oracle_sample_rate(w, layers_dev, threads, sample_tokens, sample_layers):
                            nthreads=threads)
         xb = orc.residual(xb, out["y"], 1.0 / math.sqrt(w.layers))
         elapsed += time.perf_counter() - t0
-    return sample_tokens * sample_layers / elapsed / w.layers, elapsed
+        done += 1
+    return sample_tokens * done / elapsed / w.layers, elapsed, done
 
 
 def workload(args):
@@ -408,8 +414,10 @@ def main(argv=None):
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         threads = os.cpu_count() or 1
-        st, sl = (min(T, 16 * threads), min(w.layers, 3))
-        rate, el = oracle_sample_rate(w, layers, threads, st, sl)
+        # layer after layer until ~12 s of CPU work (the sample stays bounded:
+        # 16 tokens per thread, at most the whole stack)
+        st = min(T, 16 * threads)
+        rate, el, sl = oracle_sample_rate(w, layers, threads, st, w.layers, min_seconds=12.0)
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "cpu_model": cpu_model(),
                "sample": f"{st} tokens x layers 0-{sl - 1} of the {T}-token {w.layers}-layer "
@@ -696,7 +704,7 @@ def run_reference(args, ws, rank):
         oracle_sample_rate(w, L0, threads, min(sample, threads), 1)
     tok, secs = 0, 0.0
     for _ in range(args.steps):
-        _, el = oracle_sample_rate(w, L0, threads, sample, 1)
+        _, el, _ = oracle_sample_rate(w, L0, threads, sample, 1)
         tok += sample
         secs += el
     value = tok / secs / w.layers
