@@ -17,8 +17,9 @@
 //   1. every CTA reads the residual rows x, computes their RMS norm and the
 //      normalised rows xn = bf16(x / rms(x)) (kept in shared memory as the
 //      fp16 MMA operand, in 16-byte pieces ordered for 128-bit fragment
-//      loads), and router CTA c computes the logits of its experts (router
-//      weight slice copied before the previous launch ends);
+//      loads), and router CTA c computes the logits of its experts on bf16
+//      mma.sync (its router weight slice is copied from before the launch
+//      waits on the previous one);
 //   -- barrier 1 (all logits written) --
 //   2. every CTA selects each token's top-k (the same warp top-k as the
 //      routing kernels, so every CTA holds the same routing) and numbers the
