@@ -219,22 +219,19 @@ def routing_pointers(plan, x, T, L):
     return bg.moe_route(plan, x, T, L.router_w, L.router_bias)
 
 
-@pytest.mark.parametrize("T", [1, 4, 8])
-def test_decode_fused_layer_chain(T):
+def fused_layer_chain(w, layers, alpha):
     """The fused decode layer (moe_forward_stack on a chunk of at most 8
     tokens: router, top-k, gate/up, down, combine and stack update in one
-    launch per layer) against the oracle over the 40-layer stack. At every
+    launch per layer) against the oracle over `layers` of the 40-layer stack
+    (alpha the stack's residual scale). At every
     layer the GPU runs that one layer on the oracle's residual rows; its
     routing must equal the oracle's (rows with the gap), its FP32 block output
     (kept in the plan's scratch) must be within 2e-2 * rms of the oracle's,
     and the updated rows must be bf16(x + y/sqrt(L)) of that output."""
-    w = synth.standard_workloads()[f"decode_t{T}_l40"]
     sh = w.shape
-    k, H = sh.top_k, sh.hidden
-    layers = stack.make_layers(w, "cuda")
+    T, k, H = w.tokens, sh.top_k, sh.hidden
     plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
                                            sh.group_size, int(sh.has_shared), T), 0)
-    alpha = stack.residual_alpha(w.layers)
     orc = oracle.get()
     try:
         x = synth.decode_pool(w, 1, "cuda")[0].contiguous()
@@ -265,10 +262,29 @@ def test_decode_fused_layer_chain(T):
                 np.abs(bits_f64(parity.bits(xn)) - bits_f64(orc.rmsnorm(parity.bits(x_chk))))
                 <= parity.bf16_ulp(bits_f64(orc.rmsnorm(parity.bits(x_chk)))) + 1e-30), li
             xo = orc.residual(xo, o["y"], alpha)
-        assert compared >= 0.9 * T * w.layers
+        assert compared >= 0.9 * T * len(layers)
         assert bg.moe_get_error(plan) == 0
     finally:
         bg.moe_plan_destroy(plan)
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+def test_decode_fused_layer_chain(T):
+    """The chain above over the whole 40-layer stack at the benchmark's batch
+    sizes."""
+    w = synth.standard_workloads()[f"decode_t{T}_l40"]
+    fused_layer_chain(w, stack.make_layers(w, "cuda"), stack.residual_alpha(w.layers))
+
+
+@pytest.mark.parametrize("T", [2, 3, 5, 7])
+def test_decode_fused_layer_chain_other_sizes(T):
+    """The same chain over the first 6 layers of the stack at batch sizes the
+    benchmark skips: 2, and odd token counts, where a slot's last pair of
+    MMA columns holds one token."""
+    w = dataclasses.replace(synth.standard_workloads()["decode_t8_l40"], name=f"decode_t{T}_l40",
+                            tokens=T)
+    fused_layer_chain(w, [stack.make_layer(w, li, "cuda") for li in range(6)],
+                      stack.residual_alpha(w.layers))
 
 
 @pytest.mark.parametrize("T", [1, 8])
