@@ -12,15 +12,17 @@
 // The general path runs a decode layer as four dependent launches (routing,
 // gate/up, down, combine), each paying a launch boundary and one or two
 // dependent round trips through L2. Here one persistent CTA per SM does the
-// whole layer, with two grid barriers (arrival counter in device memory,
-// bounded waits):
+// whole layer, with one grid barrier (arrival counter in device memory,
+// bounded waits) and one hand-off through tagged values:
 //   1. every CTA reads the residual rows x, computes their RMS norm and the
 //      normalised rows xn = bf16(x / rms(x)) (kept in shared memory as the
 //      fp16 MMA operand, in 16-byte pieces ordered for 128-bit fragment
 //      loads), and router CTA c computes the logits of its experts on bf16
 //      mma.sync (its router weight slice is copied from before the launch
 //      waits on the previous one);
-//   -- barrier 1 (all logits written) --
+//   -- each logit is written with the launch's number in the high half of a
+//      64-bit word; a top-k warp reads its token's row (one entry per lane
+//      first, then all) until every entry carries this launch's number --
 //   2. every CTA selects each token's top-k (the same warp top-k as the
 //      routing kernels, so every CTA holds the same routing) and numbers the
 //      active experts in ascending order: slot 0 the shared expert, then one
@@ -33,7 +35,7 @@
 //      weights the tensor-core GEMM rebuilds) and runs mma.sync with FP32
 //      accumulation, SwiGLU in FP32 registers, activations stored as fp16
 //      rows per (slot, token); no block barrier per unit;
-//   -- barrier 2 (all activations written) --
+//   -- grid barrier (all activations written) --
 //   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
 //      those 16 down rows (copied while it waits at barrier 2) by the slot's
 //      activation rows, then forms
@@ -77,7 +79,8 @@ struct Params {
   CUtensorMap mg, mu, msg, msu;   // gate/up packed words, 3D boxes (32 words, 8 rows, K/256)
   CUtensorMap md, msd;             // down packed words, 3D boxes (32 words, 16 rows, K/256)
   CUtensorMap mr;            // router weight bf16 [H][E], boxes of 8 experts x 256 rows
-  float* logits;             // [T][E]
+  unsigned* epoch;           // launches of this layer kernel so far on the plan
+  unsigned long long* tlog;  // [T][E] router logits, tag epoch + 1 in the high word
   uint16_t* act;             // [rows][I] fp16, K order perm8 (row = slot offset + token)
   int32_t* topk_idx;         // [T][k] (written by CTA 0)
   float* topk_w;             // [T][k]
@@ -363,6 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   DEC_TRACE(1);
   pdl_begin();   // x and everything below come from the previous launch
   DEC_TRACE(2);
+  const unsigned ep = __ldcg(p.epoch);   // set by the previous launch's last CTA
+  bool ok = true;
 
   // ------------------------------------------- 1. norms, operand rows, router
   for (int e = tid; e < E; e += kThreads) tmask_s[e] = 0u;
@@ -487,20 +492,54 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) v += rpart_s[w][t][ecol + q];
     const int e = e0 + q;
-    if (e < E) p.logits[(size_t)t * E + e] = v + (p.rbias ? p.rbias[e] : 0.f);
+    // one 64-bit store: the value and this launch's tag land together
+    if (e < E)
+      p.tlog[(size_t)t * E + e] = ((unsigned long long)(ep + 1u) << 32) |
+                                  __float_as_uint(v + (p.rbias ? p.rbias[e] : 0.f));
   }
 
   DEC_TRACE(3);
-  bool ok = grid_barrier(p.bar, (unsigned)ncta, p.err, 40, &flag_s);
+  // (no grid barrier here: each top-k warp polls its token's logits until
+  // every one carries this launch's tag)
+  __syncthreads();
   DEC_TRACE(4);
-  if (!ok || abort_s) goto drain;
+  if (abort_s) goto drain;
 
   // ------------------------------------------------------- 2. top-k, slots
   if (warp < T) {
-    int idx;
-    float w;
-    topk_warp<VPL>(p.logits + (size_t)warp * E, E, k, idx, w);
-    if (lane < k) {
+    // this token's logits, re-read (bounded) until all carry tag ep + 1
+    float lv[VPL];
+    const unsigned long long* lrow = p.tlog + (size_t)warp * E;
+    const unsigned long long tw0 = globaltimer_ns();
+    bool ready;
+    {   // first one entry per lane (a 256-byte read per warp), until tagged
+      const int e = lane + 32 * (VPL - 1) < E ? lane + 32 * (VPL - 1) : lane;
+      while (!__all_sync(0xffffffffu, (unsigned)(__ldcg(lrow + e) >> 32) == ep + 1u) &&
+             globaltimer_ns() - tw0 <= p.err.limit_ns)
+        __nanosleep(64);
+    }
+    for (;;) {
+      bool mine = true;
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) {
+        const int e = lane + 32 * i;
+        const unsigned long long v = e < E ? __ldcg(lrow + e) : ((unsigned long long)(ep + 1u) << 32);
+        mine &= (unsigned)(v >> 32) == ep + 1u;
+        lv[i] = e < E ? __uint_as_float((unsigned)v) : -INFINITY;
+      }
+      if ((ready = __all_sync(0xffffffffu, mine))) break;
+      if (globaltimer_ns() - tw0 > p.err.limit_ns) break;
+      __nanosleep(32);
+    }
+    int idx = 0;
+    float w = 0.f;
+    if (ready) {
+      topk_select<VPL>(lv, E, k, idx, w);
+    } else {
+      if (lane == 0) report_timeout(p.err, 40);
+      abort_s = 1;
+    }
+    if (ready && lane < k) {
       idx_s[warp][lane] = idx;
       w_s[warp][lane] = w;
       atomicOr(&tmask_s[idx], 1u << warp);
@@ -511,6 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     }
   }
   __syncthreads();
+  if (abort_s) goto drain;
   DEC_TRACE2(6);
   {
     // slots: 0 = shared (if any), then the selected experts in ascending
@@ -714,7 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   // the first down chunks are issued while thread 0 takes barrier 2 (every
   // warp's unit buffer, the whole ring, has been read at its first sync),
   // one chunk per issuing thread: lane 0 of warps 4 .. 7 takes chunk warp - 4
-  ok = grid_barrier(p.bar, 2u * ncta, p.err, 42, &flag_s, [&] {
+  ok = grid_barrier(p.bar, (unsigned)ncta, p.err, 42, &flag_s, [&] {
     const int b = warp - (kWarps - kRing);
     if (lane == 0 && b >= 0 && b < n_dc && !abort_s) {
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -850,10 +890,14 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
       if (p.y_out) p.y_out[(size_t)t * H + h] = y;
     }
   }
-  // the last CTA to leave sets the counter back to 0 for the next launch
   __syncthreads();
   DEC_TRACE(8);
-  if (tid == 0 && atomicAdd(p.bar, 1u) == 3u * ncta - 1u) *p.bar = 0u;
+  // the last CTA to leave sets the counter back to 0 and advances the launch
+  // count (the next launch's logits tag)
+  if (tid == 0 && atomicAdd(p.bar, 1u) == 2u * ncta - 1u) {
+    *p.bar = 0u;
+    *p.epoch = ep + 1u;
+  }
   return;
 
 drain:
@@ -945,7 +989,8 @@ cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sm
   p.msu = a.maps[4];
   p.msd = a.maps[5];
   p.mr = a.router_map;
-  p.logits = a.logits;
+  p.epoch = a.epoch;
+  p.tlog = a.tlogits;
   p.act = a.act;
   p.topk_idx = a.topk_idx;
   p.topk_w = a.topk_w;

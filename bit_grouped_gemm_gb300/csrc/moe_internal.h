@@ -171,12 +171,13 @@ struct DecodeLayerArgs {
   CUtensorMap maps[6];           // gate, up, down, shared gate, up, down (encode_slab_3d:
                                  // 8-row boxes for gate/up, 16 for down)
   CUtensorMap router_map;        // router weight, encode_router_slices
-  float* logits;                 // [T][E] scratch
   uint16_t* act;                 // [T*k + T][I] fp16 scratch
   int32_t* topk_idx;             // [T][k] routing of the layer (outputs)
   float* topk_w;
   float* y_out;                  // [T][H] FP32 block output, or null
   unsigned* bar;                 // grid-barrier counter, 0 between launches
+  unsigned* epoch;               // launches of the fused layer so far (the logits' tag - 1)
+  unsigned long long* tlogits;   // [T][E] logits with the launch's tag in the high word
 };
 bool decode_fused_fits(int T, int H, int I, int E, int k, int has_shared, int num_sms);
 cudaError_t launch_decode_layer(const DecodeLayerArgs& a, DevErr err, int num_sms, cudaStream_t st);

@@ -27,9 +27,15 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
   size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
-      bmap2, num_tiles2, err, arrive, xs, act, d, dsh, total;
+      bmap2, num_tiles2, err, arrive, tlogits, xs, act, d, dsh, total;
   int nblk_max, max_tiles, max_tiles2, rows_cap;
 };
+
+// The fused decode layer's router logits tagged with its launch count
+// (at most 8 tokens).
+size_t tlogits_bytes(const moe_plan_desc& d) {
+  return (size_t)(d.max_tokens < 8 ? d.max_tokens : 8) * d.num_experts * 8;
+}
 
 Layout make_layout(const moe_plan_desc& d) {
   Layout L;
@@ -59,7 +65,8 @@ Layout make_layout(const moe_plan_desc& d) {
   L.bmap2 = take((size_t)L.max_tiles2 * 3 * 4);
   L.num_tiles2 = take(16);
   L.err = take(16);
-  L.arrive = take(16);
+  L.arrive = take(16);   // route_large arrivals and generation, fused-layer barrier, launch count
+  L.tlogits = take(tlogits_bytes(d));
   L.xs = take((size_t)L.rows_cap * d.hidden * 2);
   L.act = take((size_t)L.rows_cap * d.inter * 2);
   L.d = take(Tm * k * d.hidden * 2);
@@ -373,12 +380,13 @@ moe_status decode_layer_impl(moe_plan* p, uint16_t* x, int T, const moe_layer& L
             p->qmap3(&a.maps[5], sh.down.qweight, er * H, I, 16) &&
             p->rmap(&a.router_map, Ly.router_w, H, E);
   if (!ok) return MOE_ERR_CUDA;
-  a.logits = p->at<float>(p->L.logits);
   a.act = p->at<uint16_t>(p->L.act);
   a.topk_idx = p->at<int32_t>(p->L.topk_idx);
   a.topk_w = p->at<float>(p->L.topk_w);
   a.y_out = d.has_shared ? p->at<float>(p->L.dsh) : nullptr;
   a.bar = p->at<unsigned>(p->L.arrive) + 2;
+  a.epoch = p->at<unsigned>(p->L.arrive) + 3;
+  a.tlogits = p->at<unsigned long long>(p->L.tlogits);
   p->last_path = 3;
   return st_of(timed(p, 9, st, [&] { return launch_decode_layer(a, p->err(), p->num_sms, st); }));
 }
@@ -627,6 +635,7 @@ moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* ou
   }
   cudaMemset(p->scratch + p->L.err, 0, 16);
   cudaMemset(p->scratch + p->L.arrive, 0, 16);
+  cudaMemset(p->scratch + p->L.tlogits, 0, tlogits_bytes(*desc));
   bool ok = true;
   for (int i = 0; i < 4 && ok; ++i) {
     const uint32_t box_rows = 128u >> i;
@@ -789,8 +798,11 @@ moe_status moe_get_error(moe_plan_t p) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e == cudaSuccess) e = cudaMemcpy(h, p->at<int>(p->L.err), 8, cudaMemcpyDeviceToHost);
   if (e == cudaSuccess) e = cudaMemset(p->at<int>(p->L.err), 0, 8);
-  // a launch that gave up at a barrier leaves its arrival counters set
+  // a launch that gave up at a barrier leaves its arrival counters set, and
+  // the fused layer's launch count and tagged logits may disagree
   if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT)) e = cudaMemset(p->at<int>(p->L.arrive), 0, 16);
+  if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT))
+    e = cudaMemset(p->scratch + p->L.tlogits, 0, tlogits_bytes(p->d));
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaSetDevice(prev);
   if (e != cudaSuccess) return MOE_ERR_CUDA;

@@ -25,15 +25,16 @@ __device__ __forceinline__ float key_value(uint32_t k) {
 // One token's selection by one warp, from its logits row (read through L2:
 // the row may have been written by other CTAs of the same launch). Lane j < k
 // gets the j-th selected expert and its renormalised softmax weight.
+// The warp's top-k of one row of E values, given as lane + 32 i -> lv[i]
+// (entries past E ignored).
 template <int VPL>   // values per lane, E <= 32 * VPL
-__device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k,
-                                          int& idx, float& w) {
+__device__ __forceinline__ void topk_select(const float (&lv)[VPL], int E, int k, int& idx,
+                                            float& w) {
   const int lane = threadIdx.x & 31;
   uint32_t key[VPL];
 #pragma unroll
   for (int i = 0; i < VPL; ++i) {
-    const int e = lane + 32 * i;
-    const float l = e < E ? __ldcg(row + e) : -INFINITY;
+    const float l = lv[i];
     key[i] = order_key(isnan(l) ? -INFINITY : l + 0.0f);   // + 0 turns -0 into +0
   }
   uint32_t live = 0;   // bit i: lane's value i not selected yet and e < E
@@ -68,6 +69,19 @@ __device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, 
   }
   idx = my_idx;
   w = my_val / zsum;
+}
+
+template <int VPL>   // values per lane, E <= 32 * VPL
+__device__ __forceinline__ void topk_warp(const float* __restrict__ row, int E, int k,
+                                          int& idx, float& w) {
+  const int lane = threadIdx.x & 31;
+  float lv[VPL];
+#pragma unroll
+  for (int i = 0; i < VPL; ++i) {
+    const int e = lane + 32 * i;
+    lv[i] = e < E ? __ldcg(row + e) : -INFINITY;
+  }
+  topk_select<VPL>(lv, E, k, idx, w);
 }
 
 }  // namespace moe
