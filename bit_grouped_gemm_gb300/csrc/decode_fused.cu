@@ -119,6 +119,13 @@ __host__ __device__ inline Smem smem_layout(int H, int I) {
   return L;
 }
 
+// A relaxed load that the compiler must issue every time (polling loops).
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -514,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
     bool ready;
     {   // first one entry per lane (a 256-byte read per warp), until tagged
       const int e = lane + 32 * (VPL - 1) < E ? lane + 32 * (VPL - 1) : lane;
-      while (!__all_sync(0xffffffffu, (unsigned)(__ldcg(lrow + e) >> 32) == ep + 1u) &&
+      while (!__all_sync(0xffffffffu, (unsigned)(ld_relaxed_u64(lrow + e) >> 32) == ep + 1u) &&
              globaltimer_ns() - tw0 <= p.err.limit_ns)
         __nanosleep(64);
     }
@@ -523,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
 #pragma unroll
       for (int i = 0; i < VPL; ++i) {
         const int e = lane + 32 * i;
-        const unsigned long long v = e < E ? __ldcg(lrow + e) : ((unsigned long long)(ep + 1u) << 32);
+        const unsigned long long v = e < E ? ld_relaxed_u64(lrow + e) : ((unsigned long long)(ep + 1u) << 32);
         mine &= (unsigned)(v >> 32) == ep + 1u;
         lv[i] = e < E ? __uint_as_float((unsigned)v) : -INFINITY;
       }
