@@ -287,6 +287,41 @@ def test_decode_fused_layer_chain_other_sizes(T):
                       stack.residual_alpha(w.layers))
 
 
+def test_decode_fused_after_timeout_reset():
+    """A bounded wait that runs out latches MOE_ERR_DEVICE_TIMEOUT; clearing it
+    also resets the fused decode layer's launch count and its launch-tagged
+    router logits, so the fused steps that follow give the bits they gave
+    before the error (and no stale logits are taken for new ones)."""
+    w = synth.standard_workloads()["decode_t4_l40"]
+    sh = w.shape
+    layers = [stack.make_layer(w, li, "cuda") for li in range(3)]
+    plan = bg.moe_plan_create(bg.plan_desc(sh.hidden, sh.inter, sh.num_experts, sh.top_k,
+                                           sh.group_size, int(sh.has_shared), w.tokens), 0)
+    alpha = stack.residual_alpha(w.layers)
+    try:
+        x0 = synth.decode_pool(w, 1, "cuda")[0].contiguous()
+        xn = torch.empty_like(x0)
+        arr = bg.moe_layers(layers)
+
+        def two_steps():
+            x = x0.clone()
+            bg.moe_forward_stack(plan, x, xn, w.tokens, arr, alpha)
+            bg.moe_forward_stack(plan, x, xn, w.tokens, arr, alpha)
+            torch.cuda.synchronize()
+            return x.view(torch.int16).cpu().numpy()
+
+        a = two_steps()
+        assert bg.moe_last_gemm_path(plan) == 3
+        assert bg.moe_get_error(plan) == 0
+        bg.moe_debug_wait_timeout(plan, 20000)      # 20 ms limit, never satisfied
+        assert bg.moe_get_error(plan) == 5          # MOE_ERR_DEVICE_TIMEOUT, cleared
+        b = two_steps()
+        assert bg.moe_get_error(plan) == 0
+        assert np.array_equal(a, b)
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
 @pytest.mark.parametrize("T", [1, 8])
 def test_decode_fused_stack_matches_layer_by_layer(T):
     """One moe_forward_stack call over the 40 layers (the launch sequence the
