@@ -37,7 +37,7 @@
 //      rows per (slot, token); no block barrier per unit;
 //   -- grid barrier (all activations written) --
 //   4. CTA c < H/16 owns 16 output columns: for every slot it multiplies
-//      those 16 down rows (copied while it waits at barrier 2) by the slot's
+//      those 16 down rows (copied while it waits at the barrier) by the slot's
 //      activation rows, then forms
 //          y[t] = shared[t] + sum_j w[t][j] * expert_j[t]   (FP32, j in rank order)
 //      and updates x[t] = bf16(x[t] + alpha * y[t]) in place.
@@ -133,7 +133,7 @@ __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
 }
 
 #ifdef MOE_DEC_TRACE
-// Profiling build only: %globaltimer inside the two grid barriers of every CTA
+// Profiling build only: %globaltimer inside the grid barriers of every CTA
 // (after the first sync, the fence, the arrival, the wait, the last sync).
 __device__ unsigned long long g_dec_btrace[256][2][5];
 #define DEC_BTRACE(i) \
@@ -346,10 +346,11 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   __syncthreads();
 
   // The ring of down slabs: chunk i (kSlotsPerChunk slots' 16 down rows) goes
-  // to buffer i % kRing once the gate/up units are done with the ring; one
-  // elected thread issues its copies when the buffer is free.
+  // to buffer i % kRing once the gate/up units are done with the ring: the
+  // first kRing chunks from one thread each during the grid barrier, later
+  // ones from kIssuer as buffers free up.
   int n_units = 0, n_dc = 0;             // set once the routing is known
-  int issued = 0;                        // chunks issued so far (kIssuer), a prefix
+  int issued = 0;                        // 1 + the last chunk this thread issued
   auto ring_buf = [](int i) { return i % kRing; };
   auto issue = [&](int i) {
     const int b = ring_buf(i);
@@ -758,9 +759,10 @@ __global__ void __launch_bounds__(kThreads, 1) moe_decode_layer_kernel(const __g
   }
 
   DEC_TRACE(6);
-  // the first down chunks are issued while thread 0 takes barrier 2 (every
-  // warp's unit buffer, the whole ring, has been read at its first sync),
-  // one chunk per issuing thread: lane 0 of warps 4 .. 7 takes chunk warp - 4
+  // the first down chunks are issued while thread 0 waits in the grid
+  // barrier (every warp's unit buffer, the whole ring, has been read at its
+  // first sync), one chunk per issuing thread: lane 0 of warps 4 .. 7 takes
+  // chunk warp - 4
   ok = grid_barrier(p.bar, (unsigned)ncta, p.err, 42, &flag_s, [&] {
     const int b = warp - (kWarps - kRing);
     if (lane == 0 && b >= 0 && b < n_dc && !abort_s) {
