@@ -9,5 +9,6 @@ from .binding import (KERNEL_KINDS, MoeError, MoeExperts, MoeLayer, MoePlanDesc,
                       experts, load_library, moe_debug_wait_timeout, moe_enable_timing, moe_debug_buffer,
                       moe_forward_layer, moe_forward_stack, moe_layers, moe_get_error, moe_grouped_w4_ffn, moe_last_gemm_path,
                       moe_plan_create, moe_plan_destroy, moe_plan_scratch_bytes,
-                      moe_read_timing, moe_residual_add, moe_route, moe_route_noalloc, moe_status_string,
+                      moe_read_timing, moe_residual_add, moe_route, moe_route_noalloc, moe_set_tail_split,
+                      moe_status_string,
                       moe_version, plan_desc)

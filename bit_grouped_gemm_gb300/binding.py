@@ -94,6 +94,7 @@ def load_library(path: Optional[str] = None):
         "moe_get_error": (S, [P]),
         "moe_debug_wait_timeout": (S, [P, I, P]),
         "moe_enable_timing": (S, [P, I]),
+        "moe_set_tail_split": (S, [P, I]),
         "moe_read_timing": (S, [P, ctypes.POINTER(MoeTiming)]),
         "moe_last_gemm_path": (I, [P]),
         "moe_debug_buffer": (P, [P, I]),
@@ -260,6 +261,10 @@ def moe_read_timing(plan: int) -> dict:
     t = MoeTiming()
     _check(load_library().moe_read_timing(plan, ctypes.byref(t)), "moe_read_timing")
     return {k: (t.ms[i], int(t.launches[i])) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def moe_set_tail_split(plan: int, on: bool) -> None:
+    _check(load_library().moe_set_tail_split(plan, int(bool(on))), "moe_set_tail_split")
 
 
 def moe_last_gemm_path(plan: int) -> int:

@@ -30,7 +30,13 @@
 //     alternate 32-token groups, read the accumulators back with tcgen05.ld
 //     and apply SwiGLU (gate/up) or the top-k weight (down);
 //   * persistent CTAs (one per SM, 512 TMEM columns each) walk the units;
-//     the number of units is read from device memory, never from the host.
+//     the number of units is read from device memory, never from the host;
+//   * the last, partial round of units is split along K when it would leave
+//     at least half the SMs idle: each of its units goes to two CTAs, one K
+//     half each, which write their fp32 partial sums to device memory; the
+//     CTA that arrives second at the unit's counter copies the other half's
+//     sums into shared memory, adds them to its own (the same bits whichever
+//     CTA that is) and runs the epilogue.
 // Every wait is bounded: on timeout the CTA latches an error, drains its own
 // TMA copies and MMAs, frees TMEM and exits.
 #include "moe_common.cuh"
@@ -68,7 +74,92 @@ struct Params {
   int out_ld;
   const float* topk_w;
   const int32_t* perm;
+  float* sk_ws;         // split last round: fp32 partials, one slot per CTA
+  unsigned* sk_cnt;     // split last round: arrivals per unit (zero between launches)
+  int sk_slots;         // slots in sk_ws (0: no split)
   DevErr err;
+};
+
+// One slot of split partial sums: [weight block][token][row] fp32.
+constexpr int kSlotFloats = 2 * kBM * 128;
+static_assert(kSlotFloats * 4 == (int)kSplitSlotBytes, "split slot size");
+
+// A CTA's k-th work item: unit u, 256-K weight stages [q0, q1), piece `piece`
+// of `pieces`. The full rounds deal whole units (unit k * grid + CTA); in the
+// last round r units are left for the grid's G CTAs, and when r <= G / 2 each
+// is cut into 2 pieces (K halves), piece i of unit t on CTA 2 t + i. Two
+// pieces make the sum order-free: fp32 addition is commutative, so the unit
+// gets the same bits whichever piece's CTA adds them.
+struct Item {
+  int u, q0, q1, piece, pieces;
+};
+
+__device__ __forceinline__ int tail_pieces(const Params& p, int r, int nq) {
+  const int G = gridDim.x;
+  if (r == 0 || G > p.sk_slots) return 1;
+  return G / r >= 2 && nq >= 2 ? 2 : 1;
+}
+
+__device__ __forceinline__ bool item_at(const Params& p, int k, int units, int nq, Item& it) {
+  const int G = gridDim.x, b = blockIdx.x, R = units / G, r = units - R * G;
+  if (k < R) {
+    it = {k * G + b, 0, nq, 0, 1};
+    return true;
+  }
+  if (k > R || r == 0) return false;
+  const int s = tail_pieces(p, r, nq);
+  if (b >= r * s) return false;
+  const int t = b / s, i = b - t * s;
+  it = {R * G + t, i * nq / s, (i + 1) * nq / s, i, s};
+  return true;
+}
+
+// A CTA's walk over its work items, the same in every role. Without the
+// split: units blockIdx.x, blockIdx.x + grid, ..., each over all K; with
+// it: the items of item_at.
+template <bool kSplit>
+struct Deal;
+
+template <>
+struct Deal<false> {
+  int u, units, nq;
+  __device__ __forceinline__ Deal(const Params&, int units_, int nq_) : u(blockIdx.x), units(units_), nq(nq_) {}
+  __device__ __forceinline__ bool valid() const { return u < units; }
+  __device__ __forceinline__ int unit() const { return u; }
+  __device__ __forceinline__ int q_begin() const { return 0; }
+  __device__ __forceinline__ int q_end() const { return nq; }
+  __device__ __forceinline__ int pieces() const { return 1; }
+  __device__ __forceinline__ int next_unit() const { return u + (int)gridDim.x; }   // may be >= units
+  __device__ __forceinline__ bool has_next() const { return u + (int)gridDim.x < units; }
+  __device__ __forceinline__ int next_q_begin() const { return 0; }
+  __device__ __forceinline__ void advance() { u += gridDim.x; }
+};
+
+template <>
+struct Deal<true> {
+  const Params& p;
+  int units, nq, k;
+  Item cur, nxt;
+  bool has, hn;
+  __device__ __forceinline__ Deal(const Params& p_, int units_, int nq_)
+      : p(p_), units(units_), nq(nq_), k(0) {
+    has = item_at(p, 0, units, nq, cur);
+    hn = has && item_at(p, 1, units, nq, nxt);
+  }
+  __device__ __forceinline__ bool valid() const { return has; }
+  __device__ __forceinline__ int unit() const { return has ? cur.u : units; }
+  __device__ __forceinline__ int q_begin() const { return cur.q0; }
+  __device__ __forceinline__ int q_end() const { return cur.q1; }
+  __device__ __forceinline__ int pieces() const { return cur.pieces; }
+  __device__ __forceinline__ int next_unit() const { return hn ? nxt.u : units; }
+  __device__ __forceinline__ bool has_next() const { return hn; }
+  __device__ __forceinline__ int next_q_begin() const { return hn ? nxt.q0 : 0; }
+  __device__ __forceinline__ void advance() {
+    cur = nxt;
+    has = hn;
+    ++k;
+    hn = has && item_at(p, k + 1, units, nq, nxt);
+  }
 };
 
 struct Unit {
@@ -146,6 +237,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return ok;
 }
 
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_constant__ Params p) {
   pdl_begin();
   extern __shared__ uint8_t smem_raw[];
@@ -162,8 +254,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   uint64_t* acc_full = a_full + kAStages;
   uint64_t* acc_empty = acc_full + 1;
   uint64_t* drain = acc_empty + 1;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* sk_bar = drain + 1;   // split: the other piece's partials landed
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sk_bar + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* sk_last = reinterpret_cast<volatile int*>(tmem_slot + 2);   // split: this CTA reduces
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -182,6 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     mbar_init(acc_full, 1);
     mbar_init(acc_empty, 8);
     mbar_init(drain, 1);
+    if constexpr (kSplit) mbar_init(sk_bar, 1);
     *abort_flag = 0;
     fence_mbar_init();
     for (int i = 0; i < 4; ++i) tma_prefetch_desc(&p.maps.b[i]);
@@ -212,19 +307,21 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
   const int units = (n_routed + n_shared) * p.nblk;
   const int nchunk = p.K / 64;
   const int kgroups = p.K / 64;
+  const int nq = nchunk / 4;   // 256-K weight stages per unit
 
   if (warp == 0) {
     // ------------------------------------------ TMA producer: activations
     uint32_t bcnt = 0;
     bool ok = true;
-    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit U = make_unit(p, u, n_routed, nxt);
-      nxt = fetch_unit(p, u + gridDim.x, n_routed);
+    Deal<kSplit> d(p, units, nq);
+    UnitRaw nxt = fetch_unit(p, d.unit(), n_routed);
+    for (; d.valid() && ok; d.advance()) {
+      const Unit U = make_unit(p, d.unit(), n_routed, nxt);
+      nxt = fetch_unit(p, d.next_unit(), n_routed);
       // smallest box covering the tile's rows: fewer bytes for small groups
       const int bi = U.rows > 64 ? 0 : U.rows > 32 ? 1 : U.rows > 16 ? 2 : 3;
       const uint32_t bytes = (uint32_t)kBTileBytes >> bi;
-      for (int c = 0; c < nchunk && ok; ++c) {
+      for (int c = 4 * d.q_begin(); c < 4 * d.q_end() && ok; ++c) {
         const int s = bcnt % kBStages;
         if (!(ok = warp_wait(&b_empty[s], ((bcnt / kBStages) & 1) ^ 1, abort_flag, p.err, 2, 32 * p.mode)))
           break;
@@ -248,15 +345,16 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // (its own warp, so weight tiles run ahead of the activation ring)
     uint32_t qcnt = 0;
     bool ok = true;
-    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      const Unit U = make_unit(p, u, n_routed, nxt);
-      nxt = fetch_unit(p, u + gridDim.x, n_routed);
+    Deal<kSplit> d(p, units, nq);
+    UnitRaw nxt = fetch_unit(p, d.unit(), n_routed);
+    for (; d.valid() && ok; d.advance()) {
+      const Unit U = make_unit(p, d.unit(), n_routed, nxt);
+      nxt = fetch_unit(p, d.next_unit(), n_routed);
       const int y0 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 0);
       const int y1 = (U.shared ? 0 : U.e * p.N) + block_row0(p, U.j, 1);
       const CUtensorMap* m0 = U.shared ? &p.maps.sq0 : &p.maps.q0;
       const CUtensorMap* m1 = U.shared ? &p.maps.sq1 : &p.maps.q1;
-      for (int qc = 0; qc < nchunk / 4 && ok; ++qc) {
+      for (int qc = d.q_begin(); qc < d.q_end() && ok; ++qc) {
         const int s = qcnt % kQStages;
         if (!(ok = warp_wait(&q_empty[s], ((qcnt / kQStages) & 1) ^ 1, abort_flag, p.err, 1, 32 * p.mode)))
           break;
@@ -279,17 +377,19 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // ------------------------------------------------------ MMA issuer
     // The whole warp runs the loop and takes the waits; one elected lane
     // issues the MMAs and the commits that track them.
-    uint32_t bcnt = 0, acnt = 0, it = 0;
+    uint32_t bcnt = 0, acnt = 0, itn = 0;
     bool ok = true;
-    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-      const Unit U = make_unit(p, u, n_routed, nxt);
-      nxt = fetch_unit(p, u + gridDim.x, n_routed);
+    Deal<kSplit> d(p, units, nq);
+    UnitRaw nxt = fetch_unit(p, d.unit(), n_routed);
+    for (; d.valid() && ok; d.advance(), ++itn) {
+      const Unit U = make_unit(p, d.unit(), n_routed, nxt);
+      nxt = fetch_unit(p, d.next_unit(), n_routed);
       const int ntok = (U.rows + 15) & ~15;
       const uint32_t idesc = idesc_f16_f32(128, ntok);
-      if (!(ok = warp_wait(acc_empty, (it & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
+      if (!(ok = warp_wait(acc_empty, (itn & 1) ^ 1, abort_flag, p.err, 3, 32 * p.mode))) break;
       tc_fence_after();
-      for (int c = 0; c < nchunk; ++c) {
+      const int c_first = 4 * d.q_begin();
+      for (int c = c_first; c < 4 * d.q_end(); ++c) {
         const int bs = bcnt % kBStages, as = acnt % kAStages;
         // a_full also covers the activation chunk (the forwarder saw it land)
         if (!(ok = warp_wait(&a_full[as], (acnt / kAStages) & 1, abort_flag, p.err, 5, 32 * p.mode))) break;
@@ -300,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = smem_desc_sw128(bbase + 32 * kk);
             const uint32_t a0 = tmem + kAStageCol + 64 * as + 8 * kk;
-            const uint32_t acc = (c | kk) != 0;
+            const uint32_t acc = kSplit ? (uint32_t)((c != c_first) | (kk != 0)) : (uint32_t)((c | kk) != 0);
             mma_f16_ts(tmem + kAccCol0, a0, bd, idesc, acc);
             mma_f16_ts(tmem + kAccCol1, a0 + 32, bd, idesc, acc);
           }
@@ -328,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     // so an early arrival can never count toward the previous phase.
     uint32_t cnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      for (int c = 0; c < nchunk; ++c, ++cnt) {
+    for (Deal<kSplit> d(p, units, nq); d.valid() && ok; d.advance()) {
+      for (int c = 4 * d.q_begin(); c < 4 * d.q_end(); ++c, ++cnt) {
         if (!(ok = warp_wait(&b_full[cnt % kBStages], (cnt / kBStages) & 1, abort_flag, p.err, 4,
                              32 * p.mode)))
           break;
@@ -360,26 +460,26 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     };
     const uint16_t *srow = nullptr, *brow = nullptr;
     uint2 s4 = make_uint2(0u, 0u), b4 = make_uint2(0u, 0u);
-    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
-    if ((int)blockIdx.x < units) {
-      sb_rows(make_unit(p, blockIdx.x, n_routed, nxt), srow, brow);
-      s4 = __ldg(reinterpret_cast<const uint2*>(srow));
-      b4 = __ldg(reinterpret_cast<const uint2*>(brow));
+    Deal<kSplit> d(p, units, nq);
+    UnitRaw nxt = fetch_unit(p, d.unit(), n_routed);
+    if (d.valid()) {
+      sb_rows(make_unit(p, d.unit(), n_routed, nxt), srow, brow);
+      s4 = __ldg(reinterpret_cast<const uint2*>(srow + 4 * d.q_begin()));
+      b4 = __ldg(reinterpret_cast<const uint2*>(brow + 4 * d.q_begin()));
     }
-    const int nq = nchunk / 4;
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x) {
-      nxt = fetch_unit(p, u + gridDim.x, n_routed);
+    for (; d.valid() && ok; d.advance()) {
+      nxt = fetch_unit(p, d.next_unit(), n_routed);
       const uint16_t *nsrow = nullptr, *nbrow = nullptr;
-      for (int qc = 0; qc < nq && ok; ++qc) {
+      for (int qc = d.q_begin(); qc < d.q_end() && ok; ++qc) {
         // scales/biases of the next 4 groups, one step ahead (also across units)
         uint2 s4n = s4, b4n = b4;
-        if (qc + 1 < nq) {
+        if (qc + 1 < d.q_end()) {
           s4n = __ldg(reinterpret_cast<const uint2*>(srow + 4 * (qc + 1)));
           b4n = __ldg(reinterpret_cast<const uint2*>(brow + 4 * (qc + 1)));
-        } else if (u + (int)gridDim.x < units) {
-          sb_rows(make_unit(p, u + gridDim.x, n_routed, nxt), nsrow, nbrow);
-          s4n = __ldg(reinterpret_cast<const uint2*>(nsrow));
-          b4n = __ldg(reinterpret_cast<const uint2*>(nbrow));
+        } else if (d.has_next()) {
+          sb_rows(make_unit(p, d.next_unit(), n_routed, nxt), nsrow, nbrow);
+          s4n = __ldg(reinterpret_cast<const uint2*>(nsrow + 4 * d.next_q_begin()));
+          b4n = __ldg(reinterpret_cast<const uint2*>(nbrow + 4 * d.next_q_begin()));
         }
         const int qs = qcnt % kQStages;
         if (!(ok = warp_wait(&q_full[qs], (qcnt / kQStages) & 1, abort_flag, p.err, 6, 32 * p.mode))) break;
@@ -462,12 +562,65 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
     const uint32_t lane_base = static_cast<uint32_t>(32 * quarter) << 16;
     float* s_w = reinterpret_cast<float*>(smem + kOffW) + 128 * (warp - 12);   // this warp's copy
     uint16_t* s_x = reinterpret_cast<uint16_t*>(smem + kOffX) + 1024 * (warp - 12);  // 32 x 32 fp16
-    uint32_t it = 0;
+    // Output of one 32-token group: v0/v1 hold the two weight blocks' sums
+    // (fp32 bits) of this lane's row for tokens c0 .. c0 + nval - 1.
+    auto emit = [&](const Unit& U, int c0, int nval, const uint32_t (&v0)[32], const uint32_t (&v1)[32]) {
+      // Lane l holds output column 32 * quarter + l for 32 consecutive
+      // tokens, so one register stored by the whole warp writes 32 adjacent
+      // columns of one token row: 64 (or 128) contiguous bytes.
+      if (p.mode == 0) {
+        // act = silu(gate) * up in fp16, columns in perm8 order. The 32 x 32
+        // block goes through shared memory so that each lane stores 16-byte
+        // pieces of token rows (measured faster here than one 2-byte store
+        // per element).
+        uint16_t* t16 = s_x;
+        const int col = perm8_pos(lane);
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          t16[cc * 32 + col] = f32_to_f16_sat(silu_fast(__uint_as_float(v0[cc])) *
+                                              __uint_as_float(v1[cc]));
+        __syncwarp();
+        uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + 32 * quarter;
+#pragma unroll
+        for (int it4 = 0; it4 < 4; ++it4) {
+          const int cc = it4 * 8 + (lane >> 2), seg = lane & 3;
+          if (cc < nval)
+            *reinterpret_cast<uint4*>(o + (size_t)cc * p.out_ld + 8 * seg) =
+                *reinterpret_cast<const uint4*>(t16 + cc * 32 + 8 * seg);
+        }
+        __syncwarp();
+      } else if (U.shared) {
+        // shared expert (weight 1): kept in fp32, it is as large as the output
+        float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          if (cc < nval) {
+            o[(size_t)cc * p.out_ld] = __uint_as_float(v0[cc]);
+            o[(size_t)cc * p.out_ld + 128] = __uint_as_float(v1[cc]);
+          }
+      } else {
+        // routed expert: weighted by its top-k weight, bf16
+        uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          if (cc < nval) {
+            const float w = s_w[(c0 + cc) & 127];
+            o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * w);
+            o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * w);
+          }
+      }
+    };
+    // this CTA's piece of the split last round, if it has one (always its
+    // last item)
+    Item tl;
+    const bool split = kSplit && item_at(p, units / (int)gridDim.x, units, nq, tl) && tl.pieces > 1;
+    uint32_t itn = 0;
     bool ok = true;
-    UnitRaw nxt = fetch_unit(p, blockIdx.x, n_routed);
-    for (int u = blockIdx.x; u < units && ok; u += gridDim.x, ++it) {
-      const Unit U = make_unit(p, u, n_routed, nxt);
-      nxt = fetch_unit(p, u + gridDim.x, n_routed);
+    Deal<kSplit> d(p, units, nq);
+    UnitRaw nxt = fetch_unit(p, d.unit(), n_routed);
+    for (; d.valid() && ok; d.advance(), ++itn) {
+      const Unit U = make_unit(p, d.unit(), n_routed, nxt);
+      nxt = fetch_unit(p, d.next_unit(), n_routed);
       if (p.mode == 1 && !U.shared) {
         // top-k weights of the tile's rows, fetched while the MMAs still run
 #pragma unroll
@@ -477,7 +630,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         }
         __syncwarp();
       }
-      if (!(ok = warp_wait(acc_full, it & 1, abort_flag, p.err, 8, 32 * p.mode))) break;
+      if (!(ok = warp_wait(acc_full, itn & 1, abort_flag, p.err, 8, 32 * p.mode))) break;
       tc_fence_after();
       if (32 * part >= U.rows) {
         // no group for this warp in this unit
@@ -497,52 +650,84 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
           if (lane == 0) mbar_arrive_relaxed(acc_empty);
         }
         const int nval = min(32, U.rows - c0);
-        // Lane l holds output column 32 * quarter + l for 32 consecutive
-        // tokens, so one register stored by the whole warp writes 32 adjacent
-        // columns of one token row: 64 (or 128) contiguous bytes.
-        if (p.mode == 0) {
-          // act = silu(gate) * up in fp16, columns in perm8 order. The 32 x 32
-          // block goes through shared memory so that each lane stores 16-byte
-          // pieces of token rows (measured faster here than one 2-byte store
-          // per element).
-          uint16_t* t16 = s_x;
-          const int col = perm8_pos(lane);
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc)
-            t16[cc * 32 + col] = f32_to_f16_sat(silu_fast(__uint_as_float(v0[cc])) *
-                                                __uint_as_float(v1[cc]));
-          __syncwarp();
-          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 128 * U.j + 32 * quarter;
-#pragma unroll
-          for (int it4 = 0; it4 < 4; ++it4) {
-            const int cc = it4 * 8 + (lane >> 2), seg = lane & 3;
-            if (cc < nval)
-              *reinterpret_cast<uint4*>(o + (size_t)cc * p.out_ld + 8 * seg) =
-                  *reinterpret_cast<const uint4*>(t16 + cc * 32 + 8 * seg);
-          }
-          __syncwarp();
-        } else if (U.shared) {
-          // shared expert (weight 1): kept in fp32, it is as large as the output
-          float* o = p.out_sh + (size_t)(U.m0 - p.T * p.k + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
+        if (kSplit && d.pieces() > 1) {
+          // a piece of a split unit: its partial sums, [block][token][row]
+          float* slot = p.sk_ws + (size_t)blockIdx.x * kSlotFloats + 32 * quarter + lane;
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc)
             if (cc < nval) {
-              o[(size_t)cc * p.out_ld] = __uint_as_float(v0[cc]);
-              o[(size_t)cc * p.out_ld + 128] = __uint_as_float(v1[cc]);
+              slot[(size_t)(c0 + cc) * 128] = __uint_as_float(v0[cc]);
+              slot[(size_t)(kBM + c0 + cc) * 128] = __uint_as_float(v1[cc]);
             }
         } else {
-          // routed expert: weighted by its top-k weight, bf16
-          uint16_t* o = p.out + (size_t)(U.m0 + c0) * p.out_ld + 256 * U.j + 32 * quarter + lane;
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc)
-            if (cc < nval) {
-              const float w = s_w[(c0 + cc) & 127];
-              o[(size_t)cc * p.out_ld] = f32_to_bf16(__uint_as_float(v0[cc]) * w);
-              o[(size_t)cc * p.out_ld + 128] = f32_to_bf16(__uint_as_float(v1[cc]) * w);
-            }
+          emit(U, c0, nval, v0, v1);
         }
       }
       __syncwarp();
+    }
+    if constexpr (kSplit) if (split) {
+      // Every epilogue warp comes here, whatever its waits gave, so that
+      // both named barriers complete. The CTA arrives at its unit's counter
+      // (release: every thread's fence, then one atomic) unless it gave up;
+      // the CTA whose arrival is the last adds the pieces' partials in piece
+      // order and writes the unit's output, then clears the counter for the
+      // next launch.
+      __threadfence();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const int t = tl.u - (units / (int)gridDim.x) * (int)gridDim.x;
+      if (warp == 12 && lane == 0) {
+        int last = 0;
+        if (!*abort_flag) {
+          const unsigned old = atomicAdd(p.sk_cnt + t, 1u);
+          if (old == (unsigned)tl.pieces - 1u) {
+            last = 1;
+            __threadfence();
+            p.sk_cnt[t] = 0u;
+          }
+        }
+        *sk_last = last;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (*sk_last) {
+        // the other piece's partials (block 0 and block 1, [token][row]) into
+        // the operand buffers, which the unit's finished MMAs no longer read;
+        // this piece's own sums are still in the accumulators
+        const Unit U = make_unit(p, tl.u, n_routed, fetch_unit(p, tl.u, n_routed));
+        float* o0 = reinterpret_cast<float*>(smem + kOffB);
+        float* o1 = reinterpret_cast<float*>(smem + kOffQ);
+        const uint32_t bytes = (uint32_t)U.rows * 128u * 4u;
+        if (warp == 12 && lane == 0) {
+          const float* src = p.sk_ws + (size_t)(2 * t + (tl.piece ^ 1)) * kSlotFloats;
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          mbar_arrive_expect_tx(sk_bar, 2 * bytes);
+          bulk_load(o0, src, bytes, sk_bar);
+          bulk_load(o1, src + kBM * 128, bytes, sk_bar);
+        }
+        bool got = mbar_wait(sk_bar, 0, abort_flag, p.err.limit_ns);
+        got = __all_sync(0xffffffffu, got);
+        if (!got) {
+          if (lane == 0) report_timeout(p.err, 11);
+          *abort_flag = 1;
+          // the copies land before shared memory is released
+          if (warp == 12 && lane == 0) mbar_wait_drain(sk_bar, 0, p.err.limit_ns);
+        } else {
+          for (int c0 = 32 * part; c0 < U.rows; c0 += 64) {
+            const int nval = min(32, U.rows - c0);
+            uint32_t v0[32], v1[32];
+            tmem_ld_32x32b_x32(tmem + lane_base + kAccCol0 + c0, v0);
+            tmem_ld_32x32b_x32(tmem + lane_base + kAccCol1 + c0, v1);
+            tmem_wait_ld();
+            const int row = 32 * quarter + lane;
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc)
+              if (cc < nval) {
+                v0[cc] = __float_as_uint(__uint_as_float(v0[cc]) + o0[(c0 + cc) * 128 + row]);
+                v1[cc] = __float_as_uint(__uint_as_float(v1[cc]) + o1[(c0 + cc) * 128 + row]);
+              }
+            emit(U, c0, nval, v0, v1);
+          }
+        }
+      }
     }
   }
 
@@ -588,14 +773,19 @@ cudaError_t launch_gemm_tc(int mode, const GemmProblem& g, const TcMaps& maps, D
   p.out_ld = g.out_ld;
   p.topk_w = g.topk_w;
   p.perm = g.perm;
+  p.sk_ws = g.sk_ws;
+  p.sk_cnt = g.sk_cnt;
+  p.sk_slots = g.sk_ws && g.sk_cnt ? g.sk_slots : 0;
   p.err = err;
   const int max_units = (g.max_routed_tiles + (g.has_shared ? (g.T + kBM - 1) / kBM : 0)) * p.nblk;
   int grid = num_sms < max_units ? num_sms : max_units;
   if (grid < 1) grid = 1;
-  cudaError_t e = cudaFuncSetAttribute(tc::w4_grouped_gemm_tc,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
+  // the split last round only when the plan asks for it and the grid has a
+  // slot per CTA; otherwise the kernel without it
+  auto kern = p.sk_slots >= grid ? tc::w4_grouped_gemm_tc<true> : tc::w4_grouped_gemm_tc<false>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, tc::kSmemBytes);
   if (e != cudaSuccess) return e;
-  return launch_pdl(tc::w4_grouped_gemm_tc, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, st, p);
+  return launch_pdl(kern, dim3(grid), dim3(tc::kThreads), tc::kSmemBytes, st, p);
 }
 
 #ifdef MOE_TC_STATS

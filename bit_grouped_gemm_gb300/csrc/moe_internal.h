@@ -122,7 +122,16 @@ struct GemmProblem {
   W4Dev next, snext;        // small-M gate/up only: the down matrices (routed, shared),
                             // whose rows each unit prefetches into L2 (q null: none)
   int next_K;               // reduction size of the down matrices (I)
+  float* sk_ws;             // tensor-core path: fp32 partials of the split last round,
+                            // kSplitSlotBytes per slot (null: no split)
+  unsigned* sk_cnt;         // one arrival counter per slot, zero between launches
+  int sk_slots;             // slots of sk_ws and sk_cnt
 };
+
+// Split last round of the tensor-core GEMM: one slot per CTA of
+// 2 weight blocks x 128 tokens x 128 rows fp32.
+constexpr int kSplitSlots = 192;
+constexpr size_t kSplitSlotBytes = 2u * 128u * 128u * 4u;
 
 // tcgen05 tensor-core path. `maps` holds the encoded tensor maps the kernel
 // needs (B operand, routed q for w0/w1, shared q for sw0/sw1).

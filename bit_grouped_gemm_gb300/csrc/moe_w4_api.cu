@@ -27,7 +27,7 @@ size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 struct Layout {                 // byte offsets into the scratch allocation
   size_t topk_idx, topk_w, logits, blk_cnt, cnt8, cnt, off, tile_off, num_tiles, perm, inv, bmap,
-      bmap2, num_tiles2, err, arrive, tlogits, xs, act, d, dsh, total;
+      bmap2, num_tiles2, err, arrive, tlogits, sk_cnt, sk_ws, xs, act, d, dsh, total;
   int nblk_max, max_tiles, max_tiles2, rows_cap;
 };
 
@@ -67,6 +67,8 @@ Layout make_layout(const moe_plan_desc& d) {
   L.err = take(16);
   L.arrive = take(16);   // route_large arrivals and generation, fused-layer barrier, launch count
   L.tlogits = take(tlogits_bytes(d));
+  L.sk_cnt = take(kSplitSlots * 4);
+  L.sk_ws = take((size_t)kSplitSlots * kSplitSlotBytes);
   L.xs = take((size_t)L.rows_cap * d.hidden * 2);
   L.act = take((size_t)L.rows_cap * d.inter * 2);
   L.d = take(Tm * k * d.hidden * 2);
@@ -112,6 +114,7 @@ struct moe_plan {
   std::vector<TimedLaunch> timed;
   std::vector<cudaEvent_t> ev_pool;
   int last_path = 0;
+  bool tail_split = false;   // tensor-core path: split the last round of units along K
   // encoded uint32 [rows][cols] maps of packed weights, by (base, rows, cols,
   // box rows): a layer's maps are encoded on its first call only
   std::map<std::tuple<const void*, uint64_t, uint64_t, uint32_t>, CUtensorMap> qmaps;
@@ -434,6 +437,11 @@ moe_status ffn_impl(moe_plan* p, const uint16_t* x, int T, const moe_routing* r,
   g.max_routed_tiles = (int)bound;
   g.topk_w = r->topk_w;
   g.perm = r->perm;
+  if (p->tail_split) {
+    g.sk_ws = p->at<float>(p->L.sk_ws);
+    g.sk_cnt = p->at<unsigned>(p->L.sk_cnt);
+    g.sk_slots = kSplitSlots;
+  }
 
   // gate/up: B = xs [rows][H], out = act [rows][I]
   GemmProblem g0 = g;
@@ -636,6 +644,7 @@ moe_status moe_plan_create(const moe_plan_desc* desc, int device, moe_plan_t* ou
   cudaMemset(p->scratch + p->L.err, 0, 16);
   cudaMemset(p->scratch + p->L.arrive, 0, 16);
   cudaMemset(p->scratch + p->L.tlogits, 0, tlogits_bytes(*desc));
+  cudaMemset(p->scratch + p->L.sk_cnt, 0, kSplitSlots * 4);
   bool ok = true;
   for (int i = 0; i < 4 && ok; ++i) {
     const uint32_t box_rows = 128u >> i;
@@ -803,6 +812,9 @@ moe_status moe_get_error(moe_plan_t p) {
   if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT)) e = cudaMemset(p->at<int>(p->L.arrive), 0, 16);
   if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT))
     e = cudaMemset(p->scratch + p->L.tlogits, 0, tlogits_bytes(p->d));
+  // so may the split last round's counters of a GEMM that gave up
+  if (e == cudaSuccess && (h[0] & DEVERR_TIMEOUT_BIT))
+    e = cudaMemset(p->scratch + p->L.sk_cnt, 0, kSplitSlots * 4);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   cudaSetDevice(prev);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
@@ -816,6 +828,12 @@ moe_status moe_debug_wait_timeout(moe_plan_t p, int limit_us, moe_stream_t strea
   DevErr e = p->err();
   e.limit_ns = (unsigned long long)limit_us * 1000ull;
   return st_of(launch_debug_wait(e, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+moe_status moe_set_tail_split(moe_plan_t p, int on) {
+  if (!p) return MOE_ERR_INVALID_ARG;
+  p->tail_split = on != 0;
+  return MOE_OK;
 }
 
 moe_status moe_enable_timing(moe_plan_t p, int on) {

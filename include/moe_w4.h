@@ -330,6 +330,23 @@ void* moe_debug_buffer(moe_plan_t plan, int which);
  * fused decode layer of moe_forward_stack, 4 tensor-core on SM pairs. */
 int moe_last_gemm_path(moe_plan_t plan);
 
+/* Load balance of the tensor-core path for expert groups of very different
+ * sizes (the grouped GEMM of section "Las optimizaciones en el prefill"
+ * runs over groups whose sizes vary by expert); on = 1, off = 0 (the
+ * default). Units (one
+ * 128-token tile x one weight block pair) are dealt in rounds over the SMs,
+ * and when the last round holds at most half as many units as SMs, each of
+ * its units is cut along K into two halves on different SMs, whose fp32
+ * partial sums the SM that finishes second adds (one addition, the same
+ * bits whichever SM that is: the result is the same on every run).
+ * A token's output then depends, in its last bits, on whether its tile fell
+ * into the last round. Off, every tile is summed over K in one pass, so a
+ * prompt run in chunks gives the bits of one pass. Off by default: on the
+ * 2048- and 4096-token workloads the split measured slower (the halves'
+ * partial sums cost more than the idle SMs of the last round). Host only;
+ * takes effect from the next call. */
+moe_status moe_set_tail_split(moe_plan_t plan, int on);
+
 /* Text of a status code. */
 const char* moe_status_string(moe_status s);
 

@@ -85,6 +85,7 @@ def test_null_arguments_rejected(lib):
                                           None) == 1
     assert lib.moe_forward_stack(None, None, None, 1, None, 1, 0.0, None) == 1
     assert lib.moe_get_error(None) == 1
+    assert lib.moe_set_tail_split(None, 1) == 1
 
 
 def test_noalloc_host_checks(lib):

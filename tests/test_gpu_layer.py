@@ -156,6 +156,55 @@ def test_layer_parity_all_rows(name):
         bg.moe_plan_destroy(plan2)
 
 
+def last_round_pieces(num_tiles: int, T: int, sh, num_sms: int):
+    """How the tensor-core GEMM deals the last round of units, per pass
+    (gate/up, down): units = (routed tiles + shared tiles) x weight blocks;
+    the grid is min(SMs, the host's unit bound); r units are left after the
+    full rounds, each cut into two K halves when r <= grid / 2."""
+    sh_tiles = -(-T // 128) if sh.has_shared else 0
+    bound = min(-(-T * sh.top_k // 128) + sh.num_experts, T * sh.top_k)
+    out = []
+    for nblk, K in ((sh.inter // 128, sh.hidden), (sh.hidden // 256, sh.inter)):
+        units = (num_tiles + sh_tiles) * nblk
+        G = max(1, min(num_sms, (bound + sh_tiles) * nblk))
+        r = units % G
+        out.append(2 if r and G // r >= 2 and K // 256 >= 2 else 1)
+    return out
+
+
+@pytest.mark.parametrize("name", ["t2048_zipf", "prefill_t4096_l40_zipf"])
+def test_split_last_round(name):
+    """The split of the GEMM's last round of units (each left-over unit summed
+    over two K halves on two SMs, which the second to finish adds): the
+    workload's own routing is checked to split the gate/up pass, every output
+    row with the split on and off is compared with the oracle, and two runs
+    with the split give the same bits (the SM that adds the halves changes
+    from run to run; their sum does not)."""
+    w = WL[name]
+    sh = w.shape
+    c = Case(w)
+    plan = make_plan(w)
+    try:
+        r = bg.moe_route(plan, c.x, w.tokens, c.L.router_w, c.L.router_bias)
+        g = parity.routing_to_numpy(r, w.tokens, sh.top_k, sh.num_experts)
+        sms = torch.cuda.get_device_properties(0).multi_processor_count
+        pieces = last_round_pieces(int(g["num_tiles"]), w.tokens, sh, sms)
+        assert pieces[0] > 1, pieces
+        bg.moe_set_tail_split(plan, True)
+        y1 = run_layer(c, plan).clone()
+        y2 = run_layer(c, plan).clone()
+        assert np.array_equal(y1.cpu().numpy(), y2.cpu().numpy())
+        bg.moe_set_tail_split(plan, False)
+        y0 = run_layer(c, plan)
+        assert bg.moe_last_gemm_path(plan) == 1
+        orc = c.oracle_layer()
+        parity.check_y(y1.double().cpu().numpy(), orc["y"])
+        parity.check_y(y0.double().cpu().numpy(), orc["y"])
+        assert not np.array_equal(y1.cpu().numpy(), y0.cpu().numpy())   # the split ran
+    finally:
+        bg.moe_plan_destroy(plan)
+
+
 def _tie_bias(kind: str, E: int) -> np.ndarray:
     """Router biases that make every token's logits exactly these values
     (the router weight is zero): ties, signed zeros and NaNs."""
