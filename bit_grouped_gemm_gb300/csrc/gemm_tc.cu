@@ -669,9 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       // Every epilogue warp comes here, whatever its waits gave, so that
       // both named barriers complete. The CTA arrives at its unit's counter
       // (release: every thread's fence, then one atomic) unless it gave up;
-      // the CTA whose arrival is the last adds the pieces' partials in piece
-      // order and writes the unit's output, then clears the counter for the
-      // next launch.
+      // the CTA that arrives second clears the counter for the next launch,
+      // adds the other half's partial sums to its own and writes the unit's
+      // output.
       __threadfence();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const int t = tl.u - (units / (int)gridDim.x) * (int)gridDim.x;
