@@ -31,8 +31,9 @@
 //     and apply SwiGLU (gate/up) or the top-k weight (down);
 //   * persistent CTAs (one per SM, 512 TMEM columns each) walk the units;
 //     the number of units is read from device memory, never from the host;
-//   * the last, partial round of units is split along K when it would leave
-//     at least half the SMs idle: each of its units goes to two CTAs, one K
+//   * optionally (the kSplit instantiation, which the plan selects), the
+//     last, partial round of units is split along K when it would leave at
+//     least half the SMs idle: each of its units goes to two CTAs, one K
 //     half each, which write their fp32 partial sums to device memory; the
 //     CTA that arrives second at the unit's counter copies the other half's
 //     sums into shared memory, adds them to its own (the same bits whichever
@@ -665,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       }
       __syncwarp();
     }
-    if constexpr (kSplit) if (split) {
+    if (kSplit && split) {
       // Every epilogue warp comes here, whatever its waits gave, so that
       // both named barriers complete. The CTA arrives at its unit's counter
       // (release: every thread's fence, then one atomic) unless it gave up;
