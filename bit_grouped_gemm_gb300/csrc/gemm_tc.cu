@@ -673,6 +673,9 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
       // the CTA that arrives second clears the counter for the next launch,
       // adds the other half's partial sums to its own and writes the unit's
       // output.
+      // (the proxy fence: the partials are read back by a bulk copy, the
+      // async proxy)
+      asm volatile("fence.proxy.async.global;" ::: "memory");
       __threadfence();
       asm volatile("bar.sync 1, 256;" ::: "memory");
       const int t = tl.u - (units / (int)gridDim.x) * (int)gridDim.x;
@@ -699,7 +702,10 @@ __global__ void __launch_bounds__(kThreads, 1) w4_grouped_gemm_tc(const __grid_c
         const uint32_t bytes = (uint32_t)U.rows * 128u * 4u;
         if (warp == 12 && lane == 0) {
           const float* src = p.sk_ws + (size_t)(2 * t + (tl.piece ^ 1)) * kSlotFloats;
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          // generic-proxy accesses before the bulk copy: the other CTA's
+          // stores of the partials (global), this CTA's reads of the
+          // buffers (shared)
+          asm volatile("fence.proxy.async;" ::: "memory");
           mbar_arrive_expect_tx(sk_bar, 2 * bytes);
           bulk_load(o0, src, bytes, sk_bar);
           bulk_load(o1, src + kBM * 128, bytes, sk_bar);
