@@ -172,15 +172,18 @@ def last_round_pieces(num_tiles: int, T: int, sh, num_sms: int):
     return out
 
 
-@pytest.mark.parametrize("name", ["t2048_zipf", "prefill_t4096_l40_zipf"])
-def test_split_last_round(name):
+@pytest.mark.parametrize("name,tokens", [("t2048_zipf", 0), ("prefill_t4096_l40_zipf", 0),
+                                         ("t2048_zipf", 700)])
+def test_split_last_round(name, tokens):
     """The split of the GEMM's last round of units (each left-over unit summed
     over two K halves on two SMs, which the second to finish adds): the
     workload's own routing is checked to split the gate/up pass, every output
     row with the split on and off is compared with the oracle, and two runs
     with the split give the same bits (the SM that adds the halves changes
-    from run to run; their sum does not)."""
-    w = WL[name]
+    from run to run; their sum does not). At 700 tokens both passes split and
+    the last units, always in the split round, are the shared expert's
+    partial tile of 60 rows."""
+    w = WL[name] if not tokens else dataclasses.replace(WL[name], tokens=tokens)
     sh = w.shape
     c = Case(w)
     plan = make_plan(w)
@@ -190,6 +193,8 @@ def test_split_last_round(name):
         sms = torch.cuda.get_device_properties(0).multi_processor_count
         pieces = last_round_pieces(int(g["num_tiles"]), w.tokens, sh, sms)
         assert pieces[0] > 1, pieces
+        if w.tokens % 128:
+            assert pieces[1] > 1, pieces
         bg.moe_set_tail_split(plan, True)
         y1 = run_layer(c, plan).clone()
         y2 = run_layer(c, plan).clone()
